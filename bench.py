@@ -1,0 +1,358 @@
+"""Benchmark of the tiled GEMM library on one GB300 (or N replicas).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+One step = one C = A . B product of the workload (default: bf16 4096^3 with fp32
+output), inputs already resident in device memory.  Before every timed step a
+256 MiB buffer is written to flush the 129 MB L2; each step is timed with CUDA
+events on the launching stream around the single library call, and `value`
+is the FLOP rate over the sum of the K step times (max over ranks).
+
+`e2e` measures the same product through the same C ABI call with host
+buffers: per step, pinned host -> device copies of A and B, the call, and the
+device -> host copy of C, all inside the event-timed region.
+
+`--impl reference` times the CPU oracle (the plain fp64 triple loop) on a
+bounded sample of rows of the same workload; it is a deliberately slow
+baseline, not a competitor.
+
+Multi-GPU: the product has no exchange step, so N ranks run N independent
+replicas of the workload (weak scaling) with no collective on the data path;
+the barrier and the max over ranks are the only cross-rank operations.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as wl  # noqa: E402
+
+FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "tc_gemm_bf16_4096x4096x4096_f32out.md")
+KERNEL_SOURCES = [os.path.join(ROOT, "tiled_dense_gemm_02_gb300", "csrc", f) for f in ("tc_gemm.cu", "ptx.cuh")]
+
+
+def _build_library():
+    """Build libtgemm.so if stale, through the standalone build script."""
+    import importlib.util
+    path = os.path.join(ROOT, "tiled_dense_gemm_02_gb300", "build.py")
+    spec = importlib.util.spec_from_file_location("tgemm_build", path)
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod.build()
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=50)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--workload", default=wl.HEADLINE.name, choices=sorted(wl.BY_NAME))
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU work of the oracle sample")
+    return p.parse_args()
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for p in KERNEL_SOURCES:
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel source; else None."""
+    if workload != wl.HEADLINE.name or not os.path.exists(PROFILE_TRAFFIC):
+        return None
+    text = open(PROFILE_TRAFFIC).read()
+    m_bytes = re.search(r"dram_bytes_per_launch:\s*([0-9]+)", text)
+    m_hash = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
+    if not m_bytes or not m_hash or m_hash.group(1) != kernel_source_hash():
+        return None
+    return int(m_bytes.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi sampling (200 ms) while the timed region runs."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        time.sleep(0.3)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.3)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None, "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def cpu_oracle_sample(w: wl.Workload, A, B, target_seconds: float, rows: int | None = None):
+    """Time the oracle (as it stands, all host cores) on the first `rows` rows of
+    the product; `rows` is chosen to take about `target_seconds` when None."""
+    import oracle
+    fin = wl.IN_FORMAT[w.dtype]
+    threads = os.cpu_count() or 1
+    if rows is None:
+        probe = max(1, min(w.M, threads))
+        t0 = time.perf_counter()
+        oracle.gemm(np.ascontiguousarray(A[:probe]), B, fin, probe, w.N, w.K, threads=threads, with_abs=False)
+        per_row = (time.perf_counter() - t0) / probe
+        rows = int(max(probe, min(w.M, target_seconds / max(per_row, 1e-9))))
+        rows = max(threads, rows // threads * threads) if rows >= threads else rows
+    t0 = time.perf_counter()
+    oracle.gemm(np.ascontiguousarray(A[:rows]), B, fin, rows, w.N, w.K, threads=threads, with_abs=False)
+    dt = time.perf_counter() - t0
+    tflops = 2.0 * rows * w.N * w.K / dt / 1e12
+    return {"value": tflops, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": f"rows 0..{rows - 1} of the {w.M}x{w.N}x{w.K} product ({rows * w.N} outputs, "
+                      f"{dt:.2f} s, fp64 triple loop over the rounded inputs, rows split across threads)"}
+
+
+def run_reference(args, w: wl.Workload):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    A, B = wl.make_inputs(w)
+    threads = os.cpu_count() or 1
+    rows = max(threads, 2 * threads)
+    for _ in range(args.warmup):
+        cpu_oracle_sample(w, A, B, 0, rows=rows)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        cpu_oracle_sample(w, A, B, 0, rows=rows)
+        times.append(time.perf_counter() - t0)
+    per_step = sum(times) / len(times)
+    value = 2.0 * rows * w.N * w.K / per_step / 1e12
+    line = {
+        "impl": "reference", "metric": "GEMM TFLOP/s", "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_step * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K,
+                   "sample_rows_per_step": rows},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": f"{rows} rows of the {w.M}x{w.N}x{w.K} product per step"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, w: wl.Workload):
+    import torch
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+
+    _build_library()
+    import tiled_dense_gemm_02_gb300 as tg
+
+    fin, fout = wl.IN_FORMAT[w.dtype], wl.OUT_FORMAT[w.dtype]
+    A, B = wl.make_inputs(w)
+    tdt = {"f32": torch.int32, "f16": torch.int16, "bf16": torch.int16}
+    np_view = {"f32": np.int32, "f16": np.int16, "bf16": np.int16}
+    a_host = torch.from_numpy(A.view(np_view[fin])).pin_memory()
+    b_host = torch.from_numpy(B.view(np_view[fin])).pin_memory()
+    c_host = torch.empty((w.M, w.N), dtype=tdt[fout]).pin_memory()
+    a = a_host.to(dev)
+    b = b_host.to(dev)
+    c = torch.empty((w.M, w.N), dtype=tdt[fout], device=dev)
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sptr = stream.cuda_stream
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    st, plan = tg.plan(w.M, w.N, w.K, a.data_ptr(), w.K, b.data_ptr(), w.N, c.data_ptr(), w.N, w.dtype, None, sms)
+    assert st == tg.OK, tg.status_string(st)
+
+    def call():
+        s = tg.gemm(w.M, w.N, w.K, a.data_ptr(), w.K, b.data_ptr(), w.N, c.data_ptr(), w.N, w.dtype, sptr)
+        if s != tg.OK:
+            raise RuntimeError(tg.status_string(s))
+
+    for _ in range(max(args.warmup, 3)):
+        flush.fill_(1)
+        call()
+    torch.cuda.synchronize(dev)
+    assert tg.device_status(sptr) == tg.OK
+
+    # ------------------------------------------------------------- timed region
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    sampler.start()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.fill_(i)                  # evict A, B, C from L2 (outside the event pair)
+        starts[i].record(stream)
+        call()
+        ends[i].record(stream)
+    torch.cuda.synchronize(dev)
+    wall = time.perf_counter() - wall0
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop()
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    total_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    assert tg.device_status(sptr) == tg.OK
+    ms_per_step = total_ms / args.steps
+    value = world * w.flops * args.steps / (total_ms / 1e3) / 1e12
+
+    # ------------------------------------------------------------- end to end
+    e2e_steps = max(3, min(args.steps, 20))
+    e_s = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps)]
+    e_e = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps)]
+    for i in range(e2e_steps + 2):
+        j = i - 2
+        if j >= 0:
+            e_s[j].record(stream)
+        a.copy_(a_host, non_blocking=True)
+        b.copy_(b_host, non_blocking=True)
+        call()
+        c_host.copy_(c, non_blocking=True)
+        if j >= 0:
+            e_e[j].record(stream)
+        torch.cuda.synchronize(dev)
+    e2e_ms = sum(s.elapsed_time(e) for s, e in zip(e_s, e_e)) / e2e_steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = world * w.flops / (e2e_ms / 1e3) / 1e12
+
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
+
+    peaks, peak_src = load_peaks()
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    if w.dtype == wl.F32:
+        roofline = None   # the fp32 SIMT path is bound by the FP32 pipe; reported by the fp32 workloads' notes
+    else:
+        achieved = w.flops / (ms_per_step / 1e3) / 1e12
+        roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                    "frac": achieved / peak, "traffic": profiled_traffic(w.name),
+                    "peak_source": f"{peak_src} bf16_tflops (burst; kernel timed alone)",
+                    "algorithmic_flops_per_launch": w.flops,
+                    "compulsory_bytes_per_launch": w.compulsory_bytes}
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        cpu = cpu_oracle_sample(w, A, B, args.cpu_seconds)
+    line = {
+        "metric": "GEMM TFLOP/s", "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": fin, "data": "synthetic",
+        "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "in": fin, "out": fout, "accumulate": "f32",
+                   "l2": "flushed before every timed step (256 MiB write)", "parallelism": f"replicas{world}",
+                   "kernel": plan.as_dict(), "sms": sms, "step_ms_min": min(step_ms),
+                   "step_ms_median": statistics.median(step_ms), "wall_s": wall},
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "clocks": clocks,
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
+                "h2d_bytes_per_step": int(A.nbytes + B.nbytes), "d2h_bytes_per_step": int(c.numel() * c.element_size())},
+        "gpu_launches": args.steps,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def main():
+    args = parse_args()
+    w = wl.BY_NAME[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()

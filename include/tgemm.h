@@ -1,0 +1,168 @@
+/*
+ * tgemm -- tiled dense matrix multiply for NVIDIA GB300 (sm_103a).
+ *
+ * C ABI of the library (libtgemm.so).  Every entry point takes plain
+ * integers and pointers; no CUDA or framework type appears in a signature.
+ * A stream argument is a cudaStream_t passed as `void*` (NULL = the legacy
+ * default stream).
+ *
+ * The operation is the dense product of the tiling pages:
+ *     C[M,N] = A[M,K] . B[K,N],   C[i][j] = sum_{k<K} A[i][k] * B[k][j]
+ * ("CUDA tile", section 2.1; "Tiling 策略与内存层次优化", section "Tiling 如何提升
+ * 算术强度"), computed tile by tile with K split into stages
+ * ("矩阵乘法中的平铺", the l-length K-splitting paragraph).  Splitting changes
+ * only the order of the fp32 additions, never the set of terms.
+ */
+#ifndef TGEMM_H
+#define TGEMM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define TGEMM_VERSION 10000 /* major * 10000 + minor * 100 + patch */
+
+/* Entry points are the only symbols the library exports. */
+#if defined(__GNUC__)
+#define TGEMM_API __attribute__((visibility("default")))
+#else
+#define TGEMM_API
+#endif
+
+/* (input format, output format) pairs.  Every variant accumulates in fp32. */
+enum tgemm_dtype {
+  TGEMM_F32 = 0,         /* fp32 A, B -> fp32 C   (CUDA-core SIMT path)        */
+  TGEMM_F16 = 1,         /* fp16 A, B -> fp16 C   (tensor-core path)           */
+  TGEMM_BF16 = 2,        /* bf16 A, B -> bf16 C   (tensor-core path)           */
+  TGEMM_BF16_F32OUT = 3, /* bf16 A, B -> fp32 C   (tensor-core path)           */
+  TGEMM_F16_F32OUT = 4   /* fp16 A, B -> fp32 C   (tensor-core path)           */
+};
+
+/* Status codes.  0 is success; every other value is an error and nothing was
+ * launched (except TGEMM_ERR_DEVICE_TIMEOUT, which reports a past launch). */
+enum tgemm_status {
+  TGEMM_OK = 0,
+  TGEMM_ERR_INVALID_VALUE = 1,     /* negative size, leading dimension too small,
+                                      null pointer with a non-empty extent,
+                                      bad option value */
+  TGEMM_ERR_UNSUPPORTED_DTYPE = 2, /* dtype not in enum tgemm_dtype */
+  TGEMM_ERR_MISALIGNED = 3,        /* a pointer is not aligned to its element size */
+  TGEMM_ERR_ALIAS = 4,             /* C's byte range overlaps A's or B's */
+  TGEMM_ERR_UNSUPPORTED_DEVICE = 5,/* current device is not compute capability 10.3 */
+  TGEMM_ERR_LAUNCH = 6,            /* a CUDA call failed while launching; see
+                                      tgemm_status_string(TGEMM_ERR_LAUNCH) */
+  TGEMM_ERR_DEVICE_TIMEOUT = 7,    /* a kernel gave up a bounded wait (reported
+                                      by tgemm_device_status) */
+  TGEMM_ERR_TOO_LARGE = 8          /* a size exceeds what the kernels index
+                                      (M, N, K >= 2^31, or a bulk-copy bound) */
+};
+
+/*
+ * C = A . B, row-major, asynchronous on `stream`.
+ *
+ *   A: M x K, element (i, k) at A[i*lda + k], lda >= max(1, K)
+ *   B: K x N, element (k, j) at B[k*ldb + j], ldb >= max(1, N)
+ *   C: M x N, element (i, j) at C[i*ldc + j], ldc >= max(1, N)
+ * Leading dimensions are in elements of the operand's own format.  A, B and
+ * C are device pointers owned by the caller; each must be aligned to its
+ * element size.  C is overwritten (no alpha/beta); elements of C outside the
+ * M x N window (the ldc - N padding of each row) are never written.
+ *
+ * M == 0 or N == 0: nothing is done.  K == 0: C is set to +0.
+ * Any alignment and any leading dimension are accepted; 16-byte aligned rows
+ * take the bulk-tensor (TMA) loads and stores, others take per-thread copies.
+ *
+ * The call validates its arguments on the host, picks a kernel and a tile
+ * shape for the current device, and enqueues one kernel on `stream`; it
+ * returns before the product is computed.  It allocates no device memory.
+ * It keeps a small, mutex-guarded host cache of device attributes.  It is
+ * safe to call from several host threads.
+ *
+ * Errors: see enum tgemm_status.  Validation errors are returned before any
+ * CUDA call.  A launch failure returns TGEMM_ERR_LAUNCH with the CUDA error
+ * text available from tgemm_status_string.
+ */
+TGEMM_API int tgemm_gemm(int64_t M, int64_t N, int64_t K,
+               const void* A, int64_t lda,
+               const void* B, int64_t ldb,
+               void* C, int64_t ldc,
+               int dtype, void* stream);
+
+/* Kernel selection for tgemm_gemm_ex.  AUTO picks as tgemm_gemm does. */
+enum tgemm_kernel {
+  TGEMM_KERNEL_AUTO = 0,
+  TGEMM_KERNEL_TC_TMA = 1,     /* tensor cores; A and B by bulk-tensor copies */
+  TGEMM_KERNEL_TC_COPY = 2,    /* tensor cores; A and/or B by per-thread async
+                                  copies (any alignment) */
+  TGEMM_KERNEL_SIMT = 3        /* fp32 CUDA cores (TGEMM_F32 only) */
+};
+
+/* Options of tgemm_gemm_ex.  Zero-initialise and set what you need; a zero
+ * field means "the default". */
+typedef struct tgemm_options {
+  int kernel;           /* enum tgemm_kernel */
+  int tile_n;           /* tensor-core tile width: 0 (auto), 64, 128 or 256 */
+  int group_m;          /* rasterisation group height in tiles (0 = auto) */
+  int max_ctas;         /* cap on persistent CTAs (0 = one per SM) */
+  int store_mode;       /* 0 auto, 1 bulk-tensor store, 2 per-thread stores */
+  int wait_timeout_us;  /* bound of every in-kernel wait (0 = 2 s) */
+  int inject_fault;     /* test hook: 1 = the producer never signals its first
+                           stage, so the consumers' bounded waits run out and
+                           the kernel exits with TGEMM_ERR_DEVICE_TIMEOUT
+                           pending; no copy is ever issued */
+  int reserved[9];
+} tgemm_options;
+
+/* tgemm_gemm with explicit options (opts may be NULL).  A forced kernel that
+ * cannot serve the arguments (e.g. TC_TMA on rows that are not 16-byte
+ * aligned) returns TGEMM_ERR_INVALID_VALUE. */
+TGEMM_API int tgemm_gemm_ex(int64_t M, int64_t N, int64_t K,
+                  const void* A, int64_t lda,
+                  const void* B, int64_t ldb,
+                  void* C, int64_t ldc,
+                  int dtype, const tgemm_options* opts, void* stream);
+
+/* The dispatch decision tgemm_gemm_ex would take, without launching and
+ * without touching the GPU.  `sm_count` is the number of SMs to plan for.
+ * Returns the same validation status as tgemm_gemm_ex. */
+typedef struct tgemm_plan_info {
+  int kernel;        /* enum tgemm_kernel actually chosen (never AUTO) */
+  int tile_m, tile_n, tile_k;
+  int stages;        /* shared-memory ring depth */
+  int tiles_m, tiles_n;
+  int ctas;          /* CTAs launched (persistent: min(tiles, SMs)) */
+  int group_m;
+  int a_copy_bytes;  /* granule of A's per-thread copies (0 = bulk-tensor) */
+  int b_copy_bytes;  /* granule of B's per-thread copies (0 = bulk-tensor) */
+  int store_bytes;   /* granule of C's per-thread stores (0 = bulk-tensor) */
+  int smem_bytes;    /* dynamic shared memory per CTA */
+  int reserved[4];
+} tgemm_plan_info;
+
+TGEMM_API int tgemm_plan(int64_t M, int64_t N, int64_t K,
+               const void* A, int64_t lda,
+               const void* B, int64_t ldb,
+               const void* C, int64_t ldc,
+               int dtype, const tgemm_options* opts, int sm_count,
+               tgemm_plan_info* out);
+
+/* Waits for `stream`, then returns and clears the device-side status word
+ * that bounded in-kernel waits set when they give up (TGEMM_OK or
+ * TGEMM_ERR_DEVICE_TIMEOUT).  A CUDA error while synchronising returns
+ * TGEMM_ERR_LAUNCH. */
+TGEMM_API int tgemm_device_status(void* stream);
+
+/* Static text for a status code; for TGEMM_ERR_LAUNCH the text of the last
+ * CUDA error seen by the calling thread. */
+TGEMM_API const char* tgemm_status_string(int status);
+
+/* TGEMM_VERSION of the loaded library. */
+TGEMM_API int tgemm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TGEMM_H */

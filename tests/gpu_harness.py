@@ -1,0 +1,109 @@
+"""Helpers of the GPU parity tests: place seeded storage bits in device memory
+(optionally at a misaligned offset, with guard bands), call the C ABI, and
+compare the result with the oracle under the parity tolerance."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+import workloads as wl
+from tests import tolerance
+
+# NaN patterns no kernel writes; a guard element that changes was overwritten
+CANARY = {"f32": 0x7FA1B2C3, "f16": 0x7E5A, "bf16": 0x7FDA}
+NP_BITS = {"f32": np.uint32, "f16": np.uint16, "bf16": np.uint16}
+GUARD = 256  # guard elements before and after C
+
+
+def tg():
+    from tests.conftest import build_library
+    build_library()
+    import tiled_dense_gemm_02_gb300 as lib
+    return lib
+
+
+def device_bytes(nbytes: int, offset: int, dev) -> tuple[torch.Tensor, int]:
+    """A byte buffer and a pointer `offset` bytes past a 256-byte boundary."""
+    buf = torch.empty(nbytes + offset + 512, dtype=torch.uint8, device=dev)
+    base = (buf.data_ptr() + 255) // 256 * 256
+    return buf, base + offset
+
+
+def upload(bits: np.ndarray, offset: int, dev) -> tuple[torch.Tensor, int]:
+    raw = np.ascontiguousarray(bits).view(np.uint8).reshape(-1)
+    buf, ptr = device_bytes(raw.size, offset, dev)
+    start = ptr - buf.data_ptr()
+    buf[start:start + raw.size].copy_(torch.from_numpy(raw))
+    return buf, ptr
+
+
+class Result:
+    def __init__(self, got, status, plan, guard_ok, pad_ok):
+        self.got, self.status, self.plan, self.guard_ok, self.pad_ok = got, status, plan, guard_ok, pad_ok
+
+
+def run_gpu(A_bits: np.ndarray, B_bits: np.ndarray, M: int, N: int, K: int, dtype: int,
+            ldc: int | None = None, a_off: int = 0, b_off: int = 0, c_off: int = 0,
+            options=None, dev=None, check_status: bool = True) -> Result:
+    """C = A . B on the GPU through tgemm_gemm_ex; A/B given as [rows, ld] bit arrays."""
+    lib = tg()
+    dev = dev or torch.device("cuda:0")
+    fout = wl.OUT_FORMAT[dtype]
+    eo = wl.FORMATS[fout][3]
+    ldc = N if ldc is None else ldc
+    lda, ldb = A_bits.shape[1], B_bits.shape[1]
+    a_buf, a_ptr = upload(A_bits, a_off, dev)
+    b_buf, b_ptr = upload(B_bits, b_off, dev)
+    c_elems = GUARD + M * ldc + GUARD
+    c_init = np.full(c_elems, CANARY[fout], dtype=NP_BITS[fout])
+    c_buf, c_base = upload(c_init, c_off, dev)
+    c_ptr = c_base + GUARD * eo
+    stream = torch.cuda.current_stream(dev).cuda_stream
+    st_plan, plan = lib.plan(M, N, K, a_ptr, lda, b_ptr, ldb, c_ptr, ldc, dtype, options,
+                             sm_count=torch.cuda.get_device_properties(dev).multi_processor_count)
+    status = lib.gemm_ex(M, N, K, a_ptr, lda, b_ptr, ldb, c_ptr, ldc, dtype, options, stream)
+    dstat = lib.device_status(stream)
+    if check_status:
+        assert status == lib.OK, lib.status_string(status)
+        assert dstat == lib.OK, lib.status_string(dstat)
+    start = c_base - c_buf.data_ptr()
+    raw = c_buf[start:start + c_elems * eo].cpu().numpy().view(NP_BITS[fout])
+    guard_ok = bool(np.all(raw[:GUARD] == CANARY[fout]) and np.all(raw[GUARD + M * ldc:] == CANARY[fout]))
+    body = raw[GUARD:GUARD + M * ldc].reshape(M, ldc) if M > 0 else np.zeros((0, ldc), NP_BITS[fout])
+    pad_ok = bool(np.all(body[:, N:] == CANARY[fout]))
+    got = wl.decode(np.ascontiguousarray(body[:, :N]), fout)
+    res = Result(got, (status, dstat), plan, guard_ok, pad_ok)
+    res.raw = body[:, :N].copy()
+    return res
+
+
+def check_full(res: Result, A_bits, B_bits, M, N, K, dtype, label=""):
+    fin, fout = wl.IN_FORMAT[dtype], wl.OUT_FORMAT[dtype]
+    ref, S = oracle.gemm(np.ascontiguousarray(A_bits), np.ascontiguousarray(B_bits), fin, M, N, K)
+    ok, ratio, where = tolerance.check(res.got, ref, S, fin, fout)
+    assert res.guard_ok, f"{label}: guard band around C overwritten"
+    assert res.pad_ok, f"{label}: ldc padding of C overwritten"
+    assert ok, (f"{label}: error/bound {ratio:.3g} at {where}: got {res.got[where]} want {ref[where]} "
+                f"S {S[where]} plan {res.plan.as_dict()}")
+    return ratio
+
+
+def check_sampled(res: Result, A_bits, B_bits, K, dtype, rows, cols, label=""):
+    fin, fout = wl.IN_FORMAT[dtype], wl.OUT_FORMAT[dtype]
+    ref, S = oracle.entries(np.ascontiguousarray(A_bits), np.ascontiguousarray(B_bits), fin, K, rows, cols)
+    ok, ratio, where = tolerance.check(res.got[rows, cols], ref, S, fin, fout)
+    assert res.guard_ok and res.pad_ok, f"{label}: guard band or padding overwritten"
+    assert ok, f"{label}: error/bound {ratio:.3g} at sample {where} (row {rows[where]}, col {cols[where]})"
+    return ratio
+
+
+def sample_positions(M: int, N: int, n_random: int, seed: int):
+    """Every element of the first and last row and column, the corners of
+    every 128-row band, plus `n_random` uniformly drawn positions."""
+    r = wl.splitmix64(seed, 2 * n_random)
+    rows = [np.zeros(N, np.int64), np.full(N, M - 1, np.int64), np.arange(M), np.arange(M),
+            (r[:n_random] % np.uint64(M)).astype(np.int64)]
+    cols = [np.arange(N), np.arange(N), np.zeros(M, np.int64), np.full(M, N - 1, np.int64),
+            (r[n_random:] % np.uint64(N)).astype(np.int64)]
+    return np.concatenate(rows), np.concatenate(cols)

@@ -1,0 +1,139 @@
+"""The C ABI on the host: the library loads, exports every declared entry
+point, and its validation and dispatch planning behave as include/tgemm.h
+states.  None of these calls reaches the GPU (validation errors are returned
+before any CUDA call; tgemm_plan never touches the device)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def tg():
+    from tests.conftest import build_library
+    build_library()
+    import tiled_dense_gemm_02_gb300 as tg
+    return tg
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "tgemm.h")).read()
+    return sorted(set(re.findall(r"^\s*TGEMM_API\s+(?:const\s+)?\w+\s*\*?\s*(tgemm_\w+)\s*\(", text, re.M)))
+
+
+def test_header_declares_the_abi():
+    names = declared_functions()
+    assert names == sorted(["tgemm_gemm", "tgemm_gemm_ex", "tgemm_plan", "tgemm_device_status",
+                            "tgemm_status_string", "tgemm_version"])
+
+
+def test_library_exports_every_declared_symbol(tg):
+    lib = tg.library()
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    assert set(declared_functions()) == set(tg.EXPORTS)
+    assert tg.version() == 10000
+
+
+def test_struct_layouts_match_header(tg):
+    assert ctypes.sizeof(tg.Options) == 16 * 4
+    assert ctypes.sizeof(tg.PlanInfo) == 17 * 4
+
+
+def test_status_strings(tg):
+    for code in range(9):
+        assert tg.status_string(code)
+    assert tg.status_string(0) == "success"
+    assert tg.status_string(99) == "unknown status"
+
+
+# fake, well-aligned device addresses: planning never dereferences them
+A0, B0, C0 = 0x10000000, 0x20000000, 0x30000000
+
+
+def plan(tg, M, N, K, lda=None, ldb=None, ldc=None, dtype=2, A=A0, B=B0, C=C0, sms=148, **opt):
+    lda = K if lda is None else lda
+    ldb = N if ldb is None else ldb
+    ldc = N if ldc is None else ldc
+    return tg.plan(M, N, K, A, lda, B, ldb, C, ldc, dtype, opt or None, sm_count=sms)
+
+
+def test_validation_errors(tg):
+    assert plan(tg, -1, 4, 4)[0] == tg.ERR_INVALID_VALUE
+    assert plan(tg, 4, 4, 4, lda=3)[0] == tg.ERR_INVALID_VALUE
+    assert plan(tg, 4, 4, 4, ldb=3)[0] == tg.ERR_INVALID_VALUE
+    assert plan(tg, 4, 4, 4, ldc=3)[0] == tg.ERR_INVALID_VALUE
+    assert plan(tg, 4, 4, 4, dtype=7)[0] == tg.ERR_UNSUPPORTED_DTYPE
+    assert plan(tg, 4, 4, 4, A=A0 + 1)[0] == tg.ERR_MISALIGNED
+    assert plan(tg, 4, 4, 4, dtype=0, C=C0 + 2)[0] == tg.ERR_MISALIGNED
+    assert plan(tg, 4, 4, 4, A=0)[0] == tg.ERR_INVALID_VALUE
+    assert plan(tg, 4, 4, 4, C=A0 + 8)[0] == tg.ERR_ALIAS
+    assert plan(tg, 4, 4, 4, C=B0)[0] == tg.ERR_ALIAS
+    assert plan(tg, 1 << 31, 4, 4)[0] == tg.ERR_TOO_LARGE
+    assert plan(tg, 4, 4, 4, tile_n=96)[0] == tg.ERR_INVALID_VALUE
+    assert plan(tg, 4, 4, 4, dtype=0, kernel=tg.KERNEL_TC_TMA)[0] == tg.ERR_INVALID_VALUE
+    assert plan(tg, 4, 4, 4, dtype=2, kernel=tg.KERNEL_SIMT)[0] == tg.ERR_INVALID_VALUE
+    # TMA forced on rows that are not 16-byte aligned
+    assert plan(tg, 4, 4, 6, kernel=tg.KERNEL_TC_TMA)[0] == tg.ERR_INVALID_VALUE
+    assert plan(tg, 4, 6, 8, store_mode=1)[0] == tg.ERR_INVALID_VALUE
+
+
+def test_gemm_validation_never_touches_the_gpu(tg):
+    # these return before any CUDA call, so they run on a machine without a GPU
+    assert tg.gemm(-1, 4, 4, A0, 4, B0, 4, C0, 4, 2, 0) == tg.ERR_INVALID_VALUE
+    assert tg.gemm(4, 4, 4, A0, 4, B0, 4, A0, 4, 2, 0) == tg.ERR_ALIAS
+    assert tg.gemm(4, 4, 4, A0, 4, B0, 4, C0, 4, 9, 0) == tg.ERR_UNSUPPORTED_DTYPE
+    assert tg.gemm(0, 4, 4, A0, 4, B0, 4, C0, 4, 2, 0) == tg.OK   # empty: nothing to do
+    assert tg.gemm(4, 0, 4, 0, 4, 0, 4, 0, 1, 2, 0) == tg.OK
+
+
+def test_dispatch_aligned_uses_bulk_tensor_copies(tg):
+    st, p = plan(tg, 4096, 4096, 4096, dtype=3, sms=148)
+    assert st == tg.OK
+    assert p.kernel == tg.KERNEL_TC_TMA and p.a_copy_bytes == 0 and p.b_copy_bytes == 0 and p.store_bytes == 0
+    assert (p.tile_m, p.tile_k) == (128, 64)
+    assert p.tiles_m * 128 >= 4096 and p.tiles_n * p.tile_n >= 4096
+    assert p.ctas == min(148, p.tiles_m * p.tiles_n)
+    assert p.smem_bytes <= 232448
+
+
+def test_dispatch_ragged_unaligned_rows(tg):
+    # 1000 x 1500 x 4096 bf16: B and C rows are 3000 bytes (8-byte granules)
+    st, p = plan(tg, 1000, 1500, 4096, dtype=2)
+    assert st == tg.OK
+    assert p.kernel == tg.KERNEL_TC_COPY
+    assert p.a_copy_bytes == 0 and p.b_copy_bytes == 8 and p.store_bytes == 8
+    st, p = plan(tg, 33, 17, 7, dtype=1)  # odd everything: 2-byte granules
+    assert (p.a_copy_bytes, p.b_copy_bytes, p.store_bytes) == (2, 2, 2)
+    st, p = plan(tg, 64, 64, 64, dtype=2, A=A0 + 4)
+    assert p.a_copy_bytes == 4 and p.b_copy_bytes == 0
+
+
+def test_bulk_store_needs_16_byte_row_extent(tg):
+    # rows of 780 bytes inside a 784-byte pitch: per-thread stores
+    assert plan(tg, 260, 390, 304, ldc=392, ldb=392)[1].store_bytes == 16
+    assert plan(tg, 260, 392, 304, ldc=400, ldb=392)[1].store_bytes == 0
+    assert plan(tg, 260, 388, 304, ldc=392, ldb=392, dtype=3)[1].store_bytes == 0   # fp32: 1552 bytes
+
+
+def test_dispatch_options(tg):
+    st, p = plan(tg, 1024, 1024, 1024, dtype=1, tile_n=64, max_ctas=5, group_m=3, store_mode=2)
+    assert st == tg.OK
+    assert (p.tile_n, p.ctas, p.group_m, p.store_bytes) == (64, 5, 3, 16)
+    st, p = plan(tg, 1024, 1024, 1024, dtype=1, kernel=tg.KERNEL_TC_COPY)
+    assert p.kernel == tg.KERNEL_TC_COPY and p.a_copy_bytes == 16 and p.b_copy_bytes == 16
+    st, p = plan(tg, 300, 300, 300, dtype=0, A=A0 + 4)
+    assert p.kernel == tg.KERNEL_SIMT and p.a_copy_bytes == 4   # scalar loads
+    st, p = plan(tg, 64, 64, 0, lda=1, dtype=2)
+    assert st == tg.OK and p.kernel == 0   # K = 0: zero fill, no GEMM kernel
+
+
+def test_tile_width_choice_fills_the_sms(tg):
+    # small problems should not leave most SMs idle with 256-wide tiles
+    st, p = plan(tg, 1024, 1024, 1024, dtype=1, sms=148)
+    assert p.tiles_m * p.tiles_n >= 100
+    st, p = plan(tg, 8192, 8192, 8192, dtype=2, sms=148)
+    assert p.tile_n == 256

@@ -1,0 +1,191 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle.
+
+Tolerance (tests/tolerance.py): |C_gpu - C_ref| <= 2^-10 S + ulp_out(C_ref)/2
+for fp16/bf16 inputs and <= 2^-20 S for fp32, S = sum_k |a_ik b_kj|.
+Every case also checks the guard bands around C and the ldc padding.
+"""
+import numpy as np
+import pytest
+import torch
+
+import workloads as wl
+from tests import gpu_harness as H
+
+pytestmark = pytest.mark.gpu
+
+TC_DTYPES = [wl.F16, wl.BF16, wl.BF16_F32OUT, wl.F16_F32OUT]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    H.tg()
+    torch.cuda.set_device(0)
+
+
+def case(M, N, K, dtype, dist="uniform", seed=20, lda=None, ldb=None, ldc=None, **kw):
+    w = wl.Workload("case", M, N, K, dtype, dist, seed)
+    A, B = wl.make_inputs(w, lda=lda, ldb=ldb)
+    res = H.run_gpu(A, B, M, N, K, dtype, ldc=ldc, **kw)
+    return A, B, res
+
+
+# ------------------------------------------------------------------ workloads
+
+@pytest.mark.parametrize("name", ["f32_64x64x64", "f16_1024x1024x1024", "bf16_2048x2048x2048",
+                                  "bf16_1000x1500x4096_ragged"])
+def test_workload_full_product(name):
+    w = wl.BY_NAME[name]
+    A, B = wl.make_inputs(w)
+    res = H.run_gpu(A, B, w.M, w.N, w.K, w.dtype)
+    H.check_full(res, A, B, w.M, w.N, w.K, w.dtype, name)
+
+
+@pytest.mark.parametrize("name", ["bf16_4096x4096x4096_f32out", "f32_4096x4096x4096", "f32_2048x2048x2048"])
+def test_workload_sampled(name):
+    """Full-size products in the launch configuration the benchmark times,
+    checked on every element of the border rows/columns and random samples."""
+    w = wl.BY_NAME[name]
+    A, B = wl.make_inputs(w)
+    res = H.run_gpu(A, B, w.M, w.N, w.K, w.dtype)
+    rows, cols = H.sample_positions(w.M, w.N, 4096, seed=99)
+    H.check_sampled(res, A, B, w.K, w.dtype, rows, cols, name)
+
+
+# ------------------------------------------------------------ shape sweeps
+
+SHAPES = [(1, 1, 1), (7, 9, 5), (63, 65, 127), (128, 256, 64), (129, 257, 255), (300, 520, 200),
+          (257, 129, 64), (513, 300, 1000)]
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("dtype", TC_DTYPES + [wl.F32], ids=lambda d: wl.DTYPE_NAMES[d])
+def test_shape_sweep_auto(shape, dtype):
+    M, N, K = shape
+    A, B, res = case(M, N, K, dtype, seed=21)
+    H.check_full(res, A, B, M, N, K, dtype, f"{shape} {wl.DTYPE_NAMES[dtype]}")
+
+
+@pytest.mark.parametrize("tile_n", [64, 128, 256])
+@pytest.mark.parametrize("store_mode", [1, 2])
+@pytest.mark.parametrize("dtype", TC_DTYPES, ids=lambda d: wl.DTYPE_NAMES[d])
+def test_tile_widths_and_store_modes(tile_n, store_mode, dtype):
+    M, N, K = 300, 520, 200   # 3 row tiles with a 44-row tail, ragged N, K tail of 8
+    A, B, res = case(M, N, K, dtype, seed=22, options={"tile_n": tile_n, "store_mode": store_mode})
+    assert res.plan.tile_n == tile_n
+    assert (res.plan.store_bytes == 0) == (store_mode == 1)
+    H.check_full(res, A, B, M, N, K, dtype, f"tile_n {tile_n} store {store_mode}")
+
+
+@pytest.mark.parametrize("tile_n", [64, 128, 256])
+@pytest.mark.parametrize("dtype", [wl.BF16, wl.F16_F32OUT], ids=lambda d: wl.DTYPE_NAMES[d])
+def test_copy_producer_on_aligned_rows(tile_n, dtype):
+    """Force the per-thread-copy producer (16-byte granules) on aligned data."""
+    M, N, K = 260, 390, 300
+    # padded pitches (304 and 392 elements = 608 and 784 bytes) keep every row 16-byte aligned
+    A, B, res = case(M, N, K, dtype, seed=23, lda=304, ldb=392, ldc=392,
+                     options={"kernel": 2, "tile_n": tile_n})
+    assert res.plan.kernel == 2 and res.plan.a_copy_bytes == 16 and res.plan.b_copy_bytes == 16
+    H.check_full(res, A, B, M, N, K, dtype, f"copy tile_n {tile_n}")
+
+
+@pytest.mark.parametrize("offsets", [(2, 0, 0), (4, 4, 4), (8, 8, 8), (0, 2, 2), (6, 10, 12)])
+@pytest.mark.parametrize("dtype", [wl.BF16, wl.F16], ids=lambda d: wl.DTYPE_NAMES[d])
+def test_misaligned_pointers(offsets, dtype):
+    """Bases off the 16-byte grid take the copy producer / per-thread stores."""
+    a_off, b_off, c_off = offsets
+    M, N, K = 200, 333, 150
+    A, B, res = case(M, N, K, dtype, seed=24, lda=152, ldb=336, ldc=340, a_off=a_off, b_off=b_off, c_off=c_off)
+    H.check_full(res, A, B, M, N, K, dtype, f"offsets {offsets}")
+
+
+@pytest.mark.parametrize("lds", [(70, 90, 95), (72, 88, 96), (71, 83, 83), (65, 81, 81), (80, 96, 96)])
+@pytest.mark.parametrize("dtype", [wl.BF16, wl.BF16_F32OUT, wl.F32], ids=lambda d: wl.DTYPE_NAMES[d])
+def test_leading_dimensions(lds, dtype):
+    """ld > dim: A/B padding holds NaN (must never be read), C padding a canary
+    (must never be written)."""
+    lda, ldb, ldc = lds
+    M, N, K = 150, 81, 65
+    A, B, res = case(M, N, K, dtype, seed=25, lda=lda, ldb=ldb, ldc=ldc)
+    H.check_full(res, A, B, M, N, K, dtype, f"lds {lds}")
+
+
+# ------------------------------------------------------- scheduler and edges
+
+@pytest.mark.parametrize("max_ctas,group_m", [(1, 1), (3, 2), (5, 16), (7, 3)])
+def test_persistent_scheduler(max_ctas, group_m):
+    """Few CTAs walking many tiles exercises every phase of the stage ring and
+    of the two accumulator buffers."""
+    M, N, K = 1100, 1300, 300
+    A, B, res = case(M, N, K, wl.BF16, seed=26, options={"max_ctas": max_ctas, "group_m": group_m, "tile_n": 128})
+    assert res.plan.ctas == max_ctas
+    H.check_full(res, A, B, M, N, K, wl.BF16, f"ctas {max_ctas} group {group_m}")
+
+
+@pytest.mark.parametrize("K", [1, 16, 63, 64, 65, 128, 192, 320, 448, 640])
+def test_k_block_counts(K):
+    """K around multiples of the 64-wide stage and of the ring depth."""
+    M, N = 130, 260
+    for dtype, opts in ((wl.BF16_F32OUT, {"tile_n": 256}), (wl.F16, {"tile_n": 64}), (wl.F32, None)):
+        A, B, res = case(M, N, K, dtype, seed=27, options=opts)
+        H.check_full(res, A, B, M, N, K, dtype, f"K {K} {wl.DTYPE_NAMES[dtype]}")
+
+
+@pytest.mark.parametrize("N,ldc", [(390, 392), (390, 400), (392, 400), (385, 392)])
+def test_store_never_touches_row_padding(N, ldc):
+    """The row end of C is not always on a 16-byte boundary: nothing past
+    column N may change (bulk-tensor stores are used only when it is)."""
+    M, K = 260, 304
+    A, B, res = case(M, N, K, wl.BF16, seed=33, lda=304, ldb=400, ldc=ldc)
+    assert (res.plan.store_bytes == 0) == ((N * 2) % 16 == 0)
+    H.check_full(res, A, B, M, N, K, wl.BF16, f"N {N} ldc {ldc}")
+
+
+def test_empty_dimensions_leave_c_untouched():
+    for (M, N, K) in [(0, 5, 7), (5, 0, 7)]:
+        A, B, res = case(M, N, K, wl.BF16, seed=28, lda=max(K, 1), ldb=max(N, 1), ldc=max(N, 1))
+        assert res.guard_ok and res.pad_ok
+
+
+@pytest.mark.parametrize("dtype", TC_DTYPES + [wl.F32], ids=lambda d: wl.DTYPE_NAMES[d])
+def test_k_zero_writes_zeros(dtype):
+    M, N = 37, 45
+    w = wl.Workload("k0", M, 1, 1, dtype, "uniform", 29)
+    fin = wl.IN_FORMAT[dtype]
+    A = np.zeros((M, 1), dtype=H.NP_BITS[fin])
+    B = np.zeros((1, N), dtype=H.NP_BITS[fin])
+    res = H.run_gpu(A, B, M, N, 0, dtype, ldc=N + 3)
+    assert res.guard_ok and res.pad_ok
+    assert np.all(res.raw == 0)   # +0 in every format
+
+
+def test_deterministic():
+    A, B, r1 = case(700, 900, 777, wl.BF16, seed=30)
+    r2 = H.run_gpu(A, B, 700, 900, 777, wl.BF16)
+    assert np.array_equal(r1.raw, r2.raw)
+
+
+def test_nan_poisons_only_its_row():
+    M, N, K = 200, 300, 100
+    w = wl.Workload("nan", M, N, K, wl.BF16, "uniform", 31)
+    A, B = wl.make_inputs(w)
+    A = A.copy()
+    A[17, 50] = 0x7FC0   # NaN
+    res = H.run_gpu(A, B, M, N, K, wl.BF16)
+    assert np.all(np.isnan(res.got[17]))
+    assert not np.any(np.isnan(np.delete(res.got, 17, axis=0)))
+
+
+def test_simt_and_tensor_core_agree_with_oracle_on_same_values():
+    """bf16-representable values run through the fp32 SIMT path and the bf16
+    tensor-core path; both must meet their own bound against the oracle."""
+    M, N, K = 256, 384, 512
+    w = wl.Workload("x", M, N, K, wl.BF16, "uniform", 32)
+    A16, B16 = wl.make_inputs(w)
+    A32 = (A16.astype(np.uint32) << np.uint32(16))
+    B32 = (B16.astype(np.uint32) << np.uint32(16))
+    r16 = H.run_gpu(A16, B16, M, N, K, wl.BF16_F32OUT)
+    r32 = H.run_gpu(A32, B32, M, N, K, wl.F32)
+    H.check_full(r16, A16, B16, M, N, K, wl.BF16_F32OUT, "tc")
+    H.check_full(r32, A32, B32, M, N, K, wl.F32, "simt")

@@ -1,0 +1,392 @@
+// C ABI of the tiled GEMM library: argument validation, dispatch planning,
+// bulk-tensor descriptor encoding and launch.  See include/tgemm.h for the
+// contract of each entry point.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "../../include/tgemm.h"
+#include "tgemm_internal.h"
+
+namespace tgemm {
+
+// Device-side status word: bounded in-kernel waits that give up write a code
+// here; tgemm_device_status reads and clears it.
+__device__ unsigned int g_device_status = 0;
+
+namespace {
+
+thread_local std::string t_last_error;
+
+struct DeviceInfo {
+  bool ready = false;
+  bool supported = false;
+  int sm_count = 0;
+  unsigned int* status = nullptr;
+};
+
+std::mutex g_mutex;
+DeviceInfo g_devices[64];
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+int cuda_fail(cudaError_t e, const char* what) {
+  t_last_error = std::string(what) + ": " + cudaGetErrorString(e);
+  return TGEMM_ERR_LAUNCH;
+}
+
+// Look up (once per device) SM count, compute capability and the status word.
+int device_info(DeviceInfo** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= 64) {
+    t_last_error = "device ordinal out of range";
+    return TGEMM_ERR_LAUNCH;
+  }
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceInfo& d = g_devices[dev];
+  if (!d.ready) {
+    int major = 0, minor = 0, sms = 0;
+    if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return cuda_fail(e, "cudaDeviceGetAttribute");
+    d.supported = (major == 10 && minor == 3);
+    d.sm_count = sms;
+    if (d.supported) {
+      void* p = nullptr;
+      if ((e = cudaGetSymbolAddress(&p, g_device_status)) != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress");
+      d.status = static_cast<unsigned int*>(p);
+    }
+    if (!g_encode) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+      if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn) {
+        t_last_error = "cuTensorMapEncodeTiled entry point not found";
+        return TGEMM_ERR_LAUNCH;
+      }
+      g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    }
+    d.ready = true;
+  }
+  *out = &d;
+  return d.supported ? TGEMM_OK : TGEMM_ERR_UNSUPPORTED_DEVICE;
+}
+
+int in_bytes(int dtype) { return dtype == TGEMM_F32 ? 4 : 2; }
+int out_bytes(int dtype) {
+  return (dtype == TGEMM_F32 || dtype == TGEMM_BF16_F32OUT || dtype == TGEMM_F16_F32OUT) ? 4 : 2;
+}
+
+// Largest of 16/8/4/2 bytes dividing both the base address and the row pitch.
+int granule(const void* p, int64_t ld, int es) {
+  const uint64_t a = reinterpret_cast<uint64_t>(p);
+  const uint64_t pitch = static_cast<uint64_t>(ld) * es;
+  for (int g = 16; g >= 4; g /= 2)
+    if (a % g == 0 && pitch % g == 0) return g;
+  return 2;
+}
+
+bool ranges_overlap(uint64_t a0, uint64_t a1, uint64_t b0, uint64_t b1) { return a0 < b1 && b0 < a1; }
+
+struct Plan {
+  int kernel = TGEMM_KERNEL_AUTO;
+  bool noop = false, zero = false;
+  int bn = 256, stages = 4, tiles_m = 0, tiles_n = 0, ctas = 0, group_m = 1;
+  int a_copy = 0, b_copy = 0, store = 0;
+  int smem = 0;
+};
+
+// Relative MMA issue efficiency of the tile widths (shared-memory operand
+// bandwidth per FLOP grows as the tile narrows).
+double width_rate(int bn) { return bn == 256 ? 1.0 : (bn == 128 ? 0.92 : 0.7); }
+
+int pick_tile_n(int64_t M, int64_t N, int64_t K, int sms) {
+  int best = 256;
+  double best_t = 1e300;
+  for (int bn : {256, 128, 64}) {
+    const int64_t tiles = ((M + kTileM - 1) / kTileM) * ((N + bn - 1) / bn);
+    const int64_t waves = (tiles + sms - 1) / sms;
+    const double t = static_cast<double>(waves) * bn * static_cast<double>(std::max<int64_t>(K, 1)) / width_rate(bn);
+    if (t < best_t * 0.999) {
+      best_t = t;
+      best = bn;
+    }
+  }
+  return best;
+}
+
+int make_plan(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb,
+              const void* C, int64_t ldc, int dtype, const tgemm_options* o, int sms, Plan& p) {
+  if (dtype < TGEMM_F32 || dtype > TGEMM_F16_F32OUT) return TGEMM_ERR_UNSUPPORTED_DTYPE;
+  if (M < 0 || N < 0 || K < 0) return TGEMM_ERR_INVALID_VALUE;
+  if (M >= (int64_t(1) << 31) || N >= (int64_t(1) << 31) || K >= (int64_t(1) << 31)) return TGEMM_ERR_TOO_LARGE;
+  if (lda < std::max<int64_t>(1, K) || ldb < std::max<int64_t>(1, N) || ldc < std::max<int64_t>(1, N))
+    return TGEMM_ERR_INVALID_VALUE;
+  tgemm_options opt;
+  std::memset(&opt, 0, sizeof opt);
+  if (o) opt = *o;
+  if (opt.kernel < TGEMM_KERNEL_AUTO || opt.kernel > TGEMM_KERNEL_SIMT) return TGEMM_ERR_INVALID_VALUE;
+  if (opt.tile_n != 0 && opt.tile_n != 64 && opt.tile_n != 128 && opt.tile_n != 256) return TGEMM_ERR_INVALID_VALUE;
+  if (opt.group_m < 0 || opt.max_ctas < 0 || opt.store_mode < 0 || opt.store_mode > 2 || opt.wait_timeout_us < 0)
+    return TGEMM_ERR_INVALID_VALUE;
+  if (M == 0 || N == 0) {
+    p.noop = true;
+    return TGEMM_OK;
+  }
+  const int ei = in_bytes(dtype), eo = out_bytes(dtype);
+  if (!C) return TGEMM_ERR_INVALID_VALUE;
+  if (K > 0 && (!A || !B)) return TGEMM_ERR_INVALID_VALUE;
+  if (reinterpret_cast<uint64_t>(C) % eo) return TGEMM_ERR_MISALIGNED;
+  if (K > 0 && (reinterpret_cast<uint64_t>(A) % ei || reinterpret_cast<uint64_t>(B) % ei)) return TGEMM_ERR_MISALIGNED;
+  // byte extents of the three operands
+  const uint64_t c0 = reinterpret_cast<uint64_t>(C), c1 = c0 + static_cast<uint64_t>((M - 1) * ldc + N) * eo;
+  if (K > 0) {
+    const uint64_t a0 = reinterpret_cast<uint64_t>(A), a1 = a0 + static_cast<uint64_t>((M - 1) * lda + K) * ei;
+    const uint64_t b0 = reinterpret_cast<uint64_t>(B), b1 = b0 + static_cast<uint64_t>((K - 1) * ldb + N) * ei;
+    if (ranges_overlap(c0, c1, a0, a1) || ranges_overlap(c0, c1, b0, b1)) return TGEMM_ERR_ALIAS;
+  }
+  if (K == 0) {
+    p.zero = true;
+    return TGEMM_OK;
+  }
+  if (dtype == TGEMM_F32) {
+    if (opt.kernel != TGEMM_KERNEL_AUTO && opt.kernel != TGEMM_KERNEL_SIMT) return TGEMM_ERR_INVALID_VALUE;
+    p.kernel = TGEMM_KERNEL_SIMT;
+    p.tiles_m = static_cast<int>((M + kSimtBM - 1) / kSimtBM);
+    p.tiles_n = static_cast<int>((N + kSimtBN - 1) / kSimtBN);
+    if (p.tiles_m > 65535) return TGEMM_ERR_TOO_LARGE;
+    p.ctas = p.tiles_m * p.tiles_n;
+    p.bn = kSimtBN;
+    p.stages = 2;
+    p.smem = 0;
+    const bool vec = reinterpret_cast<uint64_t>(A) % 16 == 0 && reinterpret_cast<uint64_t>(B) % 16 == 0 &&
+                     reinterpret_cast<uint64_t>(C) % 16 == 0 && lda % 4 == 0 && ldb % 4 == 0 && ldc % 4 == 0;
+    p.a_copy = p.b_copy = p.store = vec ? 16 : 4;
+    return TGEMM_OK;
+  }
+  if (opt.kernel == TGEMM_KERNEL_SIMT) return TGEMM_ERR_INVALID_VALUE;
+  // bulk-tensor copies need 16-byte aligned bases and row pitches below 2^40
+  const int ga = granule(A, lda, ei), gb = granule(B, ldb, ei), gc = granule(C, ldc, eo);
+  const bool a_tma = ga == 16 && lda * ei < (int64_t(1) << 40);
+  const bool b_tma = gb == 16 && ldb * ei < (int64_t(1) << 40);
+  // A bulk-tensor store writes whole 16-byte units at the end of a row, so it
+  // is used only when the row's byte extent is a multiple of 16 (otherwise it
+  // would overwrite the ldc padding, or the bytes past the last row).
+  const bool c_tma = gc == 16 && (N * eo) % 16 == 0 && ldc * eo < (int64_t(1) << 40);
+  switch (opt.kernel) {
+    case TGEMM_KERNEL_TC_TMA:
+      if (!a_tma || !b_tma) return TGEMM_ERR_INVALID_VALUE;
+      p.kernel = TGEMM_KERNEL_TC_TMA;
+      break;
+    case TGEMM_KERNEL_TC_COPY:
+      p.kernel = TGEMM_KERNEL_TC_COPY;
+      p.a_copy = ga;
+      p.b_copy = gb;
+      break;
+    default:
+      p.kernel = (a_tma && b_tma) ? TGEMM_KERNEL_TC_TMA : TGEMM_KERNEL_TC_COPY;
+      p.a_copy = a_tma ? 0 : ga;
+      p.b_copy = b_tma ? 0 : gb;
+  }
+  if (opt.store_mode == 1 && !c_tma) return TGEMM_ERR_INVALID_VALUE;
+  p.store = (c_tma && opt.store_mode != 2) ? 0 : gc;
+  p.bn = opt.tile_n ? opt.tile_n : pick_tile_n(M, N, K, sms);
+  p.stages = tc_stages(p.bn);
+  p.tiles_m = static_cast<int>((M + kTileM - 1) / kTileM);
+  p.tiles_n = static_cast<int>((N + p.bn - 1) / p.bn);
+  const int64_t tiles = int64_t(p.tiles_m) * p.tiles_n;
+  if (tiles >= (int64_t(1) << 31)) return TGEMM_ERR_TOO_LARGE;
+  p.group_m = opt.group_m ? opt.group_m : 16;
+  p.group_m = std::max(1, std::min(p.group_m, p.tiles_m));
+  int64_t ctas = std::min<int64_t>(tiles, std::max(1, sms));
+  if (opt.max_ctas) ctas = std::min<int64_t>(ctas, opt.max_ctas);
+  p.ctas = static_cast<int>(ctas);
+  p.smem = tc_smem_bytes(p.bn);
+  return TGEMM_OK;
+}
+
+CUtensorMapDataType tmap_type(int fmt_bytes, bool bf16) {
+  if (fmt_bytes == 4) return CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  return bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+}
+
+// 2-D row-major tensor (cols x rows, pitch in bytes), box of box_cols x box_rows,
+// 128-byte swizzle, zero fill outside the tensor.
+int encode_2d(CUtensorMap* map, CUtensorMapDataType type, const void* base, int64_t cols, int64_t rows,
+              int64_t pitch_bytes, uint32_t box_cols, uint32_t box_rows) {
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(pitch_bytes)};
+  const cuuint32_t box[2] = {box_cols, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(map, type, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    t_last_error = "cuTensorMapEncodeTiled failed with CUresult " + std::to_string(static_cast<int>(r));
+    return TGEMM_ERR_LAUNCH;
+  }
+  return TGEMM_OK;
+}
+
+int run(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb, void* C,
+        int64_t ldc, int dtype, const tgemm_options* o, cudaStream_t stream) {
+  // validation that needs no device first, so bad arguments never touch CUDA
+  Plan p;
+  int st = make_plan(M, N, K, A, lda, B, ldb, C, ldc, dtype, o, 1, p);
+  if (st != TGEMM_OK || p.noop) return st;
+  DeviceInfo* dev = nullptr;
+  st = device_info(&dev);
+  if (st != TGEMM_OK) return st;
+  st = make_plan(M, N, K, A, lda, B, ldb, C, ldc, dtype, o, dev->sm_count, p);
+  if (st != TGEMM_OK) return st;
+  cudaError_t e;
+  if (p.zero) {
+    e = launch_zero_fill(C, M, N, ldc, out_bytes(dtype), stream);
+    return e == cudaSuccess ? TGEMM_OK : cuda_fail(e, "zero-fill launch");
+  }
+  if (p.kernel == TGEMM_KERNEL_SIMT) {
+    SimtArgs a;
+    a.M = static_cast<int>(M);
+    a.N = static_cast<int>(N);
+    a.K = static_cast<int>(K);
+    a.A = static_cast<const float*>(A);
+    a.lda = lda;
+    a.B = static_cast<const float*>(B);
+    a.ldb = ldb;
+    a.C = static_cast<float*>(C);
+    a.ldc = ldc;
+    a.vec = p.a_copy == 16 ? 1 : 0;
+    e = launch_simt(a, stream);
+    return e == cudaSuccess ? TGEMM_OK : cuda_fail(e, "SIMT kernel launch");
+  }
+  const bool bf16 = (dtype == TGEMM_BF16 || dtype == TGEMM_BF16_F32OUT);
+  const int eo = out_bytes(dtype);
+  CUtensorMap mA, mB, mC;
+  std::memset(&mA, 0, sizeof mA);
+  std::memset(&mB, 0, sizeof mB);
+  std::memset(&mC, 0, sizeof mC);
+  if (p.a_copy == 0 && (st = encode_2d(&mA, tmap_type(2, bf16), A, K, M, lda * 2, kTileK, kTileM)) != TGEMM_OK)
+    return st;
+  if (p.b_copy == 0 && (st = encode_2d(&mB, tmap_type(2, bf16), B, N, K, ldb * 2, 64, kTileK)) != TGEMM_OK) return st;
+  if (p.store == 0 && (st = encode_2d(&mC, tmap_type(eo, dtype == TGEMM_BF16), C, N, M, ldc * eo, 128 / eo, 32)) !=
+                          TGEMM_OK)
+    return st;
+  TcArgs a;
+  a.M = static_cast<int>(M);
+  a.N = static_cast<int>(N);
+  a.K = static_cast<int>(K);
+  a.tiles_m = p.tiles_m;
+  a.tiles_n = p.tiles_n;
+  a.num_tiles = p.tiles_m * p.tiles_n;
+  a.k_blocks = static_cast<int>((K + kTileK - 1) / kTileK);
+  a.group_m = p.group_m;
+  a.A = A;
+  a.lda = lda;
+  a.B = B;
+  a.ldb = ldb;
+  a.C = C;
+  a.ldc = ldc;
+  const uint32_t ab = bf16 ? 1u : 0u;
+  // kind::f16 instruction descriptor: D fp32 (bits 4-5 = 1), A/B format
+  // (bits 7-9, 10-12), A K-major (bit 15 = 0), B N-major (bit 16 = 1),
+  // N >> 3 (bits 17-22), M >> 4 (bits 24-28).
+  a.idesc = (1u << 4) | (ab << 7) | (ab << 10) | (1u << 16) | (static_cast<uint32_t>(p.bn >> 3) << 17) |
+            (static_cast<uint32_t>(kTileM >> 4) << 24);
+  a.out_fmt = eo == 4 ? OUT_F32 : (dtype == TGEMM_BF16 ? OUT_BF16 : OUT_F16);
+  a.a_copy = p.a_copy;
+  a.b_copy = p.b_copy;
+  a.store_granule = p.store;
+  a.inject_fault = (o && o->inject_fault) ? 1 : 0;
+  const int to_us = (o && o->wait_timeout_us) ? o->wait_timeout_us : 2000000;
+  a.timeout_ns = static_cast<unsigned long long>(to_us) * 1000ull;
+  a.status = dev->status;
+  e = launch_tc(p.bn, p.kernel == TGEMM_KERNEL_TC_COPY, mA, mB, mC, a, p.ctas, stream);
+  return e == cudaSuccess ? TGEMM_OK : cuda_fail(e, "tensor-core kernel launch");
+}
+
+}  // namespace
+}  // namespace tgemm
+
+extern "C" {
+
+int tgemm_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb, void* C,
+               int64_t ldc, int dtype, void* stream) {
+  return tgemm::run(M, N, K, A, lda, B, ldb, C, ldc, dtype, nullptr, static_cast<cudaStream_t>(stream));
+}
+
+int tgemm_gemm_ex(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb, void* C,
+                  int64_t ldc, int dtype, const tgemm_options* opts, void* stream) {
+  return tgemm::run(M, N, K, A, lda, B, ldb, C, ldc, dtype, opts, static_cast<cudaStream_t>(stream));
+}
+
+int tgemm_plan(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb, const void* C,
+               int64_t ldc, int dtype, const tgemm_options* opts, int sm_count, tgemm_plan_info* out) {
+  tgemm::Plan p;
+  const int st = tgemm::make_plan(M, N, K, A, lda, B, ldb, C, ldc, dtype, opts, sm_count < 1 ? 1 : sm_count, p);
+  if (out) {
+    std::memset(out, 0, sizeof *out);
+    if (st == TGEMM_OK && !p.noop && !p.zero) {
+      out->kernel = p.kernel;
+      out->tile_m = p.kernel == TGEMM_KERNEL_SIMT ? tgemm::kSimtBM : tgemm::kTileM;
+      out->tile_n = p.bn;
+      out->tile_k = p.kernel == TGEMM_KERNEL_SIMT ? tgemm::kSimtBK : tgemm::kTileK;
+      out->stages = p.stages;
+      out->tiles_m = p.tiles_m;
+      out->tiles_n = p.tiles_n;
+      out->ctas = p.ctas;
+      out->group_m = p.group_m;
+      out->a_copy_bytes = p.a_copy;
+      out->b_copy_bytes = p.b_copy;
+      out->store_bytes = p.store;
+      out->smem_bytes = p.smem;
+    }
+  }
+  return st;
+}
+
+int tgemm_device_status(void* stream) {
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return tgemm::cuda_fail(e, "cudaStreamSynchronize");
+  tgemm::DeviceInfo* dev = nullptr;
+  int st = tgemm::device_info(&dev);
+  if (st != TGEMM_OK) return st;
+  unsigned int word = 0;
+  if ((e = cudaMemcpy(&word, dev->status, sizeof word, cudaMemcpyDeviceToHost)) != cudaSuccess)
+    return tgemm::cuda_fail(e, "reading the device status word");
+  if (word == 0) return TGEMM_OK;
+  const unsigned int zero = 0;
+  if ((e = cudaMemcpy(dev->status, &zero, sizeof zero, cudaMemcpyHostToDevice)) != cudaSuccess)
+    return tgemm::cuda_fail(e, "clearing the device status word");
+  tgemm::t_last_error = "bounded wait gave up at site " + std::to_string(word & 0xFFu);
+  return TGEMM_ERR_DEVICE_TIMEOUT;
+}
+
+const char* tgemm_status_string(int status) {
+  switch (status) {
+    case TGEMM_OK: return "success";
+    case TGEMM_ERR_INVALID_VALUE: return "invalid value (size, leading dimension, pointer or option)";
+    case TGEMM_ERR_UNSUPPORTED_DTYPE: return "unsupported dtype";
+    case TGEMM_ERR_MISALIGNED: return "pointer not aligned to its element size";
+    case TGEMM_ERR_ALIAS: return "C overlaps A or B";
+    case TGEMM_ERR_UNSUPPORTED_DEVICE: return "current device is not compute capability 10.3 (sm_103a)";
+    case TGEMM_ERR_LAUNCH: return tgemm::t_last_error.empty() ? "CUDA error" : tgemm::t_last_error.c_str();
+    case TGEMM_ERR_DEVICE_TIMEOUT: return "a kernel gave up a bounded wait";
+    case TGEMM_ERR_TOO_LARGE: return "size too large";
+    default: return "unknown status";
+  }
+}
+
+int tgemm_version(void) { return TGEMM_VERSION; }
+
+}  // extern "C"

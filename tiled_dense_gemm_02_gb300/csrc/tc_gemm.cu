@@ -1,0 +1,544 @@
+// Tensor-core tiled GEMM for sm_103a: C[M,N] = A[M,K] . B[K,N], fp16/bf16 in,
+// fp32 accumulate in tensor memory, fp32/fp16/bf16 out.
+//
+// Three levels of tiling ("Tiling 策略与内存层次优化", section 多级 Tiling 策略),
+// mapped onto Blackwell:
+//   * output tiles of 128 x BN (BN = 64/128/256) owned by one CTA at a time; a
+//     persistent grid of at most one CTA per SM walks the tile list in a
+//     grouped (swizzled) order, so consecutive tiles of a CTA wave share B
+//     panels in L2 ("GPU Kernel 的 Tile、Grid、Wave 与 Launch Overhead": fewer,
+//     larger workers instead of many waves);
+//   * K is split into 64-element stages ("矩阵乘法中的平铺", the l-length
+//     K-splitting paragraph); each stage's A and B tiles go through a
+//     multi-stage shared-memory ring ("Double Buffering / Multi-Stage
+//     Pipelining") with the 128-byte XOR swizzle ("Bank Conflict 与 Swizzling"),
+//     filled by bulk-tensor copies (TMA) or, for rows that are not 16-byte
+//     aligned, by per-thread async copies writing the same swizzled layout;
+//   * the register/MMA level becomes tcgen05.mma issued by one thread, 128 x BN
+//     x 16 per instruction, accumulating fp32 in tensor memory (two accumulator
+//     buffers, so the epilogue of one tile overlaps the MMAs of the next).
+// The epilogue reads tensor memory into registers, converts, and writes C by
+// bulk-tensor stores (out-of-range rows/columns clipped) or by masked
+// per-thread stores ("CUDA tile", section 四.4: zero-fill loads, masked stores).
+//
+// Warp roles (one CTA per SM):
+//   warp 0      bulk-tensor producer (one elected lane)
+//   warp 1      tensor-memory allocator and MMA issuer (one elected lane)
+//   warps 2..5  epilogue, one warp per 32-lane quarter of tensor memory
+//   warps 6..9  per-thread-copy producers (only in the copy variant)
+// Every mbarrier wait is bounded in time; a wait that gives up records a code
+// in the device status word, raises a CTA-wide abort flag so the other roles
+// leave their loops, and the CTA still drains its copies and frees its tensor
+// memory before exiting.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <atomic>
+
+#include "ptx.cuh"
+#include "tgemm_internal.h"
+
+namespace tgemm {
+namespace {
+
+constexpr int kCopyLag = 2;  // stages a copy producer keeps in flight before signalling
+
+struct Ctl {
+  volatile uint32_t* abort;
+  unsigned long long timeout_ns;
+  unsigned int* status;
+};
+
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const Ctl& c, uint32_t site) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = ptx::globaltimer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 16; ++i)
+      if (ptx::mbar_try_wait(bar, parity)) return true;
+    if (*c.abort) return false;
+    if (ptx::globaltimer_ns() - t0 > c.timeout_ns) {
+      *c.abort = 1u;
+      atomicCAS(c.status, 0u, kTimeoutFlag | site);
+      return false;
+    }
+  }
+}
+
+// Lane 0 waits, the warp follows its verdict.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const Ctl& c, uint32_t site) {
+  int ok = 1;
+  if (ptx::lane_id() == 0) ok = wait_bounded(bar, parity, c, site) ? 1 : 0;
+  return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+// Tile id -> (m block, n block): groups of `group_m` block-rows are walked
+// column by column, so CTAs running at the same time touch group_m A panels
+// and few B panels.
+__device__ __forceinline__ void tile_coords(int t, const TcArgs& a, int& mb, int& nb) {
+  const int per_group = a.group_m * a.tiles_n;
+  const int g = t / per_group;
+  const int first_m = g * a.group_m;
+  const int gsz = min(a.tiles_m - first_m, a.group_m);
+  const int r = t - g * per_group;
+  mb = first_m + r % gsz;
+  nb = r / gsz;
+}
+
+// Shared-memory matrix descriptor of tcgen05 for a 128-byte-swizzled operand:
+// start address, leading-dimension byte offset, stride-dimension byte offset
+// (all >> 4), descriptor version 1 (bit 46) and swizzle mode 2 = 128 B.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) | (static_cast<uint64_t>(lbo >> 4) << 16) |
+         (static_cast<uint64_t>(sbo >> 4) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+// Offset of byte `cb` (0..127) of row `r` inside a 128-byte-swizzled block:
+// 16-byte chunk index XOR (row mod 8).
+__device__ __forceinline__ uint32_t sw128_offset(int r, int cb) {
+  return static_cast<uint32_t>(r * 128 + ((((cb >> 4) ^ (r & 7)) << 4) | (cb & 15)));
+}
+
+// ---------------------------------------------------------- copy producers
+// A tile: rows m0..m0+127, k0..k0+63 of row-major A -> K-major swizzled rows.
+template <int G>
+__device__ __forceinline__ void copy_a_tile(uint8_t* sa, const TcArgs& a, int m0, int k0, int ct) {
+  constexpr int PER_ROW = 128 / G;
+  const uint16_t* A = static_cast<const uint16_t*>(a.A);
+#pragma unroll 4
+  for (int idx = ct; idx < kTileM * PER_ROW; idx += kCopyWarps * 32) {
+    const int r = idx / PER_ROW, cb = (idx % PER_ROW) * G;
+    const int gm = m0 + r, gk = k0 + cb / 2;
+    int valid = 0;
+    if (gm < a.M) valid = max(0, min(G / 2, a.K - gk));
+    const uint16_t* src = valid ? A + static_cast<int64_t>(gm) * a.lda + gk : A;
+    const uint32_t off = sw128_offset(r, cb);
+    if constexpr (G >= 4) {
+      ptx::cp_async<G>(ptx::smem_u32(sa) + off, src, static_cast<uint32_t>(valid * 2));
+    } else {
+      *reinterpret_cast<uint16_t*>(sa + off) = valid ? *src : uint16_t(0);
+    }
+  }
+}
+
+// B tile: rows k0..k0+63, columns n0..n0+BN-1 of row-major B -> N-major
+// swizzled atoms of 64 columns (8 KB each).
+template <int G, int BN>
+__device__ __forceinline__ void copy_b_tile(uint8_t* sb, const TcArgs& a, int k0, int n0, int ct) {
+  constexpr int PER_ROW = BN * 2 / G;
+  const uint16_t* B = static_cast<const uint16_t*>(a.B);
+#pragma unroll 4
+  for (int idx = ct; idx < kTileK * PER_ROW; idx += kCopyWarps * 32) {
+    const int r = idx / PER_ROW, cb = (idx % PER_ROW) * G;
+    const int gk = k0 + r, gn = n0 + cb / 2;
+    int valid = 0;
+    if (gk < a.K) valid = max(0, min(G / 2, a.N - gn));
+    const uint16_t* src = valid ? B + static_cast<int64_t>(gk) * a.ldb + gn : B;
+    const uint32_t off = static_cast<uint32_t>((cb >> 7) * 8192) + sw128_offset(r, cb & 127);
+    if constexpr (G >= 4) {
+      ptx::cp_async<G>(ptx::smem_u32(sb) + off, src, static_cast<uint32_t>(valid * 2));
+    } else {
+      *reinterpret_cast<uint16_t*>(sb + off) = valid ? *src : uint16_t(0);
+    }
+  }
+}
+
+__device__ __forceinline__ void copy_a_dispatch(uint8_t* sa, const TcArgs& a, int m0, int k0, int ct) {
+  switch (a.a_copy) {
+    case 16: copy_a_tile<16>(sa, a, m0, k0, ct); break;
+    case 8: copy_a_tile<8>(sa, a, m0, k0, ct); break;
+    case 4: copy_a_tile<4>(sa, a, m0, k0, ct); break;
+    default: copy_a_tile<2>(sa, a, m0, k0, ct); break;
+  }
+}
+
+template <int BN>
+__device__ __forceinline__ void copy_b_dispatch(uint8_t* sb, const TcArgs& a, int k0, int n0, int ct) {
+  switch (a.b_copy) {
+    case 16: copy_b_tile<16, BN>(sb, a, k0, n0, ct); break;
+    case 8: copy_b_tile<8, BN>(sb, a, k0, n0, ct); break;
+    case 4: copy_b_tile<4, BN>(sb, a, k0, n0, ct); break;
+    default: copy_b_tile<2, BN>(sb, a, k0, n0, ct); break;
+  }
+}
+
+// ------------------------------------------------------------- epilogue
+__device__ __forceinline__ uint32_t pack_pair(float lo, float hi, int out_fmt) {
+  if (out_fmt == OUT_BF16) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+  }
+  __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Store a packed 128-byte row segment w[0..31] to global with the widest
+// access `granule` (16/8/4/2 bytes) allows; only the first `valid_bytes`
+// bytes are written (element size `es`).  Fully unrolled so w stays in
+// registers.
+__device__ __forceinline__ void store_segment(uint8_t* dst, const uint32_t (&w)[32], int valid_bytes, int granule,
+                                              int es) {
+  if (valid_bytes >= 128 && granule == 16) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      reinterpret_cast<uint4*>(dst)[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+  } else if (valid_bytes >= 128 && granule == 8) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) reinterpret_cast<uint2*>(dst)[i] = make_uint2(w[2 * i], w[2 * i + 1]);
+  } else if (granule >= 4) {
+    // 4-byte words while they are whole, then a trailing half word
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      if (4 * i + 4 <= valid_bytes) {
+        reinterpret_cast<uint32_t*>(dst)[i] = w[i];
+      } else if (es == 2 && 4 * i + 2 <= valid_bytes) {
+        reinterpret_cast<uint16_t*>(dst)[2 * i] = static_cast<uint16_t>(w[i] & 0xFFFFu);
+      }
+    }
+  } else {
+    // 2-byte aligned rows (16-bit output only)
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      if (4 * i + 2 <= valid_bytes) reinterpret_cast<uint16_t*>(dst)[2 * i] = static_cast<uint16_t>(w[i] & 0xFFFFu);
+      if (4 * i + 4 <= valid_bytes) reinterpret_cast<uint16_t*>(dst)[2 * i + 1] = static_cast<uint16_t>(w[i] >> 16);
+    }
+  }
+}
+
+// -------------------------------------------------------------- the kernel
+template <int BN, bool kCopy>
+__global__ void __launch_bounds__(tc_threads(kCopy), 1)
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
+                   const __grid_constant__ CUtensorMap mapC, const TcArgs args) {
+  constexpr int STAGES = tc_stages(BN);
+  constexpr int A_BYTES = kTileM * kTileK * 2;
+  constexpr int B_BYTES = kTileK * BN * 2;
+  constexpr uint32_t TMEM_COLS = 2 * BN;
+  static_assert(BN == 64 || BN == 128 || BN == 256, "tile width");
+  static_assert(tc_smem_bytes(BN) <= 232448, "shared memory per CTA");
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = sA + STAGES * A_BYTES;
+  uint8_t* sC = sB + STAGES * B_BYTES;
+  uint64_t* full_tma = reinterpret_cast<uint64_t*>(sC + kEpiWarps * 2 * 4096);
+  uint64_t* full_copy = full_tma + STAGES;
+  uint64_t* empty = full_copy + STAGES;
+  uint64_t* acc_full = empty + STAGES;
+  uint64_t* acc_empty = acc_full + 2;
+  uint64_t* drain = acc_empty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile uint32_t* abort_flag = tmem_slot + 1;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const bool has_tma = args.a_copy == 0 || args.b_copy == 0;
+  const bool has_copy = kCopy && (args.a_copy != 0 || args.b_copy != 0);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      ptx::mbar_init(ptx::smem_u32(&full_tma[s]), 1);
+      ptx::mbar_init(ptx::smem_u32(&full_copy[s]), kCopyWarps * 32);
+      ptx::mbar_init(ptx::smem_u32(&empty[s]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(ptx::smem_u32(&acc_full[b]), 1);
+      ptx::mbar_init(ptx::smem_u32(&acc_empty[b]), kEpiWarps);
+    }
+    ptx::mbar_init(ptx::smem_u32(drain), 1);
+    *abort_flag = 0u;
+    ptx::fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    if (args.a_copy == 0) ptx::tma_prefetch_desc(&mapA);
+    if (args.b_copy == 0) ptx::tma_prefetch_desc(&mapB);
+    if (args.store_granule == 0) ptx::tma_prefetch_desc(&mapC);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(ptx::smem_u32(tmem_slot), TMEM_COLS);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before_sync();
+  __syncthreads();
+  ptx::tc_fence_after_sync();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const Ctl ctl{abort_flag, args.timeout_ns, args.status};
+  const int num_tiles = args.num_tiles;
+  const int kbs = args.k_blocks;
+
+  if (warp == 0) {
+    // ------------------------------------------------ bulk-tensor producer
+    if (lane == 0 && has_tma && !args.inject_fault) {
+      const bool a_tma = args.a_copy == 0, b_tma = args.b_copy == 0;
+      const uint32_t tx = (a_tma ? A_BYTES : 0) + (b_tma ? B_BYTES : 0);
+      int stage = 0;
+      uint32_t phase = 0, filled = 0, last_parity = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+        int mb, nb;
+        tile_coords(t, args, mb, nb);
+        for (int kb = 0; kb < kbs; ++kb) {
+          if (!wait_bounded(ptx::smem_u32(&empty[stage]), phase ^ 1u, ctl, SITE_PRODUCER_EMPTY)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = ptx::smem_u32(&full_tma[stage]);
+          ptx::mbar_arrive_expect_tx(fb, tx);
+          if (a_tma) ptx::tma_load_2d(ptx::smem_u32(sA + stage * A_BYTES), &mapA, kb * kTileK, mb * kTileM, fb);
+          if (b_tma) {
+#pragma unroll
+            for (int j = 0; j < BN / 64; ++j)
+              ptx::tma_load_2d(ptx::smem_u32(sB + stage * B_BYTES + j * 8192), &mapB, nb * BN + j * 64, kb * kTileK,
+                               fb);
+          }
+          filled |= 1u << stage;
+          last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // Every load this thread issued must land before shared memory is released.
+      for (int s = 0; s < STAGES; ++s)
+        if ((filled >> s) & 1u) {
+          const Ctl own{abort_flag, ctl.timeout_ns, ctl.status};
+          // a fill that completed long ago returns at once; after an abort the
+          // wait still runs (bounded) because the copies are real
+          uint32_t par = (last_parity >> s) & 1u;
+          if (!ptx::mbar_try_wait(ptx::smem_u32(&full_tma[s]), par)) {
+            const uint64_t t0 = ptx::globaltimer_ns();
+            while (!ptx::mbar_try_wait(ptx::smem_u32(&full_tma[s]), par)) {
+              if (ptx::globaltimer_ns() - t0 > own.timeout_ns) {
+                atomicCAS(own.status, 0u, kTimeoutFlag | SITE_TEARDOWN);
+                break;
+              }
+            }
+          }
+        }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      int stage = 0, acc = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+        if (!wait_bounded(ptx::smem_u32(&acc_empty[acc]), acc_phase ^ 1u, ctl, SITE_MMA_ACC_EMPTY)) break;
+        ptx::tc_fence_after_sync();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+        for (int kb = 0; kb < kbs; ++kb) {
+          if (has_tma && !wait_bounded(ptx::smem_u32(&full_tma[stage]), phase, ctl, SITE_MMA_FULL)) {
+            ok = false;
+            break;
+          }
+          if (has_copy && !wait_bounded(ptx::smem_u32(&full_copy[stage]), phase, ctl, SITE_MMA_FULL)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after_sync();
+          const uint32_t a0 = ptx::smem_u32(sA + stage * A_BYTES);
+          const uint32_t b0 = ptx::smem_u32(sB + stage * B_BYTES);
+#pragma unroll
+          for (int k = 0; k < kTileK / 16; ++k) {
+            // A: K-major, 16 elements = 32 bytes further along each swizzled row.
+            // B: N-major, 16 k-rows = 2 groups of 8 rows (1024 B each) further on;
+            //    64-column atoms are 8 KB apart.
+            ptx::tc_mma_f16(d_tmem, sw128_desc(a0 + k * 32, 16, 1024), sw128_desc(b0 + k * 2048, 8192, 1024),
+                            args.idesc, (kb | k) != 0 ? 1u : 0u);
+          }
+          ptx::tc_commit(ptx::smem_u32(&empty[stage]));
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        ptx::tc_commit(ptx::smem_u32(&acc_full[acc]));
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+      // All MMAs this thread issued have finished before tensor memory is freed.
+      ptx::tc_commit(ptx::smem_u32(drain));
+      const Ctl own{abort_flag, ctl.timeout_ns, ctl.status};
+      if (!ptx::mbar_try_wait(ptx::smem_u32(drain), 0)) {
+        const uint64_t t0 = ptx::globaltimer_ns();
+        while (!ptx::mbar_try_wait(ptx::smem_u32(drain), 0)) {
+          if (ptx::globaltimer_ns() - t0 > own.timeout_ns) {
+            atomicCAS(own.status, 0u, kTimeoutFlag | SITE_DRAIN);
+            break;
+          }
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp < 2 + kEpiWarps) {
+    // --------------------------------------------------------- epilogue
+    const int q = warp & 3;  // tensor-memory lane quarter this warp may read
+    uint8_t* stage_base = sC + (warp - 2) * 2 * 4096;
+    int acc = 0, sbuf = 0;
+    uint32_t acc_phase = 0;
+    const int out_fmt = args.out_fmt;
+    const int es = out_fmt == OUT_F32 ? 4 : 2;
+    const bool tma_store = args.store_granule == 0;
+    for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+      int mb, nb;
+      tile_coords(t, args, mb, nb);
+      if (!warp_wait(ptx::smem_u32(&acc_full[acc]), acc_phase, ctl, SITE_EPI_ACC_FULL)) break;
+      ptx::tc_fence_after_sync();
+      const int row = mb * kTileM + q * 32 + lane;
+      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
+      // one chunk = 128 bytes of output per row: 32 fp32 or 64 16-bit columns
+      const int cols_per_chunk = 128 / es;
+#pragma unroll 1
+      for (int c = 0; c < BN / cols_per_chunk; ++c) {
+        uint32_t w[32];
+        if (out_fmt == OUT_F32) {
+          ptx::tmem_ld_32x32b_x32(tbase + c * 32, w);
+          ptx::tmem_wait_ld();
+        } else {
+          uint32_t lo[32], hi[32];
+          ptx::tmem_ld_32x32b_x32(tbase + c * 64, lo);
+          ptx::tmem_ld_32x32b_x32(tbase + c * 64 + 32, hi);
+          ptx::tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            w[i] = pack_pair(__uint_as_float(lo[2 * i]), __uint_as_float(lo[2 * i + 1]), out_fmt);
+            w[16 + i] = pack_pair(__uint_as_float(hi[2 * i]), __uint_as_float(hi[2 * i + 1]), out_fmt);
+          }
+        }
+        const int col0 = nb * BN + c * cols_per_chunk;
+        if (tma_store) {
+          uint8_t* buf = stage_base + sbuf * 4096;
+          if (lane == 0) ptx::bulk_wait_group_read<1>();
+          __syncwarp();
+#pragma unroll
+          for (int ch = 0; ch < 8; ++ch)
+            *reinterpret_cast<uint4*>(buf + sw128_offset(lane, ch * 16)) =
+                make_uint4(w[4 * ch], w[4 * ch + 1], w[4 * ch + 2], w[4 * ch + 3]);
+          ptx::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            ptx::tma_store_2d(&mapC, col0, mb * kTileM + q * 32, ptx::smem_u32(buf));
+            ptx::bulk_commit_group();
+          }
+          sbuf ^= 1;
+        } else if (row < args.M && col0 < args.N) {
+          uint8_t* dst = static_cast<uint8_t*>(args.C) + (static_cast<int64_t>(row) * args.ldc + col0) * es;
+          const int valid = min(args.N - col0, cols_per_chunk) * es;
+          store_segment(dst, w, valid, args.store_granule, es);
+        }
+      }
+      // this warp's reads of the accumulator buffer are complete
+      ptx::tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&acc_empty[acc]));
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+    if (lane == 0) ptx::bulk_wait_group<0>();
+    __syncwarp();
+  } else if constexpr (kCopy) {
+    // -------------------------------------------------- copy producers
+    const int ct = threadIdx.x - (2 + kEpiWarps) * 32;
+    if (has_copy && !args.inject_fault) {
+      int stage = 0, pending = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+        int mb, nb;
+        tile_coords(t, args, mb, nb);
+        for (int kb = 0; kb < kbs; ++kb) {
+          if (!warp_wait(ptx::smem_u32(&empty[stage]), phase ^ 1u, ctl, SITE_COPY_EMPTY)) {
+            ok = false;
+            break;
+          }
+          if (args.a_copy) copy_a_dispatch(sA + stage * A_BYTES, args, mb * kTileM, kb * kTileK, ct);
+          if (args.b_copy) copy_b_dispatch<BN>(sB + stage * B_BYTES, args, kb * kTileK, nb * BN, ct);
+          ptx::cp_async_commit();
+          if (pending == kCopyLag) {
+            ptx::cp_async_wait<kCopyLag>();
+            ptx::fence_proxy_async_smem();
+            ptx::mbar_arrive(ptx::smem_u32(&full_copy[(stage + STAGES - kCopyLag) % STAGES]));
+          } else {
+            ++pending;
+          }
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      ptx::cp_async_wait<0>();
+      ptx::fence_proxy_async_smem();
+      if (ok)
+        for (int j = pending; j >= 1; --j) ptx::mbar_arrive(ptx::smem_u32(&full_copy[(stage + STAGES - j) % STAGES]));
+    }
+  }
+
+  // ------------------------------------------------------------- teardown
+  ptx::tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after_sync();
+    ptx::tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+__global__ void zero_fill_kernel(uint8_t* C, int64_t rows, int64_t row_bytes, int64_t ld_bytes) {
+  const int64_t total = rows * row_bytes;
+  for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < total; i += int64_t(gridDim.x) * blockDim.x) {
+    const int64_t r = i / row_bytes, b = i % row_bytes;
+    C[r * ld_bytes + b] = 0;
+  }
+}
+
+template <int BN, bool kCopy>
+cudaError_t launch_one(const CUtensorMap& mA, const CUtensorMap& mB, const CUtensorMap& mC, const TcArgs& args,
+                       int ctas, cudaStream_t stream) {
+  constexpr int smem = tc_smem_bytes(BN);
+  auto kernel = tc_gemm_kernel<BN, kCopy>;
+  // The attribute is per device; set it on every device the first time.
+  static std::atomic<uint64_t> done_mask{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = 1ull << (dev & 63);
+  if (!(done_mask.load(std::memory_order_acquire) & bit)) {
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    done_mask.fetch_or(bit, std::memory_order_acq_rel);
+  }
+  kernel<<<ctas, tc_threads(kCopy), smem, stream>>>(mA, mB, mC, args);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_tc(int bn, bool copy, const CUtensorMap& mA, const CUtensorMap& mB, const CUtensorMap& mC,
+                      const TcArgs& args, int ctas, cudaStream_t stream) {
+  if (copy) {
+    switch (bn) {
+      case 256: return launch_one<256, true>(mA, mB, mC, args, ctas, stream);
+      case 128: return launch_one<128, true>(mA, mB, mC, args, ctas, stream);
+      default: return launch_one<64, true>(mA, mB, mC, args, ctas, stream);
+    }
+  }
+  switch (bn) {
+    case 256: return launch_one<256, false>(mA, mB, mC, args, ctas, stream);
+    case 128: return launch_one<128, false>(mA, mB, mC, args, ctas, stream);
+    default: return launch_one<64, false>(mA, mB, mC, args, ctas, stream);
+  }
+}
+
+cudaError_t launch_zero_fill(void* C, int64_t rows, int64_t cols, int64_t ldc, int elem_bytes, cudaStream_t stream) {
+  const int64_t total = rows * cols * elem_bytes;
+  int blocks = static_cast<int>(std::min<int64_t>((total + 255) / 256, 4096));
+  if (blocks < 1) blocks = 1;
+  zero_fill_kernel<<<blocks, 256, 0, stream>>>(static_cast<uint8_t*>(C), rows, cols * elem_bytes, ldc * elem_bytes);
+  return cudaGetLastError();
+}
+
+}  // namespace tgemm

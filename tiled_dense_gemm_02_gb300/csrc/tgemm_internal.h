@@ -1,0 +1,80 @@
+// Internal interfaces between the host dispatcher (api.cu) and the kernels.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace tgemm {
+
+// Output formats of the tensor-core epilogue.
+enum OutFmt : int { OUT_F32 = 0, OUT_F16 = 1, OUT_BF16 = 2 };
+
+// Device-side status codes written by bounded waits (0 = none).  The low byte
+// names the wait that gave up.
+enum WaitSite : uint32_t {
+  SITE_PRODUCER_EMPTY = 1,
+  SITE_MMA_FULL = 2,
+  SITE_MMA_ACC_EMPTY = 3,
+  SITE_EPI_ACC_FULL = 4,
+  SITE_COPY_EMPTY = 5,
+  SITE_DRAIN = 6,
+  SITE_TEARDOWN = 7,
+};
+constexpr uint32_t kTimeoutFlag = 0x7E000000u;
+
+struct TcArgs {
+  int M, N, K;
+  int tiles_m, tiles_n, num_tiles, k_blocks;
+  int group_m;
+  const void* A;
+  int64_t lda;
+  const void* B;
+  int64_t ldb;
+  void* C;
+  int64_t ldc;
+  uint32_t idesc;       // tcgen05 instruction descriptor (kind::f16)
+  int out_fmt;          // OutFmt
+  int a_copy;           // granule (bytes) of A's per-thread copies; 0 = TMA
+  int b_copy;           // granule (bytes) of B's per-thread copies; 0 = TMA
+  int store_granule;    // granule (bytes) of per-thread C stores; 0 = TMA store
+  int inject_fault;
+  unsigned long long timeout_ns;
+  unsigned int* status; // device status word
+};
+
+struct SimtArgs {
+  int M, N, K;
+  const float* A;
+  int64_t lda;
+  const float* B;
+  int64_t ldb;
+  float* C;
+  int64_t ldc;
+  int vec;              // 1 when A/B/C rows allow 16-byte vector accesses
+};
+
+// Tile shapes of the tensor-core kernel.
+constexpr int kTileM = 128;
+constexpr int kTileK = 64;
+constexpr int kEpiWarps = 4;
+constexpr int kCopyWarps = 4;
+
+constexpr int tc_stages(int bn) { return bn == 256 ? 4 : (bn == 128 ? 6 : 8); }
+constexpr int tc_smem_bytes(int bn) {
+  return 1024 + tc_stages(bn) * (kTileM * kTileK * 2 + kTileK * bn * 2) + kEpiWarps * 2 * 4096 + 256;
+}
+constexpr int tc_threads(bool copy) { return 32 * (2 + kEpiWarps + (copy ? kCopyWarps : 0)); }
+
+// Launchers (return the cudaError_t of the launch).
+cudaError_t launch_tc(int bn, bool copy, const CUtensorMap& mapA, const CUtensorMap& mapB, const CUtensorMap& mapC,
+                      const TcArgs& args, int ctas, cudaStream_t stream);
+cudaError_t launch_simt(const SimtArgs& args, cudaStream_t stream);
+cudaError_t launch_zero_fill(void* C, int64_t rows, int64_t cols, int64_t ldc, int elem_bytes, cudaStream_t stream);
+
+// SIMT tile shape.
+constexpr int kSimtBM = 128;
+constexpr int kSimtBN = 128;
+constexpr int kSimtBK = 8;
+
+}  // namespace tgemm
