@@ -103,7 +103,8 @@ enum tgemm_kernel {
  * field means "the default". */
 typedef struct tgemm_options {
   int kernel;           /* enum tgemm_kernel */
-  int tile_n;           /* tensor-core tile width: 0 (auto), 64, 128 or 256 */
+  int tile_n;           /* tensor-core tile width: 0 (auto), 64, 128, 192,
+                           224 or 256 */
   int group_m;          /* rasterisation group height in tiles (0 = auto) */
   int max_ctas;         /* cap on persistent CTAs (0 = one per SM) */
   int store_mode;       /* 0 auto, 1 bulk-tensor store, 2 per-thread stores */

@@ -74,6 +74,7 @@ def test_validation_errors(tg):
     assert plan(tg, 4, 4, 4, C=B0)[0] == tg.ERR_ALIAS
     assert plan(tg, 1 << 31, 4, 4)[0] == tg.ERR_TOO_LARGE
     assert plan(tg, 4, 4, 4, tile_n=96)[0] == tg.ERR_INVALID_VALUE
+    assert plan(tg, 4, 4, 4, tile_n=160)[0] == tg.ERR_INVALID_VALUE
     assert plan(tg, 4, 4, 4, dtype=0, kernel=tg.KERNEL_TC_TMA)[0] == tg.ERR_INVALID_VALUE
     assert plan(tg, 4, 4, 4, dtype=2, kernel=tg.KERNEL_SIMT)[0] == tg.ERR_INVALID_VALUE
     # TMA forced on rows that are not 16-byte aligned
@@ -137,3 +138,10 @@ def test_tile_width_choice_fills_the_sms(tg):
     assert p.tiles_m * p.tiles_n >= 100
     st, p = plan(tg, 8192, 8192, 8192, dtype=2, sms=148)
     assert p.tile_n == 256
+    # 4096^3 on 152 SMs: 256-wide tiles (4 rounds) beat 224-wide ones (4 full
+    # rounds of a less efficient tile) as measured
+    st, p = plan(tg, 4096, 4096, 4096, dtype=3, sms=152)
+    assert p.tile_n == 256
+    for bn in (64, 128, 192, 224, 256):
+        st, p = plan(tg, 512, 512, 512, tile_n=bn)
+        assert st == tg.OK and p.smem_bytes <= 232448 and p.stages >= 3

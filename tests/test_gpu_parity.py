@@ -67,7 +67,7 @@ def test_shape_sweep_auto(shape, dtype):
     H.check_full(res, A, B, M, N, K, dtype, f"{shape} {wl.DTYPE_NAMES[dtype]}")
 
 
-@pytest.mark.parametrize("tile_n", [64, 128, 256])
+@pytest.mark.parametrize("tile_n", [64, 128, 192, 224, 256])
 @pytest.mark.parametrize("store_mode", [1, 2])
 @pytest.mark.parametrize("dtype", TC_DTYPES, ids=lambda d: wl.DTYPE_NAMES[d])
 def test_tile_widths_and_store_modes(tile_n, store_mode, dtype):
@@ -78,7 +78,7 @@ def test_tile_widths_and_store_modes(tile_n, store_mode, dtype):
     H.check_full(res, A, B, M, N, K, dtype, f"tile_n {tile_n} store {store_mode}")
 
 
-@pytest.mark.parametrize("tile_n", [64, 128, 256])
+@pytest.mark.parametrize("tile_n", [64, 128, 192, 224, 256])
 @pytest.mark.parametrize("dtype", [wl.BF16, wl.F16_F32OUT], ids=lambda d: wl.DTYPE_NAMES[d])
 def test_copy_producer_on_aligned_rows(tile_n, dtype):
     """Force the per-thread-copy producer (16-byte granules) on aligned data."""
@@ -127,7 +127,8 @@ def test_persistent_scheduler(max_ctas, group_m):
 def test_k_block_counts(K):
     """K around multiples of the 64-wide stage and of the ring depth."""
     M, N = 130, 260
-    for dtype, opts in ((wl.BF16_F32OUT, {"tile_n": 256}), (wl.F16, {"tile_n": 64}), (wl.F32, None)):
+    for dtype, opts in ((wl.BF16_F32OUT, {"tile_n": 256}), (wl.F16, {"tile_n": 64}), (wl.BF16, {"tile_n": 224}),
+                        (wl.F16_F32OUT, {"tile_n": 192}), (wl.F32, None)):
         A, B, res = case(M, N, K, dtype, seed=27, options=opts)
         H.check_full(res, A, B, M, N, K, dtype, f"K {K} {wl.DTYPE_NAMES[dtype]}")
 

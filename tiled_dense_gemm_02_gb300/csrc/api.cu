@@ -107,17 +107,30 @@ struct Plan {
   int smem = 0;
 };
 
-// Relative MMA issue efficiency of the tile widths (shared-memory operand
-// bandwidth per FLOP grows as the tile narrows).
-double width_rate(int bn) { return bn == 256 ? 1.0 : (bn == 128 ? 0.92 : 0.7); }
+// Relative throughput of one SM per output column for each tile width,
+// measured on GB300 with bf16 4096^3 (per-wave time of one 128 x BN tile):
+// operand traffic per FLOP grows as the tile narrows, and the 224-wide tile
+// still moves four 64-column B atoms.
+double width_rate(int bn) {
+  switch (bn) {
+    case 256: return 1.0;
+    case 224: return 0.86;
+    case 192: return 0.8;
+    case 128: return 0.65;
+    default: return 0.34;
+  }
+}
 
+// Tile width minimising (waves x width / rate): the persistent grid runs
+// ceil(tiles / SMs) rounds of BN-wide tiles.
 int pick_tile_n(int64_t M, int64_t N, int64_t K, int sms) {
+  (void)K;
   int best = 256;
   double best_t = 1e300;
-  for (int bn : {256, 128, 64}) {
+  for (int bn : {256, 224, 192, 128, 64}) {
     const int64_t tiles = ((M + kTileM - 1) / kTileM) * ((N + bn - 1) / bn);
     const int64_t waves = (tiles + sms - 1) / sms;
-    const double t = static_cast<double>(waves) * bn * static_cast<double>(std::max<int64_t>(K, 1)) / width_rate(bn);
+    const double t = static_cast<double>(waves) * bn / width_rate(bn);
     if (t < best_t * 0.999) {
       best_t = t;
       best = bn;
@@ -137,7 +150,7 @@ int make_plan(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const
   std::memset(&opt, 0, sizeof opt);
   if (o) opt = *o;
   if (opt.kernel < TGEMM_KERNEL_AUTO || opt.kernel > TGEMM_KERNEL_SIMT) return TGEMM_ERR_INVALID_VALUE;
-  if (opt.tile_n != 0 && opt.tile_n != 64 && opt.tile_n != 128 && opt.tile_n != 256) return TGEMM_ERR_INVALID_VALUE;
+  if (opt.tile_n != 0 && !tc_valid_bn(opt.tile_n)) return TGEMM_ERR_INVALID_VALUE;
   if (opt.group_m < 0 || opt.max_ctas < 0 || opt.store_mode < 0 || opt.store_mode > 2 || opt.wait_timeout_us < 0)
     return TGEMM_ERR_INVALID_VALUE;
   if (M == 0 || N == 0) {
@@ -207,7 +220,7 @@ int make_plan(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const
   p.tiles_n = static_cast<int>((N + p.bn - 1) / p.bn);
   const int64_t tiles = int64_t(p.tiles_m) * p.tiles_n;
   if (tiles >= (int64_t(1) << 31)) return TGEMM_ERR_TOO_LARGE;
-  p.group_m = opt.group_m ? opt.group_m : 16;
+  p.group_m = opt.group_m ? opt.group_m : 8;
   p.group_m = std::max(1, std::min(p.group_m, p.tiles_m));
   int64_t ctas = std::min<int64_t>(tiles, std::max(1, sms));
   if (opt.max_ctas) ctas = std::min<int64_t>(ctas, opt.max_ctas);

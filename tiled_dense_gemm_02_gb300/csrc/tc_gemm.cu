@@ -41,7 +41,6 @@
 namespace tgemm {
 namespace {
 
-constexpr int kCopyLag = 2;  // stages a copy producer keeps in flight before signalling
 
 struct Ctl {
   volatile uint32_t* abort;
@@ -212,10 +211,14 @@ __global__ void __launch_bounds__(tc_threads(kCopy), 1)
                    const __grid_constant__ CUtensorMap mapC, const TcArgs args) {
   constexpr int STAGES = tc_stages(BN);
   constexpr int A_BYTES = kTileM * kTileK * 2;
-  constexpr int B_BYTES = kTileK * BN * 2;
-  constexpr uint32_t TMEM_COLS = 2 * BN;
-  static_assert(BN == 64 || BN == 128 || BN == 256, "tile width");
-  static_assert(tc_smem_bytes(BN) <= 232448, "shared memory per CTA");
+  constexpr int B_BYTES = tc_b_atoms(BN) * 8192;
+  constexpr int ACC = tc_acc_stride(BN);
+  constexpr uint32_t TMEM_COLS = 2 * ACC;
+  // copy producers signal a stage once the copies LAG stages later are issued
+  constexpr int LAG = STAGES - 2;
+  static_assert(tc_valid_bn(BN), "tile width");
+  static_assert(STAGES >= 3 && LAG >= 1, "ring depth");
+  static_assert(tc_smem_bytes(BN) <= kSmemLimit, "shared memory per CTA");
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -289,7 +292,7 @@ __global__ void __launch_bounds__(tc_threads(kCopy), 1)
           if (a_tma) ptx::tma_load_2d(ptx::smem_u32(sA + stage * A_BYTES), &mapA, kb * kTileK, mb * kTileM, fb);
           if (b_tma) {
 #pragma unroll
-            for (int j = 0; j < BN / 64; ++j)
+            for (int j = 0; j < tc_b_atoms(BN); ++j)
               ptx::tma_load_2d(ptx::smem_u32(sB + stage * B_BYTES + j * 8192), &mapB, nb * BN + j * 64, kb * kTileK,
                                fb);
           }
@@ -328,7 +331,7 @@ __global__ void __launch_bounds__(tc_threads(kCopy), 1)
       for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
         if (!wait_bounded(ptx::smem_u32(&acc_empty[acc]), acc_phase ^ 1u, ctl, SITE_MMA_ACC_EMPTY)) break;
         ptx::tc_fence_after_sync();
-        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * ACC);
         for (int kb = 0; kb < kbs; ++kb) {
           if (has_tma && !wait_bounded(ptx::smem_u32(&full_tma[stage]), phase, ctl, SITE_MMA_FULL)) {
             ok = false;
@@ -389,28 +392,32 @@ __global__ void __launch_bounds__(tc_threads(kCopy), 1)
       if (!warp_wait(ptx::smem_u32(&acc_full[acc]), acc_phase, ctl, SITE_EPI_ACC_FULL)) break;
       ptx::tc_fence_after_sync();
       const int row = mb * kTileM + q * 32 + lane;
-      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
-      // one chunk = 128 bytes of output per row: 32 fp32 or 64 16-bit columns
+      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * ACC);
+      // one chunk = 128 bytes of output per row: 32 fp32 or 64 16-bit columns;
+      // with 16-bit output and BN % 64 == 32 the last chunk is 32 columns wide
       const int cols_per_chunk = 128 / es;
+      const int chunks = (BN + cols_per_chunk - 1) / cols_per_chunk;
 #pragma unroll 1
-      for (int c = 0; c < BN / cols_per_chunk; ++c) {
+      for (int c = 0; c < chunks; ++c) {
+        const int col_in_tile = c * cols_per_chunk;
+        const bool half = col_in_tile + cols_per_chunk > BN;  // only 16-bit output, BN = 224
         uint32_t w[32];
         if (out_fmt == OUT_F32) {
-          ptx::tmem_ld_32x32b_x32(tbase + c * 32, w);
+          ptx::tmem_ld_32x32b_x32(tbase + col_in_tile, w);
           ptx::tmem_wait_ld();
         } else {
           uint32_t lo[32], hi[32];
-          ptx::tmem_ld_32x32b_x32(tbase + c * 64, lo);
-          ptx::tmem_ld_32x32b_x32(tbase + c * 64 + 32, hi);
+          ptx::tmem_ld_32x32b_x32(tbase + col_in_tile, lo);
+          if (!half) ptx::tmem_ld_32x32b_x32(tbase + col_in_tile + 32, hi);
           ptx::tmem_wait_ld();
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             w[i] = pack_pair(__uint_as_float(lo[2 * i]), __uint_as_float(lo[2 * i + 1]), out_fmt);
-            w[16 + i] = pack_pair(__uint_as_float(hi[2 * i]), __uint_as_float(hi[2 * i + 1]), out_fmt);
+            w[16 + i] = half ? 0u : pack_pair(__uint_as_float(hi[2 * i]), __uint_as_float(hi[2 * i + 1]), out_fmt);
           }
         }
-        const int col0 = nb * BN + c * cols_per_chunk;
-        if (tma_store) {
+        const int col0 = nb * BN + col_in_tile;
+        if (tma_store && !half) {
           uint8_t* buf = stage_base + sbuf * 4096;
           if (lane == 0) ptx::bulk_wait_group_read<1>();
           __syncwarp();
@@ -427,8 +434,10 @@ __global__ void __launch_bounds__(tc_threads(kCopy), 1)
           sbuf ^= 1;
         } else if (row < args.M && col0 < args.N) {
           uint8_t* dst = static_cast<uint8_t*>(args.C) + (static_cast<int64_t>(row) * args.ldc + col0) * es;
-          const int valid = min(args.N - col0, cols_per_chunk) * es;
-          store_segment(dst, w, valid, args.store_granule, es);
+          const int width = half ? 32 : cols_per_chunk;
+          const int valid = min(args.N - col0, width) * es;
+          // the half chunk's rows are 16-byte aligned whenever bulk stores are on
+          store_segment(dst, w, valid, tma_store ? 16 : args.store_granule, es);
         }
       }
       // this warp's reads of the accumulator buffer are complete
@@ -458,10 +467,10 @@ __global__ void __launch_bounds__(tc_threads(kCopy), 1)
           if (args.a_copy) copy_a_dispatch(sA + stage * A_BYTES, args, mb * kTileM, kb * kTileK, ct);
           if (args.b_copy) copy_b_dispatch<BN>(sB + stage * B_BYTES, args, kb * kTileK, nb * BN, ct);
           ptx::cp_async_commit();
-          if (pending == kCopyLag) {
-            ptx::cp_async_wait<kCopyLag>();
+          if (pending == LAG) {
+            ptx::cp_async_wait<LAG>();
             ptx::fence_proxy_async_smem();
-            ptx::mbar_arrive(ptx::smem_u32(&full_copy[(stage + STAGES - kCopyLag) % STAGES]));
+            ptx::mbar_arrive(ptx::smem_u32(&full_copy[(stage + STAGES - LAG) % STAGES]));
           } else {
             ++pending;
           }
@@ -519,18 +528,19 @@ cudaError_t launch_one(const CUtensorMap& mA, const CUtensorMap& mB, const CUten
 
 cudaError_t launch_tc(int bn, bool copy, const CUtensorMap& mA, const CUtensorMap& mB, const CUtensorMap& mC,
                       const TcArgs& args, int ctas, cudaStream_t stream) {
-  if (copy) {
-    switch (bn) {
-      case 256: return launch_one<256, true>(mA, mB, mC, args, ctas, stream);
-      case 128: return launch_one<128, true>(mA, mB, mC, args, ctas, stream);
-      default: return launch_one<64, true>(mA, mB, mC, args, ctas, stream);
-    }
-  }
+#define TGEMM_LAUNCH_BN(BNV)                                                                       \
+  case BNV:                                                                                        \
+    return copy ? launch_one<BNV, true>(mA, mB, mC, args, ctas, stream)                            \
+                : launch_one<BNV, false>(mA, mB, mC, args, ctas, stream);
   switch (bn) {
-    case 256: return launch_one<256, false>(mA, mB, mC, args, ctas, stream);
-    case 128: return launch_one<128, false>(mA, mB, mC, args, ctas, stream);
-    default: return launch_one<64, false>(mA, mB, mC, args, ctas, stream);
+    TGEMM_LAUNCH_BN(64)
+    TGEMM_LAUNCH_BN(128)
+    TGEMM_LAUNCH_BN(192)
+    TGEMM_LAUNCH_BN(224)
+    TGEMM_LAUNCH_BN(256)
+    default: return cudaErrorInvalidValue;
   }
+#undef TGEMM_LAUNCH_BN
 }
 
 cudaError_t launch_zero_fill(void* C, int64_t rows, int64_t cols, int64_t ldc, int elem_bytes, cudaStream_t stream) {

@@ -54,16 +54,28 @@ struct SimtArgs {
   int vec;              // 1 when A/B/C rows allow 16-byte vector accesses
 };
 
-// Tile shapes of the tensor-core kernel.
+// Tile shapes of the tensor-core kernel: 128 x BN output tiles, K stages of
+// 64.  BN is one of 64, 128, 192, 224, 256; B is staged in 64-column atoms of
+// 8 KB (the last atom of BN = 224 is half used).
 constexpr int kTileM = 128;
 constexpr int kTileK = 64;
 constexpr int kEpiWarps = 4;
 constexpr int kCopyWarps = 4;
+constexpr int kSmemLimit = 232448;                 // opt-in shared memory per CTA
+constexpr int kEpiBytes = kEpiWarps * 2 * 4096;    // epilogue staging
+constexpr int kBarrierBytes = 256;
 
-constexpr int tc_stages(int bn) { return bn == 256 ? 4 : (bn == 128 ? 6 : 8); }
-constexpr int tc_smem_bytes(int bn) {
-  return 1024 + tc_stages(bn) * (kTileM * kTileK * 2 + kTileK * bn * 2) + kEpiWarps * 2 * 4096 + 256;
+constexpr bool tc_valid_bn(int bn) { return bn == 64 || bn == 128 || bn == 192 || bn == 224 || bn == 256; }
+constexpr int tc_b_atoms(int bn) { return (bn + 63) / 64; }
+constexpr int tc_stage_bytes(int bn) { return kTileM * kTileK * 2 + tc_b_atoms(bn) * 8192; }
+constexpr int tc_stages(int bn) {
+  return (kSmemLimit - 1024 - kEpiBytes - kBarrierBytes) / tc_stage_bytes(bn) > 8
+             ? 8
+             : (kSmemLimit - 1024 - kEpiBytes - kBarrierBytes) / tc_stage_bytes(bn);
 }
+constexpr int tc_smem_bytes(int bn) { return 1024 + tc_stages(bn) * tc_stage_bytes(bn) + kEpiBytes + kBarrierBytes; }
+// Tensor-memory columns between the two accumulator buffers (a power of two).
+constexpr int tc_acc_stride(int bn) { return bn <= 64 ? 64 : (bn <= 128 ? 128 : 256); }
 constexpr int tc_threads(bool copy) { return 32 * (2 + kEpiWarps + (copy ? kCopyWarps : 0)); }
 
 // Launchers (return the cudaError_t of the launch).
