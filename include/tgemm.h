@@ -113,7 +113,11 @@ typedef struct tgemm_options {
                            stage, so the consumers' bounded waits run out and
                            the kernel exits with TGEMM_ERR_DEVICE_TIMEOUT
                            pending; no copy is ever issued */
-  int reserved[9];
+  int cta_group;        /* tensor-core tiles per CTA (0 auto): 1 = 128 x N
+                           tiles on one SM, 2 = 256 x N tiles on a pair of
+                           SMs (a 2-CTA cluster; bulk-tensor operands only,
+                           tile_n 128, 192, 224 or 256) */
+  int reserved[8];
 } tgemm_options;
 
 /* tgemm_gemm with explicit options (opts may be NULL).  A forced kernel that
@@ -139,7 +143,9 @@ typedef struct tgemm_plan_info {
   int b_copy_bytes;  /* granule of B's per-thread copies (0 = bulk-tensor) */
   int store_bytes;   /* granule of C's per-thread stores (0 = bulk-tensor) */
   int smem_bytes;    /* dynamic shared memory per CTA */
-  int reserved[4];
+  int cta_group;     /* 1: one SM per tile; 2: a CTA pair per 256-row tile
+                        (tile_m is then 256 and ctas counts CTAs, two per pair) */
+  int reserved[3];
 } tgemm_plan_info;
 
 TGEMM_API int tgemm_plan(int64_t M, int64_t N, int64_t K,

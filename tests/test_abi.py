@@ -95,8 +95,8 @@ def test_dispatch_aligned_uses_bulk_tensor_copies(tg):
     st, p = plan(tg, 4096, 4096, 4096, dtype=3, sms=148)
     assert st == tg.OK
     assert p.kernel == tg.KERNEL_TC_TMA and p.a_copy_bytes == 0 and p.b_copy_bytes == 0 and p.store_bytes == 0
-    assert (p.tile_m, p.tile_k) == (128, 64)
-    assert p.tiles_m * 128 >= 4096 and p.tiles_n * p.tile_n >= 4096
+    assert p.tile_m in (128, 256) and p.tile_k == 64
+    assert p.tiles_m * p.tile_m >= 4096 and p.tiles_n * p.tile_n >= 4096
     assert p.ctas == min(148, p.tiles_m * p.tiles_n)
     assert p.smem_bytes <= 232448
 
@@ -120,6 +120,21 @@ def test_bulk_store_needs_16_byte_row_extent(tg):
     assert plan(tg, 260, 388, 304, ldc=392, ldb=392, dtype=3)[1].store_bytes == 0   # fp32: 1552 bytes
 
 
+def test_pair_planning(tg):
+    st, p = plan(tg, 4096, 4096, 4096, dtype=3, sms=152)
+    assert st == tg.OK and p.cta_group == 2 and p.tile_m == 256 and p.ctas % 2 == 0 and p.ctas <= 152
+    st, p = plan(tg, 4096, 4096, 4096, dtype=3, sms=152, cta_group=1)
+    assert p.cta_group == 1 and p.tile_m == 128
+    st, p = plan(tg, 300, 520, 200, dtype=2, cta_group=2, tile_n=224)
+    assert st == tg.OK and (p.tiles_m, p.tiles_n, p.ctas) == (2, 3, 12)
+    # pairs need bulk-tensor operands and a pair width
+    assert plan(tg, 1000, 1500, 4096, dtype=2, cta_group=2)[0] == tg.ERR_INVALID_VALUE
+    assert plan(tg, 512, 512, 512, dtype=2, cta_group=2, tile_n=64)[0] == tg.ERR_INVALID_VALUE
+    assert plan(tg, 512, 512, 512, dtype=2, cta_group=3)[0] == tg.ERR_INVALID_VALUE
+    st, p = plan(tg, 1100, 1300, 330, lda=336, ldb=1304, dtype=3, cta_group=2, tile_n=256, max_ctas=6)
+    assert st == tg.OK and p.ctas == 6
+
+
 def test_dispatch_options(tg):
     st, p = plan(tg, 1024, 1024, 1024, dtype=1, tile_n=64, max_ctas=5, group_m=3, store_mode=2)
     assert st == tg.OK
@@ -135,12 +150,12 @@ def test_dispatch_options(tg):
 def test_tile_width_choice_fills_the_sms(tg):
     # small problems should not leave most SMs idle with 256-wide tiles
     st, p = plan(tg, 1024, 1024, 1024, dtype=1, sms=148)
-    assert p.tiles_m * p.tiles_n >= 100
+    assert p.ctas >= 64
     st, p = plan(tg, 8192, 8192, 8192, dtype=2, sms=148)
-    assert p.tile_n == 256
-    # 4096^3 on 152 SMs: 256-wide tiles (4 rounds) beat 224-wide ones (4 full
-    # rounds of a less efficient tile) as measured
-    st, p = plan(tg, 4096, 4096, 4096, dtype=3, sms=152)
+    assert p.tile_n in (224, 256) and p.cta_group == 2
+    # one SM per tile at 4096^3 on 152 SMs: 256-wide tiles (4 rounds) beat
+    # 224-wide ones (4 full rounds of a less efficient tile) as measured
+    st, p = plan(tg, 4096, 4096, 4096, dtype=3, sms=152, cta_group=1)
     assert p.tile_n == 256
     for bn in (64, 128, 192, 224, 256):
         st, p = plan(tg, 512, 512, 512, tile_n=bn)

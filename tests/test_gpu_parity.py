@@ -111,6 +111,41 @@ def test_leading_dimensions(lds, dtype):
     H.check_full(res, A, B, M, N, K, dtype, f"lds {lds}")
 
 
+# ------------------------------------------------------------ CTA-pair kernel
+
+@pytest.mark.parametrize("tile_n", [128, 192, 224, 256])
+@pytest.mark.parametrize("dtype", TC_DTYPES, ids=lambda d: wl.DTYPE_NAMES[d])
+def test_pair_kernel(tile_n, dtype):
+    """256 x tile_n tiles on CTA pairs: ragged M (two pair tiles, the second
+    44 rows), ragged N and a K tail."""
+    M, N, K = 300, 520, 200
+    A, B, res = case(M, N, K, dtype, seed=34, options={"cta_group": 2, "tile_n": tile_n})
+    assert res.plan.cta_group == 2 and res.plan.tile_m == 256 and res.plan.tile_n == tile_n
+    H.check_full(res, A, B, M, N, K, dtype, f"pair tile_n {tile_n}")
+
+
+@pytest.mark.parametrize("store_mode", [1, 2])
+@pytest.mark.parametrize("max_ctas", [2, 6, 0])
+def test_pair_kernel_persistent(store_mode, max_ctas):
+    """One or three pairs walking many 256 x 256 tiles (every ring and
+    accumulator phase), and the full grid."""
+    M, N, K = 1100, 1300, 330
+    A, B, res = case(M, N, K, wl.BF16_F32OUT, seed=35, lda=336, ldb=1304,
+                     options={"cta_group": 2, "tile_n": 256, "max_ctas": max_ctas, "store_mode": store_mode})
+    assert res.plan.cta_group == 2
+    if max_ctas:
+        assert res.plan.ctas == max_ctas
+    H.check_full(res, A, B, M, N, K, wl.BF16_F32OUT, f"pair ctas {max_ctas} store {store_mode}")
+
+
+@pytest.mark.parametrize("K", [16, 64, 65, 384, 385])
+def test_pair_kernel_k_depths(K):
+    M, N = 257, 260
+    lda = (K + 7) // 8 * 8   # 16-byte rows for the bulk-tensor loads of the pair kernel
+    A, B, res = case(M, N, K, wl.BF16, seed=36, lda=lda, ldb=264, options={"cta_group": 2, "tile_n": 128})
+    H.check_full(res, A, B, M, N, K, wl.BF16, f"pair K {K}")
+
+
 # ------------------------------------------------------- scheduler and edges
 
 @pytest.mark.parametrize("max_ctas,group_m", [(1, 1), (3, 2), (5, 16), (7, 3)])

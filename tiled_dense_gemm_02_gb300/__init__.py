@@ -32,7 +32,7 @@ class Options(ctypes.Structure):
     """struct tgemm_options"""
     _fields_ = [("kernel", ctypes.c_int), ("tile_n", ctypes.c_int), ("group_m", ctypes.c_int),
                 ("max_ctas", ctypes.c_int), ("store_mode", ctypes.c_int), ("wait_timeout_us", ctypes.c_int),
-                ("inject_fault", ctypes.c_int), ("reserved", ctypes.c_int * 9)]
+                ("inject_fault", ctypes.c_int), ("cta_group", ctypes.c_int), ("reserved", ctypes.c_int * 8)]
 
 
 class PlanInfo(ctypes.Structure):
@@ -41,7 +41,7 @@ class PlanInfo(ctypes.Structure):
                 ("tile_k", ctypes.c_int), ("stages", ctypes.c_int), ("tiles_m", ctypes.c_int),
                 ("tiles_n", ctypes.c_int), ("ctas", ctypes.c_int), ("group_m", ctypes.c_int),
                 ("a_copy_bytes", ctypes.c_int), ("b_copy_bytes", ctypes.c_int), ("store_bytes", ctypes.c_int),
-                ("smem_bytes", ctypes.c_int), ("reserved", ctypes.c_int * 4)]
+                ("smem_bytes", ctypes.c_int), ("cta_group", ctypes.c_int), ("reserved", ctypes.c_int * 3)]
 
     def as_dict(self) -> dict:
         return {name: getattr(self, name) for name, _ in self._fields_ if name != "reserved"}

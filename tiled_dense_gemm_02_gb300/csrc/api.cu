@@ -28,6 +28,7 @@ struct DeviceInfo {
   bool supported = false;
   int sm_count = 0;
   unsigned int* status = nullptr;
+  int pair_capacity = 0;  // resident CTA pairs of the pair kernel (0 = not queried)
 };
 
 std::mutex g_mutex;
@@ -102,6 +103,7 @@ bool ranges_overlap(uint64_t a0, uint64_t a1, uint64_t b0, uint64_t b1) { return
 struct Plan {
   int kernel = TGEMM_KERNEL_AUTO;
   bool noop = false, zero = false;
+  bool pair = false;
   int bn = 256, stages = 4, tiles_m = 0, tiles_n = 0, ctas = 0, group_m = 1;
   int a_copy = 0, b_copy = 0, store = 0;
   int smem = 0;
@@ -123,8 +125,7 @@ double width_rate(int bn) {
 
 // Tile width minimising (waves x width / rate): the persistent grid runs
 // ceil(tiles / SMs) rounds of BN-wide tiles.
-int pick_tile_n(int64_t M, int64_t N, int64_t K, int sms) {
-  (void)K;
+int pick_tile_n(int64_t M, int64_t N, int sms, double* cost) {
   int best = 256;
   double best_t = 1e300;
   for (int bn : {256, 224, 192, 128, 64}) {
@@ -136,11 +137,40 @@ int pick_tile_n(int64_t M, int64_t N, int64_t K, int sms) {
       best = bn;
     }
   }
+  if (cost) *cost = best_t;
+  return best;
+}
+
+// Per-SM throughput per output column of the pair kernel, in the units of
+// width_rate (each SM of a pair computes 128 x BN per tile), measured on GB300
+// with bf16 4096^3.
+double pair_rate(int bn) {
+  switch (bn) {
+    case 256: return 1.13;
+    case 224: return 0.99;
+    case 192: return 0.88;
+    default: return 0.64;
+  }
+}
+
+int pick_pair_tile_n(int64_t M, int64_t N, int pairs, double* cost) {
+  int best = 256;
+  double best_t = 1e300;
+  for (int bn : {256, 224, 192, 128}) {
+    const int64_t tiles = ((M + 2 * kTileM - 1) / (2 * kTileM)) * ((N + bn - 1) / bn);
+    const int64_t waves = (tiles + pairs - 1) / pairs;
+    const double t = static_cast<double>(waves) * bn / pair_rate(bn);
+    if (t < best_t * 0.999) {
+      best_t = t;
+      best = bn;
+    }
+  }
+  if (cost) *cost = best_t;
   return best;
 }
 
 int make_plan(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb,
-              const void* C, int64_t ldc, int dtype, const tgemm_options* o, int sms, Plan& p) {
+              const void* C, int64_t ldc, int dtype, const tgemm_options* o, int sms, int pair_cap, Plan& p) {
   if (dtype < TGEMM_F32 || dtype > TGEMM_F16_F32OUT) return TGEMM_ERR_UNSUPPORTED_DTYPE;
   if (M < 0 || N < 0 || K < 0) return TGEMM_ERR_INVALID_VALUE;
   if (M >= (int64_t(1) << 31) || N >= (int64_t(1) << 31) || K >= (int64_t(1) << 31)) return TGEMM_ERR_TOO_LARGE;
@@ -151,7 +181,8 @@ int make_plan(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const
   if (o) opt = *o;
   if (opt.kernel < TGEMM_KERNEL_AUTO || opt.kernel > TGEMM_KERNEL_SIMT) return TGEMM_ERR_INVALID_VALUE;
   if (opt.tile_n != 0 && !tc_valid_bn(opt.tile_n)) return TGEMM_ERR_INVALID_VALUE;
-  if (opt.group_m < 0 || opt.max_ctas < 0 || opt.store_mode < 0 || opt.store_mode > 2 || opt.wait_timeout_us < 0)
+  if (opt.group_m < 0 || opt.max_ctas < 0 || opt.store_mode < 0 || opt.store_mode > 2 || opt.wait_timeout_us < 0 ||
+      opt.cta_group < 0 || opt.cta_group > 2)
     return TGEMM_ERR_INVALID_VALUE;
   if (M == 0 || N == 0) {
     p.noop = true;
@@ -214,18 +245,44 @@ int make_plan(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const
   }
   if (opt.store_mode == 1 && !c_tma) return TGEMM_ERR_INVALID_VALUE;
   p.store = (c_tma && opt.store_mode != 2) ? 0 : gc;
-  p.bn = opt.tile_n ? opt.tile_n : pick_tile_n(M, N, K, sms);
-  p.stages = tc_stages(p.bn);
-  p.tiles_m = static_cast<int>((M + kTileM - 1) / kTileM);
+  // one SM per 128-row tile, or a CTA pair per 256-row tile (bulk-tensor
+  // operands only)
+  const bool pair_ok = p.kernel == TGEMM_KERNEL_TC_TMA && pair_cap > 0 &&
+                       (opt.tile_n == 0 || tc2_valid_bn(opt.tile_n));
+  if (opt.cta_group == 2 && !pair_ok) return TGEMM_ERR_INVALID_VALUE;
+  double cost1 = 0, cost2 = 1e300;
+  const int bn1 = opt.tile_n ? opt.tile_n : pick_tile_n(M, N, sms, &cost1);
+  int bn2 = 0;
+  if (pair_ok && opt.cta_group != 1) {
+    bn2 = opt.tile_n ? opt.tile_n : pick_pair_tile_n(M, N, pair_cap, &cost2);
+    if (opt.tile_n) {
+      const int64_t t1 = ((M + kTileM - 1) / kTileM) * ((N + bn1 - 1) / bn1);
+      const int64_t t2 = ((M + 2 * kTileM - 1) / (2 * kTileM)) * ((N + bn2 - 1) / bn2);
+      cost1 = static_cast<double>((t1 + sms - 1) / sms) * bn1 / width_rate(bn1);
+      cost2 = static_cast<double>((t2 + pair_cap - 1) / pair_cap) * bn2 / pair_rate(bn2);
+    }
+  }
+  p.pair = opt.cta_group == 2 || (opt.cta_group == 0 && bn2 != 0 && cost2 < cost1);
+  p.bn = p.pair ? bn2 : bn1;
+  p.stages = p.pair ? tc2_stages(p.bn) : tc_stages(p.bn);
+  const int tm = p.pair ? 2 * kTileM : kTileM;
+  p.tiles_m = static_cast<int>((M + tm - 1) / tm);
   p.tiles_n = static_cast<int>((N + p.bn - 1) / p.bn);
   const int64_t tiles = int64_t(p.tiles_m) * p.tiles_n;
   if (tiles >= (int64_t(1) << 31)) return TGEMM_ERR_TOO_LARGE;
   p.group_m = opt.group_m ? opt.group_m : 8;
   p.group_m = std::max(1, std::min(p.group_m, p.tiles_m));
-  int64_t ctas = std::min<int64_t>(tiles, std::max(1, sms));
-  if (opt.max_ctas) ctas = std::min<int64_t>(ctas, opt.max_ctas);
+  int64_t ctas;
+  if (p.pair) {
+    int64_t pairs = std::min<int64_t>(tiles, pair_cap);
+    if (opt.max_ctas) pairs = std::min<int64_t>(pairs, std::max(1, opt.max_ctas / 2));
+    ctas = 2 * pairs;
+  } else {
+    ctas = std::min<int64_t>(tiles, std::max(1, sms));
+    if (opt.max_ctas) ctas = std::min<int64_t>(ctas, opt.max_ctas);
+  }
   p.ctas = static_cast<int>(ctas);
-  p.smem = tc_smem_bytes(p.bn);
+  p.smem = p.pair ? tc2_smem_bytes(p.bn) : tc_smem_bytes(p.bn);
   return TGEMM_OK;
 }
 
@@ -252,16 +309,32 @@ int encode_2d(CUtensorMap* map, CUtensorMapDataType type, const void* base, int6
   return TGEMM_OK;
 }
 
+// Resident CTA pairs of the pair kernel on the current device (queried once;
+// the 256-wide instantiation stands for all widths, which use the same shared
+// memory and threads).  0 when the query fails: the pair kernel is then not used.
+int pair_capacity(DeviceInfo* d) {
+  std::lock_guard<std::mutex> lock(g_mutex);
+  if (d->pair_capacity == 0) {
+    int pairs = 0;
+    if (tc_pair_capacity(256, &pairs) != cudaSuccess || pairs < 1) {
+      cudaGetLastError();
+      pairs = -1;
+    }
+    d->pair_capacity = pairs;
+  }
+  return d->pair_capacity > 0 ? d->pair_capacity : 0;
+}
+
 int run(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb, void* C,
         int64_t ldc, int dtype, const tgemm_options* o, cudaStream_t stream) {
   // validation that needs no device first, so bad arguments never touch CUDA
   Plan p;
-  int st = make_plan(M, N, K, A, lda, B, ldb, C, ldc, dtype, o, 1, p);
+  int st = make_plan(M, N, K, A, lda, B, ldb, C, ldc, dtype, o, 1, 1, p);
   if (st != TGEMM_OK || p.noop) return st;
   DeviceInfo* dev = nullptr;
   st = device_info(&dev);
   if (st != TGEMM_OK) return st;
-  st = make_plan(M, N, K, A, lda, B, ldb, C, ldc, dtype, o, dev->sm_count, p);
+  st = make_plan(M, N, K, A, lda, B, ldb, C, ldc, dtype, o, dev->sm_count, pair_capacity(dev), p);
   if (st != TGEMM_OK) return st;
   cudaError_t e;
   if (p.zero) {
@@ -314,8 +387,9 @@ int run(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void*
   // kind::f16 instruction descriptor: D fp32 (bits 4-5 = 1), A/B format
   // (bits 7-9, 10-12), A K-major (bit 15 = 0), B N-major (bit 16 = 1),
   // N >> 3 (bits 17-22), M >> 4 (bits 24-28).
+  const uint32_t mma_m = p.pair ? 2 * kTileM : kTileM;
   a.idesc = (1u << 4) | (ab << 7) | (ab << 10) | (1u << 16) | (static_cast<uint32_t>(p.bn >> 3) << 17) |
-            (static_cast<uint32_t>(kTileM >> 4) << 24);
+            ((mma_m >> 4) << 24);
   a.out_fmt = eo == 4 ? OUT_F32 : (dtype == TGEMM_BF16 ? OUT_BF16 : OUT_F16);
   a.a_copy = p.a_copy;
   a.b_copy = p.b_copy;
@@ -324,7 +398,10 @@ int run(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void*
   const int to_us = (o && o->wait_timeout_us) ? o->wait_timeout_us : 2000000;
   a.timeout_ns = static_cast<unsigned long long>(to_us) * 1000ull;
   a.status = dev->status;
-  e = launch_tc(p.bn, p.kernel == TGEMM_KERNEL_TC_COPY, mA, mB, mC, a, p.ctas, stream);
+  if (p.pair)
+    e = launch_tc_pair(p.bn, mA, mB, mC, a, p.ctas / 2, stream);
+  else
+    e = launch_tc(p.bn, p.kernel == TGEMM_KERNEL_TC_COPY, mA, mB, mC, a, p.ctas, stream);
   return e == cudaSuccess ? TGEMM_OK : cuda_fail(e, "tensor-core kernel launch");
 }
 
@@ -346,12 +423,13 @@ int tgemm_gemm_ex(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, c
 int tgemm_plan(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb, const void* C,
                int64_t ldc, int dtype, const tgemm_options* opts, int sm_count, tgemm_plan_info* out) {
   tgemm::Plan p;
-  const int st = tgemm::make_plan(M, N, K, A, lda, B, ldb, C, ldc, dtype, opts, sm_count < 1 ? 1 : sm_count, p);
+  const int sms = sm_count < 1 ? 1 : sm_count;
+  const int st = tgemm::make_plan(M, N, K, A, lda, B, ldb, C, ldc, dtype, opts, sms, sms / 2, p);
   if (out) {
     std::memset(out, 0, sizeof *out);
     if (st == TGEMM_OK && !p.noop && !p.zero) {
       out->kernel = p.kernel;
-      out->tile_m = p.kernel == TGEMM_KERNEL_SIMT ? tgemm::kSimtBM : tgemm::kTileM;
+      out->tile_m = p.kernel == TGEMM_KERNEL_SIMT ? tgemm::kSimtBM : (p.pair ? 2 : 1) * tgemm::kTileM;
       out->tile_n = p.bn;
       out->tile_k = p.kernel == TGEMM_KERNEL_SIMT ? tgemm::kSimtBK : tgemm::kTileK;
       out->stages = p.stages;
@@ -363,6 +441,7 @@ int tgemm_plan(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, cons
       out->b_copy_bytes = p.b_copy;
       out->store_bytes = p.store;
       out->smem_bytes = p.smem;
+      out->cta_group = p.pair ? 2 : 1;
     }
   }
   return st;

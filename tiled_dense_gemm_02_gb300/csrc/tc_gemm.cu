@@ -35,68 +35,11 @@
 
 #include <atomic>
 
-#include "ptx.cuh"
-#include "tgemm_internal.h"
+#include "tc_common.cuh"
 
 namespace tgemm {
 namespace {
 
-
-struct Ctl {
-  volatile uint32_t* abort;
-  unsigned long long timeout_ns;
-  unsigned int* status;
-};
-
-__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const Ctl& c, uint32_t site) {
-  if (ptx::mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = ptx::globaltimer_ns();
-  while (true) {
-#pragma unroll 1
-    for (int i = 0; i < 16; ++i)
-      if (ptx::mbar_try_wait(bar, parity)) return true;
-    if (*c.abort) return false;
-    if (ptx::globaltimer_ns() - t0 > c.timeout_ns) {
-      *c.abort = 1u;
-      atomicCAS(c.status, 0u, kTimeoutFlag | site);
-      return false;
-    }
-  }
-}
-
-// Lane 0 waits, the warp follows its verdict.
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const Ctl& c, uint32_t site) {
-  int ok = 1;
-  if (ptx::lane_id() == 0) ok = wait_bounded(bar, parity, c, site) ? 1 : 0;
-  return __shfl_sync(0xffffffffu, ok, 0) != 0;
-}
-
-// Tile id -> (m block, n block): groups of `group_m` block-rows are walked
-// column by column, so CTAs running at the same time touch group_m A panels
-// and few B panels.
-__device__ __forceinline__ void tile_coords(int t, const TcArgs& a, int& mb, int& nb) {
-  const int per_group = a.group_m * a.tiles_n;
-  const int g = t / per_group;
-  const int first_m = g * a.group_m;
-  const int gsz = min(a.tiles_m - first_m, a.group_m);
-  const int r = t - g * per_group;
-  mb = first_m + r % gsz;
-  nb = r / gsz;
-}
-
-// Shared-memory matrix descriptor of tcgen05 for a 128-byte-swizzled operand:
-// start address, leading-dimension byte offset, stride-dimension byte offset
-// (all >> 4), descriptor version 1 (bit 46) and swizzle mode 2 = 128 B.
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-  return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) | (static_cast<uint64_t>(lbo >> 4) << 16) |
-         (static_cast<uint64_t>(sbo >> 4) << 32) | (1ull << 46) | (2ull << 61);
-}
-
-// Offset of byte `cb` (0..127) of row `r` inside a 128-byte-swizzled block:
-// 16-byte chunk index XOR (row mod 8).
-__device__ __forceinline__ uint32_t sw128_offset(int r, int cb) {
-  return static_cast<uint32_t>(r * 128 + ((((cb >> 4) ^ (r & 7)) << 4) | (cb & 15)));
-}
 
 // ---------------------------------------------------------- copy producers
 // A tile: rows m0..m0+127, k0..k0+63 of row-major A -> K-major swizzled rows.
@@ -158,49 +101,6 @@ __device__ __forceinline__ void copy_b_dispatch(uint8_t* sb, const TcArgs& a, in
     case 8: copy_b_tile<8, BN>(sb, a, k0, n0, ct); break;
     case 4: copy_b_tile<4, BN>(sb, a, k0, n0, ct); break;
     default: copy_b_tile<2, BN>(sb, a, k0, n0, ct); break;
-  }
-}
-
-// ------------------------------------------------------------- epilogue
-__device__ __forceinline__ uint32_t pack_pair(float lo, float hi, int out_fmt) {
-  if (out_fmt == OUT_BF16) {
-    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<uint32_t*>(&v);
-  }
-  __half2 v = __floats2half2_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&v);
-}
-
-// Store a packed 128-byte row segment w[0..31] to global with the widest
-// access `granule` (16/8/4/2 bytes) allows; only the first `valid_bytes`
-// bytes are written (element size `es`).  Fully unrolled so w stays in
-// registers.
-__device__ __forceinline__ void store_segment(uint8_t* dst, const uint32_t (&w)[32], int valid_bytes, int granule,
-                                              int es) {
-  if (valid_bytes >= 128 && granule == 16) {
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-      reinterpret_cast<uint4*>(dst)[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
-  } else if (valid_bytes >= 128 && granule == 8) {
-#pragma unroll
-    for (int i = 0; i < 16; ++i) reinterpret_cast<uint2*>(dst)[i] = make_uint2(w[2 * i], w[2 * i + 1]);
-  } else if (granule >= 4) {
-    // 4-byte words while they are whole, then a trailing half word
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      if (4 * i + 4 <= valid_bytes) {
-        reinterpret_cast<uint32_t*>(dst)[i] = w[i];
-      } else if (es == 2 && 4 * i + 2 <= valid_bytes) {
-        reinterpret_cast<uint16_t*>(dst)[2 * i] = static_cast<uint16_t>(w[i] & 0xFFFFu);
-      }
-    }
-  } else {
-    // 2-byte aligned rows (16-bit output only)
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      if (4 * i + 2 <= valid_bytes) reinterpret_cast<uint16_t*>(dst)[2 * i] = static_cast<uint16_t>(w[i] & 0xFFFFu);
-      if (4 * i + 4 <= valid_bytes) reinterpret_cast<uint16_t*>(dst)[2 * i + 1] = static_cast<uint16_t>(w[i] >> 16);
-    }
   }
 }
 
@@ -383,63 +283,13 @@ __global__ void __launch_bounds__(tc_threads(kCopy), 1)
     uint8_t* stage_base = sC + (warp - 2) * 2 * 4096;
     int acc = 0, sbuf = 0;
     uint32_t acc_phase = 0;
-    const int out_fmt = args.out_fmt;
-    const int es = out_fmt == OUT_F32 ? 4 : 2;
-    const bool tma_store = args.store_granule == 0;
     for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
       int mb, nb;
       tile_coords(t, args, mb, nb);
       if (!warp_wait(ptx::smem_u32(&acc_full[acc]), acc_phase, ctl, SITE_EPI_ACC_FULL)) break;
       ptx::tc_fence_after_sync();
-      const int row = mb * kTileM + q * 32 + lane;
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * ACC);
-      // one chunk = 128 bytes of output per row: 32 fp32 or 64 16-bit columns;
-      // with 16-bit output and BN % 64 == 32 the last chunk is 32 columns wide
-      const int cols_per_chunk = 128 / es;
-      const int chunks = (BN + cols_per_chunk - 1) / cols_per_chunk;
-#pragma unroll 1
-      for (int c = 0; c < chunks; ++c) {
-        const int col_in_tile = c * cols_per_chunk;
-        const bool half = col_in_tile + cols_per_chunk > BN;  // only 16-bit output, BN = 224
-        uint32_t w[32];
-        if (out_fmt == OUT_F32) {
-          ptx::tmem_ld_32x32b_x32(tbase + col_in_tile, w);
-          ptx::tmem_wait_ld();
-        } else {
-          uint32_t lo[32], hi[32];
-          ptx::tmem_ld_32x32b_x32(tbase + col_in_tile, lo);
-          if (!half) ptx::tmem_ld_32x32b_x32(tbase + col_in_tile + 32, hi);
-          ptx::tmem_wait_ld();
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            w[i] = pack_pair(__uint_as_float(lo[2 * i]), __uint_as_float(lo[2 * i + 1]), out_fmt);
-            w[16 + i] = half ? 0u : pack_pair(__uint_as_float(hi[2 * i]), __uint_as_float(hi[2 * i + 1]), out_fmt);
-          }
-        }
-        const int col0 = nb * BN + col_in_tile;
-        if (tma_store && !half) {
-          uint8_t* buf = stage_base + sbuf * 4096;
-          if (lane == 0) ptx::bulk_wait_group_read<1>();
-          __syncwarp();
-#pragma unroll
-          for (int ch = 0; ch < 8; ++ch)
-            *reinterpret_cast<uint4*>(buf + sw128_offset(lane, ch * 16)) =
-                make_uint4(w[4 * ch], w[4 * ch + 1], w[4 * ch + 2], w[4 * ch + 3]);
-          ptx::fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            ptx::tma_store_2d(&mapC, col0, mb * kTileM + q * 32, ptx::smem_u32(buf));
-            ptx::bulk_commit_group();
-          }
-          sbuf ^= 1;
-        } else if (row < args.M && col0 < args.N) {
-          uint8_t* dst = static_cast<uint8_t*>(args.C) + (static_cast<int64_t>(row) * args.ldc + col0) * es;
-          const int width = half ? 32 : cols_per_chunk;
-          const int valid = min(args.N - col0, width) * es;
-          // the half chunk's rows are 16-byte aligned whenever bulk stores are on
-          store_segment(dst, w, valid, tma_store ? 16 : args.store_granule, es);
-        }
-      }
+      epilogue_tile<BN>(tbase, mb * kTileM + q * 32, nb * BN, args, &mapC, stage_base, sbuf, lane);
       // this warp's reads of the accumulator buffer are complete
       ptx::tc_fence_before_sync();
       __syncwarp();

@@ -1,0 +1,285 @@
+// Tensor-core GEMM on CTA pairs (clusters of two SMs): one 256 x BN output
+// tile per pair, computed by tcgen05.mma.cta_group::2 with M = 256.
+//
+// This is the same tiling as tc_gemm.cu one level up: the block tile grows to
+// 256 x BN so that each byte staged in shared memory feeds twice the MMA work
+// of the 128 x BN tile ("Tiling 策略与内存层次优化", §约束一 and the tiled
+// intensity 2*TM*TN/((TM+TN)*e); "矩阵乘法中的平铺": traffic 2mnk/b falls as
+// the output block grows).  Each CTA of the pair stages its own 128 rows of A
+// and half of the B columns, so the pair moves (256 + BN) x 64 elements per K
+// stage for a 256 x BN x 64 product, against (128 + BN) x 64 for a 128 x BN x
+// 64 product on one SM: 32 KB instead of 48 KB per SM per stage at BN = 256,
+// which leaves room for six stages in flight.
+//
+// Roles (both CTAs unless noted):
+//   warp 0      bulk-tensor producer: loads this CTA's A rows and B columns;
+//               completion is signalled on the leader CTA's full barrier
+//   warp 1      tensor-memory allocation (both CTAs together); MMA issue by
+//               one thread of the leader CTA (cluster rank 0), whose commits
+//               are multicast to both CTAs' empty / accumulator-full barriers
+//   warps 2..5  epilogue of this CTA's 128 rows; they release the accumulator
+//               buffer by arriving on the leader's accumulator-empty barrier
+// Every wait is bounded (see tc_common.cuh); CTAs of a pair only meet at the
+// two cluster barriers (after set-up and before tensor memory is freed),
+// which both always reach.
+#include <atomic>
+
+#include "tc_common.cuh"
+
+namespace tgemm {
+namespace {
+
+template <int BN>
+__global__ void __launch_bounds__(32 * (2 + kEpiWarps), 1)
+    tc_gemm_2sm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
+                       const __grid_constant__ CUtensorMap mapC, const TcArgs args) {
+  constexpr int BNH = BN / 2;  // B columns staged by each CTA
+  constexpr int STAGES = tc2_stages(BN);
+  constexpr int A_BYTES = kTileM * kTileK * 2;
+  constexpr int B_BYTES = tc_b_atoms(BNH) * 8192;
+  constexpr int ACC = 256;
+  constexpr uint32_t TMEM_COLS = 512;
+  static_assert(tc2_valid_bn(BN), "pair tile width");
+  static_assert(tc2_smem_bytes(BN) <= kSmemLimit, "shared memory per CTA");
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = sA + STAGES * A_BYTES;
+  uint8_t* sC = sB + STAGES * B_BYTES;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sC + kEpiBytes);
+  uint64_t* empty = full + STAGES;
+  uint64_t* acc_full = empty + STAGES;
+  uint64_t* acc_empty = acc_full + 2;
+  uint64_t* drain = acc_empty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile uint32_t* abort_flag = tmem_slot + 1;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = ptx::cluster_ctarank();
+  const bool leader = rank == 0;
+  const int pair = blockIdx.x >> 1;
+  const int npairs = gridDim.x >> 1;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      ptx::mbar_init(ptx::smem_u32(&full[s]), 1);   // leader only: its producer's expect_tx
+      ptx::mbar_init(ptx::smem_u32(&empty[s]), 1);  // multicast MMA commit
+    }
+    for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(ptx::smem_u32(&acc_full[b]), 1);              // multicast MMA commit
+      ptx::mbar_init(ptx::smem_u32(&acc_empty[b]), 2 * kEpiWarps);  // leader only: both CTAs' epilogues
+    }
+    ptx::mbar_init(ptx::smem_u32(drain), 1);
+    *abort_flag = 0u;
+    ptx::fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    ptx::tma_prefetch_desc(&mapA);
+    ptx::tma_prefetch_desc(&mapB);
+    if (args.store_granule == 0) ptx::tma_prefetch_desc(&mapC);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc_pair(ptx::smem_u32(tmem_slot), TMEM_COLS);
+    ptx::tmem_relinquish_pair();
+  }
+  // barriers of both CTAs are initialised before any remote arrive or multicast
+  ptx::tc_fence_before_sync();
+  ptx::cluster_sync();
+  ptx::tc_fence_after_sync();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const Ctl ctl{abort_flag, args.timeout_ns, args.status};
+  const int num_tiles = args.num_tiles;
+  const int kbs = args.k_blocks;
+
+  if (warp == 0) {
+    // ------------------------------------------------ bulk-tensor producer
+    if (lane == 0 && !args.inject_fault) {
+      const uint32_t tx_pair = 2u * (A_BYTES + tc_b_atoms(BNH) * 8192u);
+      int stage = 0;
+      uint32_t phase = 0, filled = 0, last_parity = 0;
+      bool ok = true;
+      for (int t = pair; t < num_tiles && ok; t += npairs) {
+        int mb, nb;
+        tile_coords(t, args, mb, nb);
+        for (int kb = 0; kb < kbs; ++kb) {
+          if (!wait_bounded(ptx::smem_u32(&empty[stage]), phase ^ 1u, ctl, SITE_PRODUCER_EMPTY)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb_local = ptx::smem_u32(&full[stage]);
+          const uint32_t fb = ptx::mapa_shared(fb_local, 0);
+          if (leader) ptx::mbar_arrive_expect_tx(fb_local, tx_pair);
+          ptx::tma_load_2d_pair(ptx::smem_u32(sA + stage * A_BYTES), &mapA, kb * kTileK,
+                                mb * 2 * kTileM + static_cast<int>(rank) * kTileM, fb);
+#pragma unroll
+          for (int j = 0; j < tc_b_atoms(BNH); ++j)
+            ptx::tma_load_2d_pair(ptx::smem_u32(sB + stage * B_BYTES + j * 8192), &mapB,
+                                  nb * BN + static_cast<int>(rank) * BNH + j * 64, kb * kTileK, fb);
+          filled |= 1u << stage;
+          last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // Loads still in flight must land before shared memory is released: the
+      // leader waits for its full barriers (both CTAs' bytes), the peer for the
+      // MMA's release of each stage it filled (consumption implies arrival).
+      for (int s = 0; s < STAGES; ++s)
+        if ((filled >> s) & 1u) {
+          const uint32_t par = (last_parity >> s) & 1u;
+          if (leader)
+            wait_teardown(ptx::smem_u32(&full[s]), par, ctl, SITE_TEARDOWN);
+          else
+            wait_teardown(ptx::smem_u32(&empty[s]), par, ctl, SITE_TEARDOWN);
+        }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------ MMA issuer (leader CTA only)
+    if (leader && lane == 0) {
+      int stage = 0, acc = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool ok = true;
+      for (int t = pair; t < num_tiles && ok; t += npairs) {
+        if (!wait_bounded(ptx::smem_u32(&acc_empty[acc]), acc_phase ^ 1u, ctl, SITE_MMA_ACC_EMPTY)) break;
+        ptx::tc_fence_after_sync();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * ACC);
+        for (int kb = 0; kb < kbs; ++kb) {
+          if (!wait_bounded(ptx::smem_u32(&full[stage]), phase, ctl, SITE_MMA_FULL)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after_sync();
+          const uint32_t a0 = ptx::smem_u32(sA + stage * A_BYTES);
+          const uint32_t b0 = ptx::smem_u32(sB + stage * B_BYTES);
+#pragma unroll
+          for (int k = 0; k < kTileK / 16; ++k)
+            ptx::tc_mma_f16_pair(d_tmem, sw128_desc(a0 + k * 32, 16, 1024), sw128_desc(b0 + k * 2048, 8192, 1024),
+                                 args.idesc, (kb | k) != 0 ? 1u : 0u);
+          ptx::tc_commit_pair_multicast(ptx::smem_u32(&empty[stage]), 0x3);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        ptx::tc_commit_pair_multicast(ptx::smem_u32(&acc_full[acc]), 0x3);
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+      // all pair MMAs have finished before either CTA frees tensor memory
+      ptx::tc_commit_pair(ptx::smem_u32(drain));
+      wait_teardown(ptx::smem_u32(drain), 0, ctl, SITE_DRAIN);
+    }
+    __syncwarp();
+  } else {
+    // --------------------------------------------------------- epilogue
+    const int q = warp & 3;
+    uint8_t* stage_base = sC + (warp - 2) * 2 * 4096;
+    int acc = 0, sbuf = 0;
+    uint32_t acc_phase = 0;
+    for (int t = pair; t < num_tiles; t += npairs) {
+      int mb, nb;
+      tile_coords(t, args, mb, nb);
+      if (!warp_wait(ptx::smem_u32(&acc_full[acc]), acc_phase, ctl, SITE_EPI_ACC_FULL)) break;
+      ptx::tc_fence_after_sync();
+      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * ACC);
+      epilogue_tile<BN>(tbase, mb * 2 * kTileM + static_cast<int>(rank) * kTileM + q * 32, nb * BN, args, &mapC,
+                        stage_base, sbuf, lane);
+      ptx::tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive_cluster(ptx::mapa_shared(ptx::smem_u32(&acc_empty[acc]), 0));
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+    if (lane == 0) ptx::bulk_wait_group<0>();
+    __syncwarp();
+  }
+
+  // ------------------------------------------------------------- teardown
+  ptx::tc_fence_before_sync();
+  ptx::cluster_sync();
+  if (warp == 1) {
+    ptx::tc_fence_after_sync();
+    ptx::tmem_dealloc_pair(tmem_base, TMEM_COLS);
+  }
+}
+
+template <int BN>
+cudaError_t launch_pair(const CUtensorMap& mA, const CUtensorMap& mB, const CUtensorMap& mC, const TcArgs& args,
+                        int pairs, cudaStream_t stream) {
+  constexpr int smem = tc2_smem_bytes(BN);
+  auto kernel = tc_gemm_2sm_kernel<BN>;
+  static std::atomic<uint64_t> done_mask{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = 1ull << (dev & 63);
+  if (!(done_mask.load(std::memory_order_acquire) & bit)) {
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    done_mask.fetch_or(bit, std::memory_order_acq_rel);
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * pairs, 1, 1);
+  cfg.blockDim = dim3(32 * (2 + kEpiWarps), 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, mA, mB, mC, args);
+}
+
+template <int BN>
+cudaError_t max_pairs(int* out) {
+  constexpr int smem = tc2_smem_bytes(BN);
+  auto kernel = tc_gemm_2sm_kernel<BN>;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2, 1, 1);
+  cfg.blockDim = dim3(32 * (2 + kEpiWarps), 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaOccupancyMaxActiveClusters(out, kernel, &cfg);
+}
+
+}  // namespace
+
+cudaError_t launch_tc_pair(int bn, const CUtensorMap& mA, const CUtensorMap& mB, const CUtensorMap& mC,
+                           const TcArgs& args, int pairs, cudaStream_t stream) {
+  switch (bn) {
+    case 128: return launch_pair<128>(mA, mB, mC, args, pairs, stream);
+    case 192: return launch_pair<192>(mA, mB, mC, args, pairs, stream);
+    case 224: return launch_pair<224>(mA, mB, mC, args, pairs, stream);
+    case 256: return launch_pair<256>(mA, mB, mC, args, pairs, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t tc_pair_capacity(int bn, int* pairs) {
+  switch (bn) {
+    case 128: return max_pairs<128>(pairs);
+    case 192: return max_pairs<192>(pairs);
+    case 224: return max_pairs<224>(pairs);
+    case 256: return max_pairs<256>(pairs);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace tgemm

@@ -78,9 +78,26 @@ constexpr int tc_smem_bytes(int bn) { return 1024 + tc_stages(bn) * tc_stage_byt
 constexpr int tc_acc_stride(int bn) { return bn <= 64 ? 64 : (bn <= 128 ? 128 : 256); }
 constexpr int tc_threads(bool copy) { return 32 * (2 + kEpiWarps + (copy ? kCopyWarps : 0)); }
 
+// CTA-pair kernel: 256 x BN tiles, each CTA stages 128 rows of A and BN/2
+// columns of B.
+constexpr bool tc2_valid_bn(int bn) { return bn == 128 || bn == 192 || bn == 224 || bn == 256; }
+constexpr int tc2_stage_bytes(int bn) { return kTileM * kTileK * 2 + tc_b_atoms(bn / 2) * 8192; }
+constexpr int tc2_stages(int bn) {
+  return (kSmemLimit - 1024 - kEpiBytes - kBarrierBytes) / tc2_stage_bytes(bn) > 8
+             ? 8
+             : (kSmemLimit - 1024 - kEpiBytes - kBarrierBytes) / tc2_stage_bytes(bn);
+}
+constexpr int tc2_smem_bytes(int bn) {
+  return 1024 + tc2_stages(bn) * tc2_stage_bytes(bn) + kEpiBytes + kBarrierBytes;
+}
+
 // Launchers (return the cudaError_t of the launch).
 cudaError_t launch_tc(int bn, bool copy, const CUtensorMap& mapA, const CUtensorMap& mapB, const CUtensorMap& mapC,
                       const TcArgs& args, int ctas, cudaStream_t stream);
+cudaError_t launch_tc_pair(int bn, const CUtensorMap& mapA, const CUtensorMap& mapB, const CUtensorMap& mapC,
+                           const TcArgs& args, int pairs, cudaStream_t stream);
+// Number of CTA pairs of the pair kernel that can be resident at once.
+cudaError_t tc_pair_capacity(int bn, int* pairs);
 cudaError_t launch_simt(const SimtArgs& args, cudaStream_t stream);
 cudaError_t launch_zero_fill(void* C, int64_t rows, int64_t cols, int64_t ldc, int elem_bytes, cudaStream_t stream);
 
