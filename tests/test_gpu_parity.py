@@ -113,13 +113,15 @@ def test_leading_dimensions(lds, dtype):
 
 # ------------------------------------------------------------ CTA-pair kernel
 
+@pytest.mark.parametrize("store_mode", [1, 2])
 @pytest.mark.parametrize("tile_n", [128, 192, 224, 256])
 @pytest.mark.parametrize("dtype", TC_DTYPES, ids=lambda d: wl.DTYPE_NAMES[d])
-def test_pair_kernel(tile_n, dtype):
+def test_pair_kernel(tile_n, dtype, store_mode):
     """256 x tile_n tiles on CTA pairs: ragged M (two pair tiles, the second
-    44 rows), ragged N and a K tail."""
+    44 rows), ragged N and a K tail; staged bulk-tensor stores (store_mode 1)
+    and the unstaged variant with a deeper ring (store_mode 2)."""
     M, N, K = 300, 520, 200
-    A, B, res = case(M, N, K, dtype, seed=34, options={"cta_group": 2, "tile_n": tile_n})
+    A, B, res = case(M, N, K, dtype, seed=34, options={"cta_group": 2, "tile_n": tile_n, "store_mode": store_mode})
     assert res.plan.cta_group == 2 and res.plan.tile_m == 256 and res.plan.tile_n == tile_n
     H.check_full(res, A, B, M, N, K, dtype, f"pair tile_n {tile_n}")
 

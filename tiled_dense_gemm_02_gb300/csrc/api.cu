@@ -264,7 +264,7 @@ int make_plan(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const
   }
   p.pair = opt.cta_group == 2 || (opt.cta_group == 0 && bn2 != 0 && cost2 < cost1);
   p.bn = p.pair ? bn2 : bn1;
-  p.stages = p.pair ? tc2_stages(p.bn) : tc_stages(p.bn);
+  p.stages = p.pair ? tc2_stages(p.bn, p.store == 0) : tc_stages(p.bn);
   const int tm = p.pair ? 2 * kTileM : kTileM;
   p.tiles_m = static_cast<int>((M + tm - 1) / tm);
   p.tiles_n = static_cast<int>((N + p.bn - 1) / p.bn);
@@ -282,7 +282,7 @@ int make_plan(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const
     if (opt.max_ctas) ctas = std::min<int64_t>(ctas, opt.max_ctas);
   }
   p.ctas = static_cast<int>(ctas);
-  p.smem = p.pair ? tc2_smem_bytes(p.bn) : tc_smem_bytes(p.bn);
+  p.smem = p.pair ? tc2_smem_bytes(p.bn, p.store == 0) : tc_smem_bytes(p.bn);
   return TGEMM_OK;
 }
 
@@ -399,7 +399,7 @@ int run(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void*
   a.timeout_ns = static_cast<unsigned long long>(to_us) * 1000ull;
   a.status = dev->status;
   if (p.pair)
-    e = launch_tc_pair(p.bn, mA, mB, mC, a, p.ctas / 2, stream);
+    e = launch_tc_pair(p.bn, p.store == 0, mA, mB, mC, a, p.ctas / 2, stream);
   else
     e = launch_tc(p.bn, p.kernel == TGEMM_KERNEL_TC_COPY, mA, mB, mC, a, p.ctas, stream);
   return e == cudaSuccess ? TGEMM_OK : cuda_fail(e, "tensor-core kernel launch");

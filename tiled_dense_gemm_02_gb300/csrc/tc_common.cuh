@@ -131,12 +131,13 @@ __device__ __forceinline__ void wait_teardown(uint32_t bar, uint32_t parity, con
 // per-thread stores.  Chunks are 128 bytes of output per row (32 fp32 or 64
 // 16-bit columns); with 16-bit output and BN % 64 == 32 the last chunk is 32
 // columns wide and is stored per thread.
-template <int BN>
+template <int BN, bool kStaged = true>
 __device__ __forceinline__ void epilogue_tile(uint32_t tbase, int row0, int col_base, const TcArgs& args,
                                               const CUtensorMap* mapC, uint8_t* stage_base, int& sbuf, int lane) {
   const int out_fmt = args.out_fmt;
   const int es = out_fmt == OUT_F32 ? 4 : 2;
-  const bool tma_store = args.store_granule == 0;
+  // without staging buffers every chunk goes out by per-thread stores
+  const bool tma_store = kStaged && args.store_granule == 0;
   const int row = row0 + lane;
   const int cols_per_chunk = 128 / es;
   const int chunks = (BN + cols_per_chunk - 1) / cols_per_chunk;

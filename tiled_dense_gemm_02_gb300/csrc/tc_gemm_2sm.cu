@@ -29,25 +29,25 @@
 namespace tgemm {
 namespace {
 
-template <int BN>
+template <int BN, bool kStaged>
 __global__ void __launch_bounds__(32 * (2 + kEpiWarps), 1)
     tc_gemm_2sm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
                        const __grid_constant__ CUtensorMap mapC, const TcArgs args) {
   constexpr int BNH = BN / 2;  // B columns staged by each CTA
-  constexpr int STAGES = tc2_stages(BN);
+  constexpr int STAGES = tc2_stages(BN, kStaged);
   constexpr int A_BYTES = kTileM * kTileK * 2;
   constexpr int B_BYTES = tc_b_atoms(BNH) * 8192;
   constexpr int ACC = 256;
   constexpr uint32_t TMEM_COLS = 512;
   static_assert(tc2_valid_bn(BN), "pair tile width");
-  static_assert(tc2_smem_bytes(BN) <= kSmemLimit, "shared memory per CTA");
+  static_assert(tc2_smem_bytes(BN, kStaged) <= kSmemLimit, "shared memory per CTA");
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
   uint8_t* sB = sA + STAGES * A_BYTES;
   uint8_t* sC = sB + STAGES * B_BYTES;
-  uint64_t* full = reinterpret_cast<uint64_t*>(sC + kEpiBytes);
+  uint64_t* full = reinterpret_cast<uint64_t*>(sC + tc2_epi_bytes(kStaged));
   uint64_t* empty = full + STAGES;
   uint64_t* acc_full = empty + STAGES;
   uint64_t* acc_empty = acc_full + 2;
@@ -78,7 +78,7 @@ __global__ void __launch_bounds__(32 * (2 + kEpiWarps), 1)
   if (warp == 0 && lane == 0) {
     ptx::tma_prefetch_desc(&mapA);
     ptx::tma_prefetch_desc(&mapB);
-    if (args.store_granule == 0) ptx::tma_prefetch_desc(&mapC);
+    if (kStaged && args.store_granule == 0) ptx::tma_prefetch_desc(&mapC);
   }
   if (warp == 1) {
     ptx::tmem_alloc_pair(ptx::smem_u32(tmem_slot), TMEM_COLS);
@@ -188,7 +188,7 @@ __global__ void __launch_bounds__(32 * (2 + kEpiWarps), 1)
       if (!warp_wait(ptx::smem_u32(&acc_full[acc]), acc_phase, ctl, SITE_EPI_ACC_FULL)) break;
       ptx::tc_fence_after_sync();
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * ACC);
-      epilogue_tile<BN>(tbase, mb * 2 * kTileM + static_cast<int>(rank) * kTileM + q * 32, nb * BN, args, &mapC,
+      epilogue_tile<BN, kStaged>(tbase, mb * 2 * kTileM + static_cast<int>(rank) * kTileM + q * 32, nb * BN, args, &mapC,
                         stage_base, sbuf, lane);
       ptx::tc_fence_before_sync();
       __syncwarp();
@@ -209,11 +209,11 @@ __global__ void __launch_bounds__(32 * (2 + kEpiWarps), 1)
   }
 }
 
-template <int BN>
+template <int BN, bool kStaged>
 cudaError_t launch_pair(const CUtensorMap& mA, const CUtensorMap& mB, const CUtensorMap& mC, const TcArgs& args,
                         int pairs, cudaStream_t stream) {
-  constexpr int smem = tc2_smem_bytes(BN);
-  auto kernel = tc_gemm_2sm_kernel<BN>;
+  constexpr int smem = tc2_smem_bytes(BN, kStaged);
+  auto kernel = tc_gemm_2sm_kernel<BN, kStaged>;
   static std::atomic<uint64_t> done_mask{0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -241,8 +241,8 @@ cudaError_t launch_pair(const CUtensorMap& mA, const CUtensorMap& mB, const CUte
 
 template <int BN>
 cudaError_t max_pairs(int* out) {
-  constexpr int smem = tc2_smem_bytes(BN);
-  auto kernel = tc_gemm_2sm_kernel<BN>;
+  constexpr int smem = tc2_smem_bytes(BN, true);
+  auto kernel = tc_gemm_2sm_kernel<BN, true>;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -261,15 +261,20 @@ cudaError_t max_pairs(int* out) {
 
 }  // namespace
 
-cudaError_t launch_tc_pair(int bn, const CUtensorMap& mA, const CUtensorMap& mB, const CUtensorMap& mC,
+cudaError_t launch_tc_pair(int bn, bool staged, const CUtensorMap& mA, const CUtensorMap& mB, const CUtensorMap& mC,
                            const TcArgs& args, int pairs, cudaStream_t stream) {
+#define TGEMM_PAIR_BN(BNV)                                                          \
+  case BNV:                                                                         \
+    return staged ? launch_pair<BNV, true>(mA, mB, mC, args, pairs, stream)         \
+                  : launch_pair<BNV, false>(mA, mB, mC, args, pairs, stream);
   switch (bn) {
-    case 128: return launch_pair<128>(mA, mB, mC, args, pairs, stream);
-    case 192: return launch_pair<192>(mA, mB, mC, args, pairs, stream);
-    case 224: return launch_pair<224>(mA, mB, mC, args, pairs, stream);
-    case 256: return launch_pair<256>(mA, mB, mC, args, pairs, stream);
+    TGEMM_PAIR_BN(128)
+    TGEMM_PAIR_BN(192)
+    TGEMM_PAIR_BN(224)
+    TGEMM_PAIR_BN(256)
     default: return cudaErrorInvalidValue;
   }
+#undef TGEMM_PAIR_BN
 }
 
 cudaError_t tc_pair_capacity(int bn, int* pairs) {

@@ -82,20 +82,23 @@ constexpr int tc_threads(bool copy) { return 32 * (2 + kEpiWarps + (copy ? kCopy
 // columns of B.
 constexpr bool tc2_valid_bn(int bn) { return bn == 128 || bn == 192 || bn == 224 || bn == 256; }
 constexpr int tc2_stage_bytes(int bn) { return kTileM * kTileK * 2 + tc_b_atoms(bn / 2) * 8192; }
-constexpr int tc2_stages(int bn) {
-  return (kSmemLimit - 1024 - kEpiBytes - kBarrierBytes) / tc2_stage_bytes(bn) > 8
+// `staged`: the epilogue stages C tiles in shared memory for bulk-tensor
+// stores; without staging (per-thread stores) the ring gets that space.
+constexpr int tc2_epi_bytes(bool staged) { return staged ? kEpiBytes : 0; }
+constexpr int tc2_stages(int bn, bool staged) {
+  return (kSmemLimit - 1024 - tc2_epi_bytes(staged) - kBarrierBytes) / tc2_stage_bytes(bn) > 8
              ? 8
-             : (kSmemLimit - 1024 - kEpiBytes - kBarrierBytes) / tc2_stage_bytes(bn);
+             : (kSmemLimit - 1024 - tc2_epi_bytes(staged) - kBarrierBytes) / tc2_stage_bytes(bn);
 }
-constexpr int tc2_smem_bytes(int bn) {
-  return 1024 + tc2_stages(bn) * tc2_stage_bytes(bn) + kEpiBytes + kBarrierBytes;
+constexpr int tc2_smem_bytes(int bn, bool staged) {
+  return 1024 + tc2_stages(bn, staged) * tc2_stage_bytes(bn) + tc2_epi_bytes(staged) + kBarrierBytes;
 }
 
 // Launchers (return the cudaError_t of the launch).
 cudaError_t launch_tc(int bn, bool copy, const CUtensorMap& mapA, const CUtensorMap& mapB, const CUtensorMap& mapC,
                       const TcArgs& args, int ctas, cudaStream_t stream);
-cudaError_t launch_tc_pair(int bn, const CUtensorMap& mapA, const CUtensorMap& mapB, const CUtensorMap& mapC,
-                           const TcArgs& args, int pairs, cudaStream_t stream);
+cudaError_t launch_tc_pair(int bn, bool staged, const CUtensorMap& mapA, const CUtensorMap& mapB,
+                           const CUtensorMap& mapC, const TcArgs& args, int pairs, cudaStream_t stream);
 // Number of CTA pairs of the pair kernel that can be resident at once.
 cudaError_t tc_pair_capacity(int bn, int* pairs);
 cudaError_t launch_simt(const SimtArgs& args, cudaStream_t stream);
