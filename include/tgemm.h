@@ -16,6 +16,7 @@
 #ifndef TGEMM_H
 #define TGEMM_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -117,7 +118,15 @@ typedef struct tgemm_options {
                            tiles on one SM, 2 = 256 x N tiles on a pair of
                            SMs (a 2-CTA cluster; bulk-tensor operands only,
                            tile_n 128, 192, 224 or 256) */
-  int reserved[8];
+  int tile_k;           /* K depth of one shared-memory stage (0 auto): 64, or
+                           128 (two 64-deep sub-blocks per stage, one MMA
+                           completion signal per stage; CTA-pair kernel only) */
+  int stream_k;         /* split of the last round of tiles along K over all
+                           CTA pairs (needs a workspace, tgemm_gemm_ws):
+                           0 auto (currently off: on the measured shapes the
+                           fix-up costs more than the idle tail), 1 off,
+                           2 on whenever the tile count leaves a remainder */
+  int reserved[6];
 } tgemm_options;
 
 /* tgemm_gemm with explicit options (opts may be NULL).  A forced kernel that
@@ -145,15 +154,55 @@ typedef struct tgemm_plan_info {
   int smem_bytes;    /* dynamic shared memory per CTA */
   int cta_group;     /* 1: one SM per tile; 2: a CTA pair per 256-row tile
                         (tile_m is then 256 and ctas counts CTAs, two per pair) */
-  int reserved[3];
+  int dp_tiles;      /* tiles computed whole (all of them without stream-K) */
+  int sk_iters;      /* k-stages of the remaining tiles split over the pairs */
+  int workspace_bytes; /* workspace the call uses (0 without stream-K) */
 } tgemm_plan_info;
 
 TGEMM_API int tgemm_plan(int64_t M, int64_t N, int64_t K,
                const void* A, int64_t lda,
                const void* B, int64_t ldb,
                const void* C, int64_t ldc,
-               int dtype, const tgemm_options* opts, int sm_count,
+               int dtype, const tgemm_options* opts,
+               size_t workspace_bytes, int sm_count,
                tgemm_plan_info* out);
+
+/*
+ * Stream-K workspace.  When the number of output tiles leaves the last round
+ * of the persistent grid partly empty, tgemm_gemm_ws splits the k-stages of
+ * the remaining tiles evenly over all CTA pairs.  The pairs holding the first
+ * k-stages of a tile write fp32 partial sums to the workspace; the pair
+ * holding its last k-stage adds them (in a fixed order, so results do not
+ * depend on timing) and stores C.
+ *
+ * tgemm_workspace_size: bytes of workspace tgemm_gemm_ws would use for these
+ * arguments on the current device (0 when it would use none).  Same
+ * validation and status codes as tgemm_gemm_ex.
+ *
+ * tgemm_gemm_ws: tgemm_gemm_ex with a workspace.  `workspace` is device memory
+ * owned by the caller, 256-byte aligned, zero-initialised before its first use
+ * (later calls need no clearing); `workspace_bytes` smaller than
+ * tgemm_workspace_size (including 0 with a NULL workspace) makes the call run
+ * without stream-K.  Two calls that may run at the same time on the GPU must
+ * not share a workspace.  Its contents after a call are unspecified.
+ * Finishing pairs wait (bounded, see wait_timeout_us) for the partial sums of
+ * the others, so all CTA pairs of the call must be able to run at once: the
+ * grid never exceeds the resident capacity of the device; a device shared
+ * with kernels that keep SMs busy indefinitely can make the wait run out
+ * (TGEMM_ERR_DEVICE_TIMEOUT, C unspecified).
+ */
+TGEMM_API int tgemm_workspace_size(int64_t M, int64_t N, int64_t K,
+               const void* A, int64_t lda,
+               const void* B, int64_t ldb,
+               const void* C, int64_t ldc,
+               int dtype, const tgemm_options* opts, size_t* bytes);
+
+TGEMM_API int tgemm_gemm_ws(int64_t M, int64_t N, int64_t K,
+               const void* A, int64_t lda,
+               const void* B, int64_t ldb,
+               void* C, int64_t ldc,
+               int dtype, const tgemm_options* opts,
+               void* workspace, size_t workspace_bytes, void* stream);
 
 /* Waits for `stream`, then returns and clears the device-side status word
  * that bounded in-kernel waits set when they give up (TGEMM_OK or

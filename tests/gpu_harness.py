@@ -45,8 +45,11 @@ class Result:
 
 def run_gpu(A_bits: np.ndarray, B_bits: np.ndarray, M: int, N: int, K: int, dtype: int,
             ldc: int | None = None, a_off: int = 0, b_off: int = 0, c_off: int = 0,
-            options=None, dev=None, check_status: bool = True) -> Result:
-    """C = A . B on the GPU through tgemm_gemm_ex; A/B given as [rows, ld] bit arrays."""
+            options=None, dev=None, check_status: bool = True, workspace=None) -> Result:
+    """C = A . B on the GPU through the C ABI; A/B given as [rows, ld] bit arrays.
+
+    workspace: None (tgemm_gemm_ex), True (a fresh zeroed workspace of
+    tgemm_workspace_size bytes, tgemm_gemm_ws) or a torch uint8 tensor to reuse."""
     lib = tg()
     dev = dev or torch.device("cuda:0")
     fout = wl.OUT_FORMAT[dtype]
@@ -62,7 +65,22 @@ def run_gpu(A_bits: np.ndarray, B_bits: np.ndarray, M: int, N: int, K: int, dtyp
     stream = torch.cuda.current_stream(dev).cuda_stream
     st_plan, plan = lib.plan(M, N, K, a_ptr, lda, b_ptr, ldb, c_ptr, ldc, dtype, options,
                              sm_count=torch.cuda.get_device_properties(dev).multi_processor_count)
-    status = lib.gemm_ex(M, N, K, a_ptr, lda, b_ptr, ldb, c_ptr, ldc, dtype, options, stream)
+    ws_tensor = None
+    if workspace is None:
+        status = lib.gemm_ex(M, N, K, a_ptr, lda, b_ptr, ldb, c_ptr, ldc, dtype, options, stream)
+    else:
+        st_ws, nbytes = lib.workspace_size(M, N, K, a_ptr, lda, b_ptr, ldb, c_ptr, ldc, dtype, options)
+        assert st_ws == lib.OK, lib.status_string(st_ws)
+        ws_tensor = workspace if isinstance(workspace, torch.Tensor) else torch.zeros(max(nbytes, 1), dtype=torch.uint8,
+                                                                                    device=dev)
+        assert ws_tensor.data_ptr() % 256 == 0
+        if workspace is True:
+            assert ws_tensor.numel() >= nbytes
+        st_plan, plan = lib.plan(M, N, K, a_ptr, lda, b_ptr, ldb, c_ptr, ldc, dtype, options,
+                                 sm_count=torch.cuda.get_device_properties(dev).multi_processor_count,
+                                 workspace_bytes=ws_tensor.numel())
+        status = lib.gemm_ws(M, N, K, a_ptr, lda, b_ptr, ldb, c_ptr, ldc, dtype, options, ws_tensor.data_ptr(),
+                             ws_tensor.numel(), stream)
     dstat = lib.device_status(stream)
     if check_status:
         assert status == lib.OK, lib.status_string(status)
@@ -75,6 +93,7 @@ def run_gpu(A_bits: np.ndarray, B_bits: np.ndarray, M: int, N: int, K: int, dtyp
     got = wl.decode(np.ascontiguousarray(body[:, :N]), fout)
     res = Result(got, (status, dstat), plan, guard_ok, pad_ok)
     res.raw = body[:, :N].copy()
+    res.workspace = ws_tensor
     return res
 
 

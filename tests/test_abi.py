@@ -26,8 +26,8 @@ def declared_functions():
 
 def test_header_declares_the_abi():
     names = declared_functions()
-    assert names == sorted(["tgemm_gemm", "tgemm_gemm_ex", "tgemm_plan", "tgemm_device_status",
-                            "tgemm_status_string", "tgemm_version"])
+    assert names == sorted(["tgemm_gemm", "tgemm_gemm_ex", "tgemm_gemm_ws", "tgemm_workspace_size", "tgemm_plan",
+                            "tgemm_device_status", "tgemm_status_string", "tgemm_version"])
 
 
 def test_library_exports_every_declared_symbol(tg):
@@ -40,6 +40,8 @@ def test_library_exports_every_declared_symbol(tg):
 
 def test_struct_layouts_match_header(tg):
     assert ctypes.sizeof(tg.Options) == 16 * 4
+    assert [f for f, _ in tg.Options._fields_][:9] == ["kernel", "tile_n", "group_m", "max_ctas", "store_mode",
+                                                       "wait_timeout_us", "inject_fault", "cta_group", "tile_k"]
     assert ctypes.sizeof(tg.PlanInfo) == 17 * 4
 
 
@@ -54,11 +56,11 @@ def test_status_strings(tg):
 A0, B0, C0 = 0x10000000, 0x20000000, 0x30000000
 
 
-def plan(tg, M, N, K, lda=None, ldb=None, ldc=None, dtype=2, A=A0, B=B0, C=C0, sms=148, **opt):
+def plan(tg, M, N, K, lda=None, ldb=None, ldc=None, dtype=2, A=A0, B=B0, C=C0, sms=148, ws=0, **opt):
     lda = K if lda is None else lda
     ldb = N if ldb is None else ldb
     ldc = N if ldc is None else ldc
-    return tg.plan(M, N, K, A, lda, B, ldb, C, ldc, dtype, opt or None, sm_count=sms)
+    return tg.plan(M, N, K, A, lda, B, ldb, C, ldc, dtype, opt or None, sm_count=sms, workspace_bytes=ws)
 
 
 def test_validation_errors(tg):
@@ -95,7 +97,7 @@ def test_dispatch_aligned_uses_bulk_tensor_copies(tg):
     st, p = plan(tg, 4096, 4096, 4096, dtype=3, sms=148)
     assert st == tg.OK
     assert p.kernel == tg.KERNEL_TC_TMA and p.a_copy_bytes == 0 and p.b_copy_bytes == 0 and p.store_bytes == 0
-    assert p.tile_m in (128, 256) and p.tile_k == 64
+    assert p.tile_m in (128, 256) and p.tile_k in (64, 128)
     assert p.tiles_m * p.tile_m >= 4096 and p.tiles_n * p.tile_n >= 4096
     assert p.ctas == min(148, p.tiles_m * p.tiles_n)
     assert p.smem_bytes <= 232448
@@ -133,6 +135,10 @@ def test_pair_planning(tg):
     assert plan(tg, 512, 512, 512, dtype=2, cta_group=3)[0] == tg.ERR_INVALID_VALUE
     st, p = plan(tg, 1100, 1300, 330, lda=336, ldb=1304, dtype=3, cta_group=2, tile_n=256, max_ctas=6)
     assert st == tg.OK and p.ctas == 6
+    st, p = plan(tg, 4096, 4096, 4096, dtype=3, cta_group=2, tile_n=256, tile_k=128)
+    assert st == tg.OK and p.tile_k == 128 and p.stages == 3 and p.smem_bytes <= 232448
+    assert plan(tg, 4096, 4096, 4096, dtype=3, cta_group=1, tile_k=128)[0] == tg.ERR_INVALID_VALUE
+    assert plan(tg, 4096, 4096, 4096, dtype=3, tile_k=96)[0] == tg.ERR_INVALID_VALUE
 
 
 def test_dispatch_options(tg):
@@ -160,3 +166,64 @@ def test_tile_width_choice_fills_the_sms(tg):
     for bn in (64, 128, 192, 224, 256):
         st, p = plan(tg, 512, 512, 512, tile_n=bn)
         assert st == tg.OK and p.smem_bytes <= 232448 and p.stages >= 3
+
+
+def test_stream_k_planning(tg):
+    # 4096^3 on 152 SMs: 256 pair tiles on 76 pairs leave 28 tiles for the tail
+    st, p = plan(tg, 4096, 4096, 4096, dtype=3, sms=152, cta_group=2, tile_n=256, stream_k=2)
+    assert st == tg.OK and p.sk_iters == 0 and p.workspace_bytes == 0     # no workspace: whole tiles
+    need = 76 * 2 * 4 * 32 * 256 * 4 + 2560
+    st, p = plan(tg, 4096, 4096, 4096, dtype=3, sms=152, cta_group=2, tile_n=256, ws=need)
+    assert p.sk_iters == 0                                                # auto: off
+    st, p = plan(tg, 4096, 4096, 4096, dtype=3, sms=152, cta_group=2, tile_n=256, ws=need, stream_k=2)
+    assert st == tg.OK and p.workspace_bytes == need
+    assert p.dp_tiles == 228 and p.sk_iters == 28 * (4096 // p.tile_k)
+    assert p.ctas == 152
+    st, p = plan(tg, 4096, 4096, 4096, dtype=3, sms=152, cta_group=2, tile_n=256, ws=need - 1, stream_k=2)
+    assert p.sk_iters == 0                                                # too small: whole tiles
+    st, p = plan(tg, 4096, 4096, 4096, dtype=3, sms=152, cta_group=2, tile_n=256, ws=need, stream_k=1)
+    assert p.sk_iters == 0
+    # fewer tiles than pairs: every tile is split, all 76 pairs work
+    st, p = plan(tg, 2048, 2048, 2048, dtype=2, sms=152, cta_group=2, tile_n=256, ws=need, stream_k=2)
+    assert p.dp_tiles == 0 and p.sk_iters == 64 * (2048 // p.tile_k) and p.ctas == 152
+    assert plan(tg, 64, 64, 64, stream_k=3)[0] == tg.ERR_INVALID_VALUE
+
+
+def _units(dp_tiles, sk_iters, kb, workers, w):
+    """Python restatement of the device unit list, for the partition invariants."""
+    units = [(t, 0, kb, "full") for t in range(w, dp_tiles, workers)]
+    if sk_iters:
+        b, e = w * sk_iters // workers, (w + 1) * sk_iters // workers
+        if e > b:
+            tb, te = b // kb, (e - 1) // kb
+            lo, hi = b - tb * kb, min(e, (tb + 1) * kb) - tb * kb
+            first = (dp_tiles + tb, lo, hi, "partial" if hi < kb else ("full" if lo == 0 else "finish"))
+            if te == tb:
+                units.append(first)
+            else:
+                last = (dp_tiles + te, 0, e - te * kb, "partial" if e - te * kb < kb else "full")
+                units += [last, first]
+    return units
+
+
+@pytest.mark.parametrize("tiles,kb,workers", [(256, 32, 76), (64, 16, 76), (100, 7, 76), (5, 64, 3), (300, 3, 76)])
+def test_stream_k_partition_covers_every_stage_once(tiles, kb, workers):
+    rem = tiles % workers
+    dp = tiles - rem
+    sk = rem * kb
+    seen = {}
+    for w in range(workers):
+        us = _units(dp, sk, kb, workers, w)
+        assert sum(1 for u in us if u[0] >= dp) <= 2
+        roles = [u[3] for u in us if u[0] >= dp]
+        if "finish" in roles:
+            assert roles[-1] == "finish"   # finishing last: its partial sums exist, its ring is idle
+        for (t, lo, hi, role) in us:
+            for k in range(lo, hi):
+                assert (t, k) not in seen
+                seen[(t, k)] = w
+    assert len(seen) == tiles * kb
+    # every split tile has exactly one finishing worker, the owner of its last stage
+    for t in range(dp, tiles):
+        owners = sorted({seen[(t, k)] for k in range(kb)})
+        assert seen[(t, kb - 1)] == owners[-1]

@@ -126,25 +126,32 @@ def test_pair_kernel(tile_n, dtype, store_mode):
     H.check_full(res, A, B, M, N, K, dtype, f"pair tile_n {tile_n}")
 
 
+@pytest.mark.parametrize("tile_k", [64, 128])
 @pytest.mark.parametrize("store_mode", [1, 2])
 @pytest.mark.parametrize("max_ctas", [2, 6, 0])
-def test_pair_kernel_persistent(store_mode, max_ctas):
+def test_pair_kernel_persistent(store_mode, max_ctas, tile_k):
     """One or three pairs walking many 256 x 256 tiles (every ring and
     accumulator phase), and the full grid."""
     M, N, K = 1100, 1300, 330
     A, B, res = case(M, N, K, wl.BF16_F32OUT, seed=35, lda=336, ldb=1304,
-                     options={"cta_group": 2, "tile_n": 256, "max_ctas": max_ctas, "store_mode": store_mode})
+                     options={"cta_group": 2, "tile_n": 256, "max_ctas": max_ctas, "store_mode": store_mode,
+                              "tile_k": tile_k})
     assert res.plan.cta_group == 2
     if max_ctas:
         assert res.plan.ctas == max_ctas
     H.check_full(res, A, B, M, N, K, wl.BF16_F32OUT, f"pair ctas {max_ctas} store {store_mode}")
 
 
-@pytest.mark.parametrize("K", [16, 64, 65, 384, 385])
-def test_pair_kernel_k_depths(K):
+@pytest.mark.parametrize("tile_k", [64, 128])
+@pytest.mark.parametrize("K", [16, 64, 65, 128, 129, 384, 385, 448])
+def test_pair_kernel_k_depths(K, tile_k):
+    """K around multiples of the stage depth (64, or 128 = two sub-blocks per
+    stage, where the last stage may hold a sub-block entirely past K)."""
     M, N = 257, 260
     lda = (K + 7) // 8 * 8   # 16-byte rows for the bulk-tensor loads of the pair kernel
-    A, B, res = case(M, N, K, wl.BF16, seed=36, lda=lda, ldb=264, options={"cta_group": 2, "tile_n": 128})
+    A, B, res = case(M, N, K, wl.BF16, seed=36, lda=lda, ldb=264,
+                     options={"cta_group": 2, "tile_n": 128, "tile_k": tile_k})
+    assert res.plan.tile_k == tile_k
     H.check_full(res, A, B, M, N, K, wl.BF16, f"pair K {K}")
 
 

@@ -1,0 +1,90 @@
+"""GPU parity of the stream-K tail of the CTA-pair kernel (tgemm_gemm_ws).
+
+Tiles left over after the last full round of CTA pairs are split along K over
+all pairs; partial fp32 sums go through the caller's workspace and the pair
+holding a tile's last k-stage adds them in a fixed order.  Checked against the
+oracle, for determinism, and for reuse of one workspace by consecutive calls.
+"""
+import numpy as np
+import pytest
+import torch
+
+import workloads as wl
+from tests import gpu_harness as H
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    H.tg()
+    torch.cuda.set_device(0)
+
+
+def case(M, N, K, dtype, options, seed, lda=None, ldb=None, ldc=None, workspace=True):
+    w = wl.Workload("sk", M, N, K, dtype, "uniform", seed)
+    A, B = wl.make_inputs(w, lda=lda, ldb=ldb)
+    return A, B, H.run_gpu(A, B, M, N, K, dtype, ldc=ldc, options=options, workspace=workspace)
+
+
+@pytest.mark.parametrize("tile_k", [64, 128])
+@pytest.mark.parametrize("tile_n", [128, 192, 224, 256])
+@pytest.mark.parametrize("dtype", [wl.BF16, wl.BF16_F32OUT, wl.F16, wl.F16_F32OUT], ids=lambda d: wl.DTYPE_NAMES[d])
+def test_stream_k_tail(dtype, tile_n, tile_k):
+    """8 pairs over 5 x ceil(1300/tile_n) pair tiles: the remainder is split
+    along K (several workers per tile, finishing pairs add 1..3 partials)."""
+    M, N, K = 1100, 1304, 640
+    opts = {"cta_group": 2, "tile_n": tile_n, "tile_k": tile_k, "max_ctas": 16, "stream_k": 2}
+    A, B, res = case(M, N, K, dtype, opts, seed=70)
+    assert res.plan.cta_group == 2 and res.plan.sk_iters > 0 and res.plan.ctas == 16
+    H.check_full(res, A, B, M, N, K, dtype, f"stream-K tile_n {tile_n} tile_k {tile_k}")
+
+
+@pytest.mark.parametrize("max_ctas,K", [(6, 1024), (8, 1024), (14, 512), (0, 4096)])
+def test_stream_k_more_workers_than_tiles(max_ctas, K):
+    """10 pair tiles on 3, 4, 7 and all pairs: remainders of 1..10 tiles, up
+    to every tile split across ~8 pairs."""
+    M, N = 512, 1280
+    opts = {"cta_group": 2, "tile_n": 256, "max_ctas": max_ctas, "stream_k": 2}
+    A, B, res = case(M, N, K, wl.BF16_F32OUT, opts, seed=71)
+    H.check_full(res, A, B, M, N, K, wl.BF16_F32OUT, f"stream-K ctas {max_ctas} K {K}")
+
+
+def test_stream_k_deterministic_and_workspace_reuse():
+    """The same workspace serves consecutive calls without clearing; the
+    fixed summation order makes repeated results bitwise equal."""
+    M, N, K = 1100, 1304, 1024
+    opts = {"cta_group": 2, "tile_n": 256, "max_ctas": 16, "stream_k": 2}
+    A, B, r1 = case(M, N, K, wl.BF16, opts, seed=72)
+    assert r1.plan.sk_iters > 0
+    r2 = H.run_gpu(A, B, M, N, K, wl.BF16, options=opts, workspace=r1.workspace)
+    assert np.array_equal(r1.raw, r2.raw)
+    # different inputs through the same workspace
+    A2, B2, _ = case(M, N, K, wl.BF16, opts, seed=73, workspace=False)
+    r3 = H.run_gpu(A2, B2, M, N, K, wl.BF16, options=opts, workspace=r1.workspace)
+    H.check_full(r3, A2, B2, M, N, K, wl.BF16, "reused workspace")
+
+
+@pytest.mark.parametrize("name", ["bf16_4096x4096x4096_f32out", "bf16_2048x2048x2048"])
+def test_stream_k_workloads(name):
+    """Full-size workloads with the stream-K tail forced on (tile choice automatic)."""
+    w = wl.BY_NAME[name]
+    A, B = wl.make_inputs(w)
+    res = H.run_gpu(A, B, w.M, w.N, w.K, w.dtype, workspace=True, options={"stream_k": 2})
+    assert res.plan.sk_iters > 0
+    if w.M * w.N <= 2048 * 2048:
+        H.check_full(res, A, B, w.M, w.N, w.K, w.dtype, name)
+    else:
+        rows, cols = H.sample_positions(w.M, w.N, 4096, seed=98)
+        H.check_sampled(res, A, B, w.K, w.dtype, rows, cols, name)
+
+
+def test_workspace_too_small_runs_whole_tiles():
+    M, N, K = 1100, 1304, 640
+    opts = {"cta_group": 2, "tile_n": 256, "max_ctas": 16, "stream_k": 2}
+    ws = torch.zeros(1024, dtype=torch.uint8, device="cuda")
+    A, B, res = case(M, N, K, wl.BF16, opts, seed=74, workspace=ws)
+    assert res.plan.sk_iters == 0
+    H.check_full(res, A, B, M, N, K, wl.BF16, "small workspace")

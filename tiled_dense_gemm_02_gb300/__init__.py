@@ -24,15 +24,16 @@ ERR_UNSUPPORTED_DEVICE, ERR_LAUNCH, ERR_DEVICE_TIMEOUT, ERR_TOO_LARGE = 5, 6, 7,
 # enum tgemm_kernel
 KERNEL_AUTO, KERNEL_TC_TMA, KERNEL_TC_COPY, KERNEL_SIMT = 0, 1, 2, 3
 
-EXPORTS = ("tgemm_gemm", "tgemm_gemm_ex", "tgemm_plan", "tgemm_device_status", "tgemm_status_string",
-           "tgemm_version")
+EXPORTS = ("tgemm_gemm", "tgemm_gemm_ex", "tgemm_gemm_ws", "tgemm_workspace_size", "tgemm_plan",
+           "tgemm_device_status", "tgemm_status_string", "tgemm_version")
 
 
 class Options(ctypes.Structure):
     """struct tgemm_options"""
     _fields_ = [("kernel", ctypes.c_int), ("tile_n", ctypes.c_int), ("group_m", ctypes.c_int),
                 ("max_ctas", ctypes.c_int), ("store_mode", ctypes.c_int), ("wait_timeout_us", ctypes.c_int),
-                ("inject_fault", ctypes.c_int), ("cta_group", ctypes.c_int), ("reserved", ctypes.c_int * 8)]
+                ("inject_fault", ctypes.c_int), ("cta_group", ctypes.c_int), ("tile_k", ctypes.c_int),
+                ("stream_k", ctypes.c_int), ("reserved", ctypes.c_int * 6)]
 
 
 class PlanInfo(ctypes.Structure):
@@ -41,7 +42,8 @@ class PlanInfo(ctypes.Structure):
                 ("tile_k", ctypes.c_int), ("stages", ctypes.c_int), ("tiles_m", ctypes.c_int),
                 ("tiles_n", ctypes.c_int), ("ctas", ctypes.c_int), ("group_m", ctypes.c_int),
                 ("a_copy_bytes", ctypes.c_int), ("b_copy_bytes", ctypes.c_int), ("store_bytes", ctypes.c_int),
-                ("smem_bytes", ctypes.c_int), ("cta_group", ctypes.c_int), ("reserved", ctypes.c_int * 3)]
+                ("smem_bytes", ctypes.c_int), ("cta_group", ctypes.c_int), ("dp_tiles", ctypes.c_int),
+                ("sk_iters", ctypes.c_int), ("workspace_bytes", ctypes.c_int)]
 
     def as_dict(self) -> dict:
         return {name: getattr(self, name) for name, _ in self._fields_ if name != "reserved"}
@@ -63,8 +65,14 @@ def _load():
     lib.tgemm_gemm.restype = ip
     lib.tgemm_gemm_ex.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, ip, ctypes.POINTER(Options), vp]
     lib.tgemm_gemm_ex.restype = ip
-    lib.tgemm_plan.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, ip, ctypes.POINTER(Options), ip,
-                               ctypes.POINTER(PlanInfo)]
+    lib.tgemm_plan.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, ip, ctypes.POINTER(Options),
+                               ctypes.c_size_t, ip, ctypes.POINTER(PlanInfo)]
+    lib.tgemm_gemm_ws.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, ip, ctypes.POINTER(Options), vp,
+                                  ctypes.c_size_t, vp]
+    lib.tgemm_gemm_ws.restype = ip
+    lib.tgemm_workspace_size.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, ip, ctypes.POINTER(Options),
+                                         ctypes.POINTER(ctypes.c_size_t)]
+    lib.tgemm_workspace_size.restype = ip
     lib.tgemm_plan.restype = ip
     lib.tgemm_device_status.argtypes = [vp]
     lib.tgemm_device_status.restype = ip
@@ -104,10 +112,24 @@ def gemm_ex(M, N, K, A, lda, B, ldb, C, ldc, dtype, options=None, stream=0) -> i
     return _lib.tgemm_gemm_ex(M, N, K, A, lda, B, ldb, C, ldc, dtype, _opts(options), stream)
 
 
-def plan(M, N, K, A, lda, B, ldb, C, ldc, dtype, options=None, sm_count=148):
+def gemm_ws(M, N, K, A, lda, B, ldb, C, ldc, dtype, options=None, workspace=0, workspace_bytes=0, stream=0) -> int:
+    """tgemm_gemm_ws: tgemm_gemm_ex with a caller-owned device workspace."""
+    return _lib.tgemm_gemm_ws(M, N, K, A, lda, B, ldb, C, ldc, dtype, _opts(options), workspace, workspace_bytes,
+                              stream)
+
+
+def workspace_size(M, N, K, A, lda, B, ldb, C, ldc, dtype, options=None):
+    """tgemm_workspace_size: (status, bytes) on the current device."""
+    n = ctypes.c_size_t(0)
+    st = _lib.tgemm_workspace_size(M, N, K, A, lda, B, ldb, C, ldc, dtype, _opts(options), ctypes.byref(n))
+    return st, n.value
+
+
+def plan(M, N, K, A, lda, B, ldb, C, ldc, dtype, options=None, sm_count=148, workspace_bytes=0):
     """tgemm_plan: (status, PlanInfo) of the dispatch decision; no GPU needed."""
     info = PlanInfo()
-    st = _lib.tgemm_plan(M, N, K, A, lda, B, ldb, C, ldc, dtype, _opts(options), sm_count, ctypes.byref(info))
+    st = _lib.tgemm_plan(M, N, K, A, lda, B, ldb, C, ldc, dtype, _opts(options), workspace_bytes, sm_count,
+                         ctypes.byref(info))
     return st, info
 
 

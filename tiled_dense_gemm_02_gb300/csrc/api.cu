@@ -4,7 +4,11 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <unistd.h>
+
 #include <algorithm>
+#include <atomic>
+#include <chrono>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
@@ -104,9 +108,13 @@ struct Plan {
   int kernel = TGEMM_KERNEL_AUTO;
   bool noop = false, zero = false;
   bool pair = false;
+  int ksub = 1;  // 64-deep K sub-blocks per shared-memory stage (pair kernel)
   int bn = 256, stages = 4, tiles_m = 0, tiles_n = 0, ctas = 0, group_m = 1;
   int a_copy = 0, b_copy = 0, store = 0;
   int smem = 0;
+  int k_blocks = 0;               // k-stages per tile
+  int dp_tiles = 0, sk_iters = 0;  // stream-K split (sk_iters == 0: whole tiles only)
+  int64_t workspace = 0;          // bytes of workspace the stream-K split uses
 };
 
 // Relative throughput of one SM per output column for each tile width,
@@ -153,13 +161,18 @@ double pair_rate(int bn) {
   }
 }
 
-int pick_pair_tile_n(int64_t M, int64_t N, int pairs, double* cost) {
+// `stream_k`: the remainder of the last round is split along K over all pairs,
+// costing its share of a round plus a fix-up of about a tenth of a round.
+int pick_pair_tile_n(int64_t M, int64_t N, int pairs, bool stream_k, double* cost) {
   int best = 256;
   double best_t = 1e300;
   for (int bn : {256, 224, 192, 128}) {
     const int64_t tiles = ((M + 2 * kTileM - 1) / (2 * kTileM)) * ((N + bn - 1) / bn);
-    const int64_t waves = (tiles + pairs - 1) / pairs;
-    const double t = static_cast<double>(waves) * bn / pair_rate(bn);
+    double waves = static_cast<double>((tiles + pairs - 1) / pairs);
+    const int64_t rem = tiles % pairs;
+    if (stream_k && rem != 0 && rem * 10 <= 9 * pairs) waves = static_cast<double>(tiles / pairs) + 0.1 +
+                                                                 static_cast<double>(rem) / pairs;
+    const double t = waves * bn / pair_rate(bn);
     if (t < best_t * 0.999) {
       best_t = t;
       best = bn;
@@ -170,7 +183,8 @@ int pick_pair_tile_n(int64_t M, int64_t N, int pairs, double* cost) {
 }
 
 int make_plan(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb,
-              const void* C, int64_t ldc, int dtype, const tgemm_options* o, int sms, int pair_cap, Plan& p) {
+              const void* C, int64_t ldc, int dtype, const tgemm_options* o, int sms, int pair_cap,
+              int64_t workspace_bytes, Plan& p) {
   if (dtype < TGEMM_F32 || dtype > TGEMM_F16_F32OUT) return TGEMM_ERR_UNSUPPORTED_DTYPE;
   if (M < 0 || N < 0 || K < 0) return TGEMM_ERR_INVALID_VALUE;
   if (M >= (int64_t(1) << 31) || N >= (int64_t(1) << 31) || K >= (int64_t(1) << 31)) return TGEMM_ERR_TOO_LARGE;
@@ -182,7 +196,8 @@ int make_plan(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const
   if (opt.kernel < TGEMM_KERNEL_AUTO || opt.kernel > TGEMM_KERNEL_SIMT) return TGEMM_ERR_INVALID_VALUE;
   if (opt.tile_n != 0 && !tc_valid_bn(opt.tile_n)) return TGEMM_ERR_INVALID_VALUE;
   if (opt.group_m < 0 || opt.max_ctas < 0 || opt.store_mode < 0 || opt.store_mode > 2 || opt.wait_timeout_us < 0 ||
-      opt.cta_group < 0 || opt.cta_group > 2)
+      opt.cta_group < 0 || opt.cta_group > 2 || (opt.tile_k != 0 && opt.tile_k != 64 && opt.tile_k != 128) ||
+      opt.stream_k < 0 || opt.stream_k > 2)
     return TGEMM_ERR_INVALID_VALUE;
   if (M == 0 || N == 0) {
     p.noop = true;
@@ -254,7 +269,9 @@ int make_plan(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const
   const int bn1 = opt.tile_n ? opt.tile_n : pick_tile_n(M, N, sms, &cost1);
   int bn2 = 0;
   if (pair_ok && opt.cta_group != 1) {
-    bn2 = opt.tile_n ? opt.tile_n : pick_pair_tile_n(M, N, pair_cap, &cost2);
+    // stream-K needs a workspace of at most sk_workspace_bytes(pairs, 256)
+    const bool sk_possible = opt.stream_k == 2 && workspace_bytes >= sk_workspace_bytes(pair_cap, 256);
+    bn2 = opt.tile_n ? opt.tile_n : pick_pair_tile_n(M, N, pair_cap, sk_possible, &cost2);
     if (opt.tile_n) {
       const int64_t t1 = ((M + kTileM - 1) / kTileM) * ((N + bn1 - 1) / bn1);
       const int64_t t2 = ((M + 2 * kTileM - 1) / (2 * kTileM)) * ((N + bn2 - 1) / bn2);
@@ -263,8 +280,12 @@ int make_plan(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const
     }
   }
   p.pair = opt.cta_group == 2 || (opt.cta_group == 0 && bn2 != 0 && cost2 < cost1);
+  if (opt.tile_k == 128 && !p.pair) return TGEMM_ERR_INVALID_VALUE;
+  // 128-deep stages halve the MMA completion signals per FLOP (measured faster
+  // for long K); short K keeps 64 so the last stage wastes little.
+  p.ksub = p.pair && (opt.tile_k == 128 || (opt.tile_k == 0 && K >= 512)) ? 2 : 1;
   p.bn = p.pair ? bn2 : bn1;
-  p.stages = p.pair ? tc2_stages(p.bn, p.store == 0) : tc_stages(p.bn);
+  p.stages = p.pair ? tc2_stages(p.bn, p.store == 0, p.ksub) : tc_stages(p.bn);
   const int tm = p.pair ? 2 * kTileM : kTileM;
   p.tiles_m = static_cast<int>((M + tm - 1) / tm);
   p.tiles_n = static_cast<int>((N + p.bn - 1) / p.bn);
@@ -272,17 +293,39 @@ int make_plan(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const
   if (tiles >= (int64_t(1) << 31)) return TGEMM_ERR_TOO_LARGE;
   p.group_m = opt.group_m ? opt.group_m : 8;
   p.group_m = std::max(1, std::min(p.group_m, p.tiles_m));
+  p.k_blocks = static_cast<int>((K + kTileK * p.ksub - 1) / (kTileK * p.ksub));
+  p.dp_tiles = static_cast<int>(tiles);
   int64_t ctas;
   if (p.pair) {
-    int64_t pairs = std::min<int64_t>(tiles, pair_cap);
-    if (opt.max_ctas) pairs = std::min<int64_t>(pairs, std::max(1, opt.max_ctas / 2));
+    int64_t cap = pair_cap;
+    if (opt.max_ctas) cap = std::min<int64_t>(cap, std::max(1, opt.max_ctas / 2));
+    int64_t pairs = std::min<int64_t>(tiles, cap);
+    // Stream-K tail: when the last round of tiles would leave pairs idle, the
+    // remaining tiles' k-stages are spread over every pair.  Needs the
+    // caller's workspace; off when the round is (nearly) full or the split
+    // would give a pair less than one k-stage on average.
+    // Auto leaves it off: on the measured shapes (bf16 2048^3, 4096^3 on
+    // GB300) the partial-sum traffic and the finishing epilogue cost more
+    // than the idle part of the last round.
+    if (opt.stream_k == 2) {
+      const int64_t rem = tiles % cap;
+      const int64_t sk_iters = rem * p.k_blocks;
+      const bool worth = rem != 0 && sk_iters >= cap;
+      const int64_t need = sk_workspace_bytes(static_cast<int>(cap), p.bn);
+      if (worth && workspace_bytes >= need && sk_iters < (int64_t(1) << 31)) {
+        pairs = cap;
+        p.dp_tiles = static_cast<int>(tiles - rem);
+        p.sk_iters = static_cast<int>(sk_iters);
+        p.workspace = need;
+      }
+    }
     ctas = 2 * pairs;
   } else {
     ctas = std::min<int64_t>(tiles, std::max(1, sms));
     if (opt.max_ctas) ctas = std::min<int64_t>(ctas, opt.max_ctas);
   }
   p.ctas = static_cast<int>(ctas);
-  p.smem = p.pair ? tc2_smem_bytes(p.bn, p.store == 0) : tc_smem_bytes(p.bn);
+  p.smem = p.pair ? tc2_smem_bytes(p.bn, p.store == 0, p.ksub) : tc_smem_bytes(p.bn);
   return TGEMM_OK;
 }
 
@@ -325,16 +368,40 @@ int pair_capacity(DeviceInfo* d) {
   return d->pair_capacity > 0 ? d->pair_capacity : 0;
 }
 
+// Epoch of stream-K flags: a flag equal to the current call's epoch marks a
+// partial sum written by this call.  Starts at a per-process pseudo-random
+// value so that flags left in a reused workspace by another process are very
+// unlikely to match; never 0 (the value of a zeroed workspace).
+std::atomic<uint32_t> g_epoch{0};
+uint32_t next_epoch() {
+  uint32_t e = g_epoch.load();
+  if (e == 0) {
+    const uint64_t seed = static_cast<uint64_t>(std::chrono::steady_clock::now().time_since_epoch().count()) ^
+                          (static_cast<uint64_t>(getpid()) << 32);
+    uint32_t start = static_cast<uint32_t>(seed * 0x9E3779B97F4A7C15ull >> 32) | 1u;
+    uint32_t expected = 0;
+    g_epoch.compare_exchange_strong(expected, start);
+  }
+  uint32_t v;
+  do {
+    v = g_epoch.fetch_add(1) + 1;
+  } while (v == 0);
+  return v;
+}
+
 int run(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb, void* C,
-        int64_t ldc, int dtype, const tgemm_options* o, cudaStream_t stream) {
+        int64_t ldc, int dtype, const tgemm_options* o, void* workspace, int64_t workspace_bytes,
+        cudaStream_t stream) {
   // validation that needs no device first, so bad arguments never touch CUDA
   Plan p;
-  int st = make_plan(M, N, K, A, lda, B, ldb, C, ldc, dtype, o, 1, 1, p);
+  if (workspace_bytes < 0 || (workspace_bytes > 0 && (!workspace || reinterpret_cast<uint64_t>(workspace) % 256)))
+    return TGEMM_ERR_INVALID_VALUE;
+  int st = make_plan(M, N, K, A, lda, B, ldb, C, ldc, dtype, o, 1, 1, workspace_bytes, p);
   if (st != TGEMM_OK || p.noop) return st;
   DeviceInfo* dev = nullptr;
   st = device_info(&dev);
   if (st != TGEMM_OK) return st;
-  st = make_plan(M, N, K, A, lda, B, ldb, C, ldc, dtype, o, dev->sm_count, pair_capacity(dev), p);
+  st = make_plan(M, N, K, A, lda, B, ldb, C, ldc, dtype, o, dev->sm_count, pair_capacity(dev), workspace_bytes, p);
   if (st != TGEMM_OK) return st;
   cudaError_t e;
   if (p.zero) {
@@ -375,7 +442,19 @@ int run(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void*
   a.tiles_m = p.tiles_m;
   a.tiles_n = p.tiles_n;
   a.num_tiles = p.tiles_m * p.tiles_n;
-  a.k_blocks = static_cast<int>((K + kTileK - 1) / kTileK);
+  a.k_blocks = p.k_blocks;
+  a.dp_tiles = p.dp_tiles;
+  a.sk_iters = p.sk_iters;
+  a.sk_partials = nullptr;
+  a.sk_flags = nullptr;
+  a.sk_epoch = 0;
+  if (p.sk_iters) {
+    const int workers = p.ctas / 2;
+    a.sk_partials = static_cast<float*>(workspace);
+    a.sk_flags = reinterpret_cast<unsigned int*>(static_cast<char*>(workspace) +
+                                                 int64_t(workers) * sk_partial_floats(p.bn) * 4);
+    a.sk_epoch = next_epoch();
+  }
   a.group_m = p.group_m;
   a.A = A;
   a.lda = lda;
@@ -399,7 +478,7 @@ int run(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void*
   a.timeout_ns = static_cast<unsigned long long>(to_us) * 1000ull;
   a.status = dev->status;
   if (p.pair)
-    e = launch_tc_pair(p.bn, p.store == 0, mA, mB, mC, a, p.ctas / 2, stream);
+    e = launch_tc_pair(p.bn, p.store == 0, p.ksub, mA, mB, mC, a, p.ctas / 2, stream);
   else
     e = launch_tc(p.bn, p.kernel == TGEMM_KERNEL_TC_COPY, mA, mB, mC, a, p.ctas, stream);
   return e == cudaSuccess ? TGEMM_OK : cuda_fail(e, "tensor-core kernel launch");
@@ -412,26 +491,52 @@ extern "C" {
 
 int tgemm_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb, void* C,
                int64_t ldc, int dtype, void* stream) {
-  return tgemm::run(M, N, K, A, lda, B, ldb, C, ldc, dtype, nullptr, static_cast<cudaStream_t>(stream));
+  return tgemm::run(M, N, K, A, lda, B, ldb, C, ldc, dtype, nullptr, nullptr, 0, static_cast<cudaStream_t>(stream));
 }
 
 int tgemm_gemm_ex(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb, void* C,
                   int64_t ldc, int dtype, const tgemm_options* opts, void* stream) {
-  return tgemm::run(M, N, K, A, lda, B, ldb, C, ldc, dtype, opts, static_cast<cudaStream_t>(stream));
+  return tgemm::run(M, N, K, A, lda, B, ldb, C, ldc, dtype, opts, nullptr, 0, static_cast<cudaStream_t>(stream));
+}
+
+int tgemm_gemm_ws(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb, void* C,
+                  int64_t ldc, int dtype, const tgemm_options* opts, void* workspace, size_t workspace_bytes,
+                  void* stream) {
+  if (workspace_bytes > static_cast<size_t>(INT64_MAX)) return TGEMM_ERR_INVALID_VALUE;
+  return tgemm::run(M, N, K, A, lda, B, ldb, C, ldc, dtype, opts, workspace, static_cast<int64_t>(workspace_bytes),
+                    static_cast<cudaStream_t>(stream));
+}
+
+int tgemm_workspace_size(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb,
+                         const void* C, int64_t ldc, int dtype, const tgemm_options* opts, size_t* bytes) {
+  if (!bytes) return TGEMM_ERR_INVALID_VALUE;
+  *bytes = 0;
+  tgemm::Plan p;
+  int st = tgemm::make_plan(M, N, K, A, lda, B, ldb, C, ldc, dtype, opts, 1, 1, 0, p);
+  if (st != TGEMM_OK || p.noop || p.zero) return st;
+  tgemm::DeviceInfo* dev = nullptr;
+  st = tgemm::device_info(&dev);
+  if (st != TGEMM_OK) return st;
+  st = tgemm::make_plan(M, N, K, A, lda, B, ldb, C, ldc, dtype, opts, dev->sm_count, tgemm::pair_capacity(dev),
+                        INT64_MAX, p);
+  if (st == TGEMM_OK) *bytes = static_cast<size_t>(p.workspace);
+  return st;
 }
 
 int tgemm_plan(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb, const void* C,
-               int64_t ldc, int dtype, const tgemm_options* opts, int sm_count, tgemm_plan_info* out) {
+               int64_t ldc, int dtype, const tgemm_options* opts, size_t workspace_bytes, int sm_count,
+               tgemm_plan_info* out) {
   tgemm::Plan p;
   const int sms = sm_count < 1 ? 1 : sm_count;
-  const int st = tgemm::make_plan(M, N, K, A, lda, B, ldb, C, ldc, dtype, opts, sms, sms / 2, p);
+  const int64_t ws = workspace_bytes > static_cast<size_t>(INT64_MAX) ? INT64_MAX : static_cast<int64_t>(workspace_bytes);
+  const int st = tgemm::make_plan(M, N, K, A, lda, B, ldb, C, ldc, dtype, opts, sms, sms / 2, ws, p);
   if (out) {
     std::memset(out, 0, sizeof *out);
     if (st == TGEMM_OK && !p.noop && !p.zero) {
       out->kernel = p.kernel;
       out->tile_m = p.kernel == TGEMM_KERNEL_SIMT ? tgemm::kSimtBM : (p.pair ? 2 : 1) * tgemm::kTileM;
       out->tile_n = p.bn;
-      out->tile_k = p.kernel == TGEMM_KERNEL_SIMT ? tgemm::kSimtBK : tgemm::kTileK;
+      out->tile_k = p.kernel == TGEMM_KERNEL_SIMT ? tgemm::kSimtBK : tgemm::kTileK * p.ksub;
       out->stages = p.stages;
       out->tiles_m = p.tiles_m;
       out->tiles_n = p.tiles_n;
@@ -442,6 +547,9 @@ int tgemm_plan(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, cons
       out->store_bytes = p.store;
       out->smem_bytes = p.smem;
       out->cta_group = p.pair ? 2 : 1;
+      out->dp_tiles = p.dp_tiles;
+      out->sk_iters = p.sk_iters;
+      out->workspace_bytes = p.workspace;
     }
   }
   return st;

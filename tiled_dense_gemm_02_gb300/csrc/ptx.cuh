@@ -93,6 +93,18 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, int32_t x, 
                : "memory");
 }
 
+// Untiled bulk copy of `bytes` (multiple of 16; both addresses 16-byte aligned)
+// from global to this CTA's shared memory; completion as transaction bytes on `bar`.
+__device__ __forceinline__ void bulk_load_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+
+// Order prior generic-proxy accesses (in any state space) before later
+// async-proxy accesses, and the reverse.
+__device__ __forceinline__ void fence_proxy_async_all() { asm volatile("fence.proxy.async;" ::: "memory"); }
+
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 
 // Wait until at most N committed bulk groups still read their shared-memory source.

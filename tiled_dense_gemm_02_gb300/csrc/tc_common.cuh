@@ -124,6 +124,192 @@ __device__ __forceinline__ void wait_teardown(uint32_t bar, uint32_t parity, con
   }
 }
 
+
+// ---------------------------------------------------------------- work units
+// A persistent worker (a CTA, or a CTA pair) processes a list of units: k-stages
+// [lo, hi) of one output tile.  Whole tiles [0, dp_tiles) go round-robin; the
+// k-stages of the remaining tiles are split evenly over all workers (stream-K),
+// so the last, partial round of tiles does not leave workers idle.  A tile
+// split across workers is finished by the worker holding its last k-stage,
+// which adds the others' fp32 partial sums in increasing worker order: the
+// result does not depend on timing.
+enum UnitRole : int { UNIT_FULL = 0, UNIT_PARTIAL = 1, UNIT_FINISH = 2 };
+struct Unit {
+  int tile, lo, hi, role;
+};
+
+__device__ __forceinline__ void sk_range(const TcArgs& a, int w, int workers, int& b, int& e) {
+  b = static_cast<int>(static_cast<int64_t>(w) * a.sk_iters / workers);
+  e = static_cast<int>(static_cast<int64_t>(w + 1) * a.sk_iters / workers);
+}
+
+// The idx-th unit of worker w; false when the list is exhausted.  The host
+// keeps every stream-K range at most one tile long, so a worker has at most
+// two stream-K units: the start of a tile (listed first since it waits for
+// nobody) and the end of the previous tile (which it finishes, listed last).
+__device__ __forceinline__ bool worker_unit(const TcArgs& a, int w, int workers, int idx, Unit& u) {
+  const int ndp = a.dp_tiles > w ? (a.dp_tiles - 1 - w) / workers + 1 : 0;
+  if (idx < ndp) {
+    u = Unit{w + idx * workers, 0, a.k_blocks, UNIT_FULL};
+    return true;
+  }
+  idx -= ndp;
+  if (a.sk_iters == 0) return false;
+  int b, e;
+  sk_range(a, w, workers, b, e);
+  if (e <= b) return false;
+  const int KB = a.k_blocks;
+  const int tb = b / KB, te = (e - 1) / KB;
+  Unit first{a.dp_tiles + tb, b - tb * KB, min(e, (tb + 1) * KB) - tb * KB, UNIT_PARTIAL};
+  if (first.hi == KB) first.role = first.lo == 0 ? UNIT_FULL : UNIT_FINISH;
+  if (te == tb) {
+    if (idx != 0) return false;
+    u = first;
+    return true;
+  }
+  Unit last{a.dp_tiles + te, 0, e - te * KB, UNIT_PARTIAL};
+  if (last.hi == KB) last.role = UNIT_FULL;
+  // the start of the later tile first (a partial sum or a whole tile, waiting
+  // for nobody), the finishing unit last: its epilogue may then use the
+  // worker's idle shared-memory ring
+  if (idx == 0) {
+    u = last;
+    return true;
+  }
+  if (idx == 1) {
+    u = first;
+    return true;
+  }
+  return false;
+}
+
+// Workers whose partial sums a finishing unit of worker w must add: the
+// contiguous range [*first, w) whose stream-K ranges reach into the tile.
+__device__ __forceinline__ int sk_first_contributor(const TcArgs& a, int w, int workers, const Unit& u) {
+  const int tile_begin = (u.tile - a.dp_tiles) * a.k_blocks;
+  int f = w;
+  while (f > 0) {
+    int b, e;
+    sk_range(a, f - 1, workers, b, e);
+    if (e <= tile_begin) break;
+    --f;
+  }
+  return f;
+}
+
+__device__ __forceinline__ void st_release_gpu(unsigned int* p, unsigned int v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ unsigned int ld_acquire_gpu(const unsigned int* p) {
+  unsigned int v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Lane 0 waits (bounded) until every flag[k * stride], k < n, holds `epoch`;
+// then every lane acquires them.  False if the wait gave up.
+__device__ __forceinline__ bool warp_wait_flags(const unsigned int* flag0, int stride, int n, unsigned int epoch,
+                                                const Ctl& c, uint32_t site) {
+  int ok = 1;
+  if (ptx::lane_id() == 0) {
+    const uint64_t t0 = ptx::globaltimer_ns();
+    for (int k = 0; k < n && ok; ++k) {
+      while (ld_acquire_gpu(flag0 + k * stride) != epoch) {
+        if (*c.abort || ptx::globaltimer_ns() - t0 > c.timeout_ns) {
+          *c.abort = 1u;
+          atomicCAS(c.status, 0u, kTimeoutFlag | site);
+          ok = 0;
+          break;
+        }
+      }
+    }
+  }
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  if (ok)
+    for (int k = 0; k < n; ++k) (void)ld_acquire_gpu(flag0 + k * stride);
+  return ok != 0;
+}
+
+// Partial-sum layout of one warp's 32 rows: 32-column sub-chunk s holds
+// 8 groups of 32 lanes x float4 (4 KB), so a warp's stores and loads are
+// contiguous and a sub-chunk is one bulk copy.
+// Write this warp's fp32 accumulator rows (BN columns) as a partial sum.
+template <int BN>
+__device__ __forceinline__ void epilogue_partial(uint32_t tbase, int lane, float* dst) {
+#pragma unroll 1
+  for (int s = 0; s < BN / 32; ++s) {
+    uint32_t w[32];
+    ptx::tmem_ld_32x32b_x32(tbase + s * 32, w);
+    ptx::tmem_wait_ld();
+    float4* d = reinterpret_cast<float4*>(dst) + s * 256 + lane;
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      __stcg(d + i * 32, make_float4(__uint_as_float(w[4 * i]), __uint_as_float(w[4 * i + 1]),
+                                     __uint_as_float(w[4 * i + 2]), __uint_as_float(w[4 * i + 3])));
+  }
+}
+
+// Epilogue of a finishing unit: the partial sums of `n_add` contributors are
+// brought into this warp's share of the idle shared-memory ring by bulk
+// copies (up to `slots` chunks of 4 KB in flight), added in contributor order
+// to the accumulator read from tensor memory, converted, and written with
+// per-thread stores, 32 columns at a time.  `bar` is this warp's mbarrier
+// (count 1); `bar_phase` carries its phase from call to call.  False if a
+// wait gave up.
+template <int BN>
+__device__ __forceinline__ bool epilogue_finish(uint32_t tbase, int row0, int col_base, const TcArgs& args, int lane,
+                                                const float* add0, int64_t add_stride, int n_add, uint8_t* ring,
+                                                int slots, uint32_t bar, uint32_t& bar_phase, const Ctl& ctl) {
+  const int out_fmt = args.out_fmt;
+  const int es = out_fmt == OUT_F32 ? 4 : 2;
+  const int granule = args.store_granule == 0 ? 16 : args.store_granule;
+  const int row = row0 + lane;
+  constexpr int SUBS = BN / 32;  // 32-column sub-chunks of the accumulator
+  const int per_batch = max(1, slots / max(n_add, 1));
+  ptx::fence_proxy_async_all();  // partial sums written by generic stores, read by bulk copies
+  for (int s0 = 0; s0 < SUBS; s0 += per_batch) {
+    const int s1 = min(SUBS, s0 + per_batch);
+    __syncwarp();
+    if (lane == 0) {
+      ptx::fence_proxy_async_smem();  // earlier reads of the slots precede the new copies
+      ptx::mbar_arrive_expect_tx(bar, static_cast<uint32_t>((s1 - s0) * n_add * 4096));
+      for (int s = s0; s < s1; ++s)
+        for (int k = 0; k < n_add; ++k)
+          ptx::bulk_load_g2s(ptx::smem_u32(ring + ((s - s0) * n_add + k) * 4096),
+                             add0 + k * add_stride + static_cast<int64_t>(s) * 1024, 4096, bar);
+    }
+    if (!warp_wait(bar, bar_phase, ctl, SITE_SK_FLAG)) return false;
+    bar_phase ^= 1u;
+    for (int s = s0; s < s1; ++s) {
+      uint32_t v[32];
+      ptx::tmem_ld_32x32b_x32(tbase + s * 32, v);
+      ptx::tmem_wait_ld();
+      for (int k = 0; k < n_add; ++k) {
+        const float4* src = reinterpret_cast<const float4*>(ring + ((s - s0) * n_add + k) * 4096) + lane;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float4 p = src[i * 32];
+          v[4 * i] = __float_as_uint(__uint_as_float(v[4 * i]) + p.x);
+          v[4 * i + 1] = __float_as_uint(__uint_as_float(v[4 * i + 1]) + p.y);
+          v[4 * i + 2] = __float_as_uint(__uint_as_float(v[4 * i + 2]) + p.z);
+          v[4 * i + 3] = __float_as_uint(__uint_as_float(v[4 * i + 3]) + p.w);
+        }
+      }
+      if (out_fmt != OUT_F32) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] = pack_pair(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]), out_fmt);
+      }
+      const int col0 = col_base + s * 32;
+      if (row < args.M && col0 < args.N) {
+        uint8_t* dst = static_cast<uint8_t*>(args.C) + (static_cast<int64_t>(row) * args.ldc + col0) * es;
+        store_segment(dst, v, min(args.N - col0, 32) * es, granule, es);
+      }
+    }
+  }
+  return true;
+}
+
 // Epilogue of one warp for one tile: read the warp's 32 tensor-memory lanes
 // (rows row0 .. row0+31) of the BN accumulator columns at `tbase`, convert to
 // the output format and write C columns col_base .. col_base+BN-1, by

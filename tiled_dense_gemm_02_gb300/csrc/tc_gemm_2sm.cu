@@ -29,18 +29,21 @@
 namespace tgemm {
 namespace {
 
-template <int BN, bool kStaged>
+template <int BN, bool kStaged, int KSUB>
 __global__ void __launch_bounds__(32 * (2 + kEpiWarps), 1)
     tc_gemm_2sm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
                        const __grid_constant__ CUtensorMap mapC, const TcArgs args) {
   constexpr int BNH = BN / 2;  // B columns staged by each CTA
-  constexpr int STAGES = tc2_stages(BN, kStaged);
-  constexpr int A_BYTES = kTileM * kTileK * 2;
-  constexpr int B_BYTES = tc_b_atoms(BNH) * 8192;
+  constexpr int STAGES = tc2_stages(BN, kStaged, KSUB);
+  constexpr int A_SUB = kTileM * kTileK * 2;           // one 64-deep K sub-block of A
+  constexpr int B_SUB = tc_b_atoms(BNH) * 8192;        // one 64-deep K sub-block of B
+  constexpr int A_BYTES = KSUB * A_SUB;
+  constexpr int B_BYTES = KSUB * B_SUB;
   constexpr int ACC = 256;
   constexpr uint32_t TMEM_COLS = 512;
   static_assert(tc2_valid_bn(BN), "pair tile width");
-  static_assert(tc2_smem_bytes(BN, kStaged) <= kSmemLimit, "shared memory per CTA");
+  static_assert(tc2_smem_bytes(BN, kStaged, KSUB) <= kSmemLimit, "shared memory per CTA");
+  static_assert(STAGES >= 3, "ring depth");
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -52,7 +55,9 @@ __global__ void __launch_bounds__(32 * (2 + kEpiWarps), 1)
   uint64_t* acc_full = empty + STAGES;
   uint64_t* acc_empty = acc_full + 2;
   uint64_t* drain = acc_empty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* epi_bar = drain + 1;  // one per epilogue warp: bulk copies of partial sums
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(epi_bar + kEpiWarps);
+  static_assert((2 * STAGES + 5 + kEpiWarps) * 8 + 8 <= kBarrierBytes, "barrier area");
   volatile uint32_t* abort_flag = tmem_slot + 1;
 
   const int warp = threadIdx.x >> 5;
@@ -72,6 +77,7 @@ __global__ void __launch_bounds__(32 * (2 + kEpiWarps), 1)
       ptx::mbar_init(ptx::smem_u32(&acc_empty[b]), 2 * kEpiWarps);  // leader only: both CTAs' epilogues
     }
     ptx::mbar_init(ptx::smem_u32(drain), 1);
+    for (int w = 0; w < kEpiWarps; ++w) ptx::mbar_init(ptx::smem_u32(&epi_bar[w]), 1);
     *abort_flag = 0u;
     ptx::fence_barrier_init();
   }
@@ -91,20 +97,19 @@ __global__ void __launch_bounds__(32 * (2 + kEpiWarps), 1)
   const uint32_t tmem_base = *tmem_slot;
 
   const Ctl ctl{abort_flag, args.timeout_ns, args.status};
-  const int num_tiles = args.num_tiles;
-  const int kbs = args.k_blocks;
 
   if (warp == 0) {
     // ------------------------------------------------ bulk-tensor producer
     if (lane == 0 && !args.inject_fault) {
-      const uint32_t tx_pair = 2u * (A_BYTES + tc_b_atoms(BNH) * 8192u);
+      const uint32_t tx_pair = 2u * (A_BYTES + B_BYTES);
       int stage = 0;
       uint32_t phase = 0, filled = 0, last_parity = 0;
       bool ok = true;
-      for (int t = pair; t < num_tiles && ok; t += npairs) {
+      Unit u;
+      for (int ui = 0; ok && worker_unit(args, pair, npairs, ui, u); ++ui) {
         int mb, nb;
-        tile_coords(t, args, mb, nb);
-        for (int kb = 0; kb < kbs; ++kb) {
+        tile_coords(u.tile, args, mb, nb);
+        for (int kb = u.lo; kb < u.hi; ++kb) {
           if (!wait_bounded(ptx::smem_u32(&empty[stage]), phase ^ 1u, ctl, SITE_PRODUCER_EMPTY)) {
             ok = false;
             break;
@@ -112,12 +117,16 @@ __global__ void __launch_bounds__(32 * (2 + kEpiWarps), 1)
           const uint32_t fb_local = ptx::smem_u32(&full[stage]);
           const uint32_t fb = ptx::mapa_shared(fb_local, 0);
           if (leader) ptx::mbar_arrive_expect_tx(fb_local, tx_pair);
-          ptx::tma_load_2d_pair(ptx::smem_u32(sA + stage * A_BYTES), &mapA, kb * kTileK,
-                                mb * 2 * kTileM + static_cast<int>(rank) * kTileM, fb);
 #pragma unroll
-          for (int j = 0; j < tc_b_atoms(BNH); ++j)
-            ptx::tma_load_2d_pair(ptx::smem_u32(sB + stage * B_BYTES + j * 8192), &mapB,
-                                  nb * BN + static_cast<int>(rank) * BNH + j * 64, kb * kTileK, fb);
+          for (int s = 0; s < KSUB; ++s) {
+            const int k0 = (kb * KSUB + s) * kTileK;  // sub-blocks past K load zeros
+            ptx::tma_load_2d_pair(ptx::smem_u32(sA + stage * A_BYTES + s * A_SUB), &mapA, k0,
+                                  mb * 2 * kTileM + static_cast<int>(rank) * kTileM, fb);
+#pragma unroll
+            for (int j = 0; j < tc_b_atoms(BNH); ++j)
+              ptx::tma_load_2d_pair(ptx::smem_u32(sB + stage * B_BYTES + s * B_SUB + j * 8192), &mapB,
+                                    nb * BN + static_cast<int>(rank) * BNH + j * 64, k0, fb);
+          }
           filled |= 1u << stage;
           last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
           if (++stage == STAGES) {
@@ -144,11 +153,12 @@ __global__ void __launch_bounds__(32 * (2 + kEpiWarps), 1)
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
-      for (int t = pair; t < num_tiles && ok; t += npairs) {
+      Unit u;
+      for (int ui = 0; ok && worker_unit(args, pair, npairs, ui, u); ++ui) {
         if (!wait_bounded(ptx::smem_u32(&acc_empty[acc]), acc_phase ^ 1u, ctl, SITE_MMA_ACC_EMPTY)) break;
         ptx::tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * ACC);
-        for (int kb = 0; kb < kbs; ++kb) {
+        for (int kb = u.lo; kb < u.hi; ++kb) {
           if (!wait_bounded(ptx::smem_u32(&full[stage]), phase, ctl, SITE_MMA_FULL)) {
             ok = false;
             break;
@@ -157,9 +167,12 @@ __global__ void __launch_bounds__(32 * (2 + kEpiWarps), 1)
           const uint32_t a0 = ptx::smem_u32(sA + stage * A_BYTES);
           const uint32_t b0 = ptx::smem_u32(sB + stage * B_BYTES);
 #pragma unroll
-          for (int k = 0; k < kTileK / 16; ++k)
-            ptx::tc_mma_f16_pair(d_tmem, sw128_desc(a0 + k * 32, 16, 1024), sw128_desc(b0 + k * 2048, 8192, 1024),
-                                 args.idesc, (kb | k) != 0 ? 1u : 0u);
+          for (int s = 0; s < KSUB; ++s)
+#pragma unroll
+            for (int k = 0; k < kTileK / 16; ++k)
+              ptx::tc_mma_f16_pair(d_tmem, sw128_desc(a0 + s * A_SUB + k * 32, 16, 1024),
+                                   sw128_desc(b0 + s * B_SUB + k * 2048, 8192, 1024), args.idesc,
+                                   (kb != u.lo || s != 0 || k != 0) ? 1u : 0u);
           ptx::tc_commit_pair_multicast(ptx::smem_u32(&empty[stage]), 0x3);
           if (++stage == STAGES) {
             stage = 0;
@@ -182,14 +195,37 @@ __global__ void __launch_bounds__(32 * (2 + kEpiWarps), 1)
     uint8_t* stage_base = sC + (warp - 2) * 2 * 4096;
     int acc = 0, sbuf = 0;
     uint32_t acc_phase = 0;
-    for (int t = pair; t < num_tiles; t += npairs) {
+    // this warp's partial-sum slot and flag (stream-K), per worker, CTA and warp
+    const int64_t slot_floats = sk_partial_floats(BN);
+    const int64_t warp_off = (static_cast<int64_t>(rank) * 4 + q) * 32 * BN;
+    const int flag_off = static_cast<int>(rank) * 4 + q;
+    uint32_t epi_phase = 0;
+    Unit u;
+    for (int ui = 0; worker_unit(args, pair, npairs, ui, u); ++ui) {
       int mb, nb;
-      tile_coords(t, args, mb, nb);
+      tile_coords(u.tile, args, mb, nb);
       if (!warp_wait(ptx::smem_u32(&acc_full[acc]), acc_phase, ctl, SITE_EPI_ACC_FULL)) break;
       ptx::tc_fence_after_sync();
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * ACC);
-      epilogue_tile<BN, kStaged>(tbase, mb * 2 * kTileM + static_cast<int>(rank) * kTileM + q * 32, nb * BN, args, &mapC,
-                        stage_base, sbuf, lane);
+      const int row0 = mb * 2 * kTileM + static_cast<int>(rank) * kTileM + q * 32;
+      if (u.role == UNIT_PARTIAL) {
+        epilogue_partial<BN>(tbase, lane, args.sk_partials + pair * slot_floats + warp_off);
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) st_release_gpu(args.sk_flags + pair * 8 + flag_off, args.sk_epoch);
+      } else if (u.role == UNIT_FINISH) {
+        // the last unit of this worker: the ring is idle, each warp borrows a quarter
+        const int first = sk_first_contributor(args, pair, npairs, u);
+        if (!warp_wait_flags(args.sk_flags + first * 8 + flag_off, 8, pair - first, args.sk_epoch, ctl, SITE_SK_FLAG))
+          break;
+        constexpr int RING_SHARE = (STAGES * (A_BYTES + B_BYTES) / kEpiWarps) / 4096 * 4096;
+        if (!epilogue_finish<BN>(tbase, row0, nb * BN, args, lane, args.sk_partials + first * slot_floats + warp_off,
+                                 slot_floats, pair - first, sA + (warp - 2) * RING_SHARE, RING_SHARE / 4096,
+                                 ptx::smem_u32(&epi_bar[warp - 2]), epi_phase, ctl))
+          break;
+      } else {
+        epilogue_tile<BN, kStaged>(tbase, row0, nb * BN, args, &mapC, stage_base, sbuf, lane);
+      }
       ptx::tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive_cluster(ptx::mapa_shared(ptx::smem_u32(&acc_empty[acc]), 0));
@@ -209,11 +245,11 @@ __global__ void __launch_bounds__(32 * (2 + kEpiWarps), 1)
   }
 }
 
-template <int BN, bool kStaged>
+template <int BN, bool kStaged, int KSUB>
 cudaError_t launch_pair(const CUtensorMap& mA, const CUtensorMap& mB, const CUtensorMap& mC, const TcArgs& args,
                         int pairs, cudaStream_t stream) {
-  constexpr int smem = tc2_smem_bytes(BN, kStaged);
-  auto kernel = tc_gemm_2sm_kernel<BN, kStaged>;
+  constexpr int smem = tc2_smem_bytes(BN, kStaged, KSUB);
+  auto kernel = tc_gemm_2sm_kernel<BN, kStaged, KSUB>;
   static std::atomic<uint64_t> done_mask{0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -241,8 +277,8 @@ cudaError_t launch_pair(const CUtensorMap& mA, const CUtensorMap& mB, const CUte
 
 template <int BN>
 cudaError_t max_pairs(int* out) {
-  constexpr int smem = tc2_smem_bytes(BN, true);
-  auto kernel = tc_gemm_2sm_kernel<BN, true>;
+  constexpr int smem = tc2_smem_bytes(BN, true, 1);
+  auto kernel = tc_gemm_2sm_kernel<BN, true, 1>;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -261,12 +297,15 @@ cudaError_t max_pairs(int* out) {
 
 }  // namespace
 
-cudaError_t launch_tc_pair(int bn, bool staged, const CUtensorMap& mA, const CUtensorMap& mB, const CUtensorMap& mC,
-                           const TcArgs& args, int pairs, cudaStream_t stream) {
-#define TGEMM_PAIR_BN(BNV)                                                          \
-  case BNV:                                                                         \
-    return staged ? launch_pair<BNV, true>(mA, mB, mC, args, pairs, stream)         \
-                  : launch_pair<BNV, false>(mA, mB, mC, args, pairs, stream);
+cudaError_t launch_tc_pair(int bn, bool staged, int ksub, const CUtensorMap& mA, const CUtensorMap& mB,
+                           const CUtensorMap& mC, const TcArgs& args, int pairs, cudaStream_t stream) {
+#define TGEMM_PAIR_BN(BNV)                                                                      \
+  case BNV:                                                                                     \
+    if (ksub == 2)                                                                              \
+      return staged ? launch_pair<BNV, true, 2>(mA, mB, mC, args, pairs, stream)                \
+                    : launch_pair<BNV, false, 2>(mA, mB, mC, args, pairs, stream);              \
+    return staged ? launch_pair<BNV, true, 1>(mA, mB, mC, args, pairs, stream)                  \
+                  : launch_pair<BNV, false, 1>(mA, mB, mC, args, pairs, stream);
   switch (bn) {
     TGEMM_PAIR_BN(128)
     TGEMM_PAIR_BN(192)

@@ -20,6 +20,7 @@ enum WaitSite : uint32_t {
   SITE_COPY_EMPTY = 5,
   SITE_DRAIN = 6,
   SITE_TEARDOWN = 7,
+  SITE_SK_FLAG = 8,
 };
 constexpr uint32_t kTimeoutFlag = 0x7E000000u;
 
@@ -41,7 +42,23 @@ struct TcArgs {
   int inject_fault;
   unsigned long long timeout_ns;
   unsigned int* status; // device status word
+  // Stream-K tail (CTA-pair kernel): tiles [0, dp_tiles) are computed whole,
+  // round-robin over the workers; the k-stages of the remaining tiles are
+  // divided evenly over all workers.  sk_iters == 0 disables it.
+  int dp_tiles;
+  int sk_iters;         // (num_tiles - dp_tiles) * k_blocks
+  float* sk_partials;   // per worker: 2 CTAs x 4 warps x (32 rows x BN) fp32
+  unsigned int* sk_flags;  // per worker, CTA and epilogue warp
+  unsigned int sk_epoch;   // value a flag holds once this call's partial is written
 };
+
+// Workspace of the stream-K tail for `workers` CTA pairs and tile width bn.
+constexpr int64_t sk_partial_floats(int bn) { return int64_t(2) * 4 * 32 * bn; }
+inline int64_t sk_workspace_bytes(int workers, int bn) {
+  const int64_t part = int64_t(workers) * sk_partial_floats(bn) * 4;
+  const int64_t flags = int64_t(workers) * 8 * 4;
+  return part + ((flags + 255) / 256) * 256;
+}
 
 struct SimtArgs {
   int M, N, K;
@@ -81,23 +98,26 @@ constexpr int tc_threads(bool copy) { return 32 * (2 + kEpiWarps + (copy ? kCopy
 // CTA-pair kernel: 256 x BN tiles, each CTA stages 128 rows of A and BN/2
 // columns of B.
 constexpr bool tc2_valid_bn(int bn) { return bn == 128 || bn == 192 || bn == 224 || bn == 256; }
-constexpr int tc2_stage_bytes(int bn) { return kTileM * kTileK * 2 + tc_b_atoms(bn / 2) * 8192; }
+// A stage holds `ksub` 64-deep K sub-blocks (one commit per stage).
+constexpr int tc2_stage_bytes(int bn, int ksub = 1) {
+  return ksub * (kTileM * kTileK * 2 + tc_b_atoms(bn / 2) * 8192);
+}
 // `staged`: the epilogue stages C tiles in shared memory for bulk-tensor
 // stores; without staging (per-thread stores) the ring gets that space.
 constexpr int tc2_epi_bytes(bool staged) { return staged ? kEpiBytes : 0; }
-constexpr int tc2_stages(int bn, bool staged) {
-  return (kSmemLimit - 1024 - tc2_epi_bytes(staged) - kBarrierBytes) / tc2_stage_bytes(bn) > 8
+constexpr int tc2_stages(int bn, bool staged, int ksub = 1) {
+  return (kSmemLimit - 1024 - tc2_epi_bytes(staged) - kBarrierBytes) / tc2_stage_bytes(bn, ksub) > 8
              ? 8
-             : (kSmemLimit - 1024 - tc2_epi_bytes(staged) - kBarrierBytes) / tc2_stage_bytes(bn);
+             : (kSmemLimit - 1024 - tc2_epi_bytes(staged) - kBarrierBytes) / tc2_stage_bytes(bn, ksub);
 }
-constexpr int tc2_smem_bytes(int bn, bool staged) {
-  return 1024 + tc2_stages(bn, staged) * tc2_stage_bytes(bn) + tc2_epi_bytes(staged) + kBarrierBytes;
+constexpr int tc2_smem_bytes(int bn, bool staged, int ksub = 1) {
+  return 1024 + tc2_stages(bn, staged, ksub) * tc2_stage_bytes(bn, ksub) + tc2_epi_bytes(staged) + kBarrierBytes;
 }
 
 // Launchers (return the cudaError_t of the launch).
 cudaError_t launch_tc(int bn, bool copy, const CUtensorMap& mapA, const CUtensorMap& mapB, const CUtensorMap& mapC,
                       const TcArgs& args, int ctas, cudaStream_t stream);
-cudaError_t launch_tc_pair(int bn, bool staged, const CUtensorMap& mapA, const CUtensorMap& mapB,
+cudaError_t launch_tc_pair(int bn, bool staged, int ksub, const CUtensorMap& mapA, const CUtensorMap& mapB,
                            const CUtensorMap& mapC, const TcArgs& args, int pairs, cudaStream_t stream);
 // Number of CTA pairs of the pair kernel that can be resident at once.
 cudaError_t tc_pair_capacity(int bn, int* pairs);
