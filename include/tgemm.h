@@ -204,6 +204,41 @@ TGEMM_API int tgemm_gemm_ws(int64_t M, int64_t N, int64_t K,
                int dtype, const tgemm_options* opts,
                void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * Allocation-free variant (the tiling pages have no counterpart; this serves
+ * callers of the library).
+ *
+ * Some callers cannot allocate device memory at the time they multiply: an
+ * application or plug-in host that hands out all device memory from its own
+ * pool, or a service whose memory budget is fixed after start-up, can neither
+ * give this library a workspace nor let it call cudaMalloc.  For them,
+ * tgemm_gemm_noalloc behaves as tgemm_gemm_ws with the stream-K split on
+ * (opts->stream_k 0 is read as 2; 1 turns it off), but takes its partial sums
+ * and flags from a scratch array of TGEMM_NOALLOC_SCRATCH_BYTES built into the
+ * library, in device memory that every GPU loading the library holds until
+ * the process exits.  It allocates nothing and calls no allocating routine.
+ *
+ *  - The first call on a device looks up the device address of that array
+ *    (with the device current); make that first call before any stream
+ *    capture.
+ *  - A call whose split would need more scratch than the array holds returns
+ *    TGEMM_ERR_TOO_LARGE and launches nothing; tgemm_workspace_size (with
+ *    stream_k = 2) gives the amount a call needs.
+ *  - Every call shares the one array.  Calls that may run at the same time on
+ *    the GPU (different streams, or several host threads) race on it and can
+ *    produce wrong results; order them on one stream or use tgemm_gemm_ws.
+ *  - Nothing in the array needs clearing between calls: a flag marks a partial
+ *    sum with the value of the call that wrote it, and the array starts zeroed.
+ *  Other arguments, status codes and semantics: as tgemm_gemm_ex.
+ */
+#define TGEMM_NOALLOC_SCRATCH_BYTES ((size_t)20 * 1024 * 1024 + 4096)
+
+TGEMM_API int tgemm_gemm_noalloc(int64_t M, int64_t N, int64_t K,
+               const void* A, int64_t lda,
+               const void* B, int64_t ldb,
+               void* C, int64_t ldc,
+               int dtype, const tgemm_options* opts, void* stream);
+
 /* Waits for `stream`, then returns and clears the device-side status word
  * that bounded in-kernel waits set when they give up (TGEMM_OK or
  * TGEMM_ERR_DEVICE_TIMEOUT).  A CUDA error while synchronising returns

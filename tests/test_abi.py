@@ -27,7 +27,7 @@ def declared_functions():
 def test_header_declares_the_abi():
     names = declared_functions()
     assert names == sorted(["tgemm_gemm", "tgemm_gemm_ex", "tgemm_gemm_ws", "tgemm_workspace_size", "tgemm_plan",
-                            "tgemm_device_status", "tgemm_status_string", "tgemm_version"])
+                            "tgemm_gemm_noalloc", "tgemm_device_status", "tgemm_status_string", "tgemm_version"])
 
 
 def test_library_exports_every_declared_symbol(tg):

@@ -25,7 +25,9 @@ ERR_UNSUPPORTED_DEVICE, ERR_LAUNCH, ERR_DEVICE_TIMEOUT, ERR_TOO_LARGE = 5, 6, 7,
 KERNEL_AUTO, KERNEL_TC_TMA, KERNEL_TC_COPY, KERNEL_SIMT = 0, 1, 2, 3
 
 EXPORTS = ("tgemm_gemm", "tgemm_gemm_ex", "tgemm_gemm_ws", "tgemm_workspace_size", "tgemm_plan",
-           "tgemm_device_status", "tgemm_status_string", "tgemm_version")
+           "tgemm_gemm_noalloc", "tgemm_device_status", "tgemm_status_string", "tgemm_version")
+# bytes of the scratch array built into the library (TGEMM_NOALLOC_SCRATCH_BYTES)
+NOALLOC_SCRATCH_BYTES = 20 * 1024 * 1024 + 4096
 
 
 class Options(ctypes.Structure):
@@ -74,6 +76,8 @@ def _load():
                                          ctypes.POINTER(ctypes.c_size_t)]
     lib.tgemm_workspace_size.restype = ip
     lib.tgemm_plan.restype = ip
+    lib.tgemm_gemm_noalloc.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, ip, ctypes.POINTER(Options), vp]
+    lib.tgemm_gemm_noalloc.restype = ip
     lib.tgemm_device_status.argtypes = [vp]
     lib.tgemm_device_status.restype = ip
     lib.tgemm_status_string.argtypes = [ip]
@@ -116,6 +120,12 @@ def gemm_ws(M, N, K, A, lda, B, ldb, C, ldc, dtype, options=None, workspace=0, w
     """tgemm_gemm_ws: tgemm_gemm_ex with a caller-owned device workspace."""
     return _lib.tgemm_gemm_ws(M, N, K, A, lda, B, ldb, C, ldc, dtype, _opts(options), workspace, workspace_bytes,
                               stream)
+
+
+def gemm_noalloc(M, N, K, A, lda, B, ldb, C, ldc, dtype, options=None, stream=0) -> int:
+    """tgemm_gemm_noalloc: the stream-K variant with the library's built-in
+    scratch array, for callers that cannot allocate device memory."""
+    return _lib.tgemm_gemm_noalloc(M, N, K, A, lda, B, ldb, C, ldc, dtype, _opts(options), stream)
 
 
 def workspace_size(M, N, K, A, lda, B, ldb, C, ldc, dtype, options=None):

@@ -590,3 +590,70 @@ const char* tgemm_status_string(int status) {
 int tgemm_version(void) { return TGEMM_VERSION; }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free entry point.
+//
+// Some callers cannot allocate device memory when they multiply: a host
+// application or plug-in host that hands out all device memory through its own
+// pool at start-up, or a service whose memory budget is fixed after
+// initialisation, cannot give this library a workspace and must not see it
+// call cudaMalloc.  tgemm_gemm_noalloc serves them.  It runs the stream-K
+// variant of the CTA-pair kernel, whose partial sums and flags live in the
+// static device array below instead of a caller workspace.  The array belongs
+// to the library image: every GPU that loads the library holds it until the
+// process exits.
+static constexpr size_t kNoAllocScratchBytes = TGEMM_NOALLOC_SCRATCH_BYTES;  // 20 MiB + 4 KiB
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+namespace {
+
+std::mutex g_noalloc_mutex;
+void* g_noalloc_ptr[64] = {};
+
+// Device address of the scratch array on the current device, looked up once
+// per device with that device current (the host-side name of the array is not
+// a device address).
+int noalloc_scratch(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return tgemm::cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= 64) return TGEMM_ERR_LAUNCH;
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess || !p) return tgemm::cuda_fail(e, "cudaGetSymbolAddress(scratch)");
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return TGEMM_OK;
+}
+
+}  // namespace
+
+extern "C" int tgemm_gemm_noalloc(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
+                                  int64_t ldb, void* C, int64_t ldc, int dtype, const tgemm_options* opts,
+                                  void* stream) {
+  tgemm_options o;
+  std::memset(&o, 0, sizeof o);
+  if (opts) o = *opts;
+  if (o.stream_k == 0) o.stream_k = 2;  // this entry point is the stream-K variant
+  // validation first (no CUDA call on bad arguments)
+  tgemm::Plan p;
+  int st = tgemm::make_plan(M, N, K, A, lda, B, ldb, C, ldc, dtype, &o, 1, 1, 0, p);
+  if (st != TGEMM_OK || p.noop) return st;
+  tgemm::DeviceInfo* dev = nullptr;
+  st = tgemm::device_info(&dev);
+  if (st != TGEMM_OK) return st;
+  // scratch the call would use with no limit; beyond the static array: rejected
+  st = tgemm::make_plan(M, N, K, A, lda, B, ldb, C, ldc, dtype, &o, dev->sm_count, tgemm::pair_capacity(dev),
+                        INT64_MAX, p);
+  if (st != TGEMM_OK) return st;
+  if (static_cast<size_t>(p.workspace) > kNoAllocScratchBytes) return TGEMM_ERR_TOO_LARGE;
+  void* scratch = nullptr;
+  st = noalloc_scratch(&scratch);
+  if (st != TGEMM_OK) return st;
+  return tgemm::run(M, N, K, A, lda, B, ldb, C, ldc, dtype, &o, scratch, static_cast<int64_t>(kNoAllocScratchBytes),
+                    static_cast<cudaStream_t>(stream));
+}
