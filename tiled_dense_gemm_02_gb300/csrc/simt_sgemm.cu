@@ -25,29 +25,11 @@
 // zeros outside the matrix and mask their stores ("CUDA tile", section 四.4).
 #include "tgemm_internal.h"
 
-#ifndef TGEMM_SIMT_BK
-#define TGEMM_SIMT_BK 16
-#endif
-#ifndef TGEMM_SIMT_FFMA2
-#define TGEMM_SIMT_FFMA2 1
-#endif
-#ifndef TGEMM_SIMT_MIN_BLOCKS
-#define TGEMM_SIMT_MIN_BLOCKS 2
-#endif
-#ifndef TGEMM_SIMT_KUNROLL
-#define TGEMM_SIMT_KUNROLL 16
-#endif
-#define TGEMM_PRAGMA(x) _Pragma(#x)
-#define TGEMM_UNROLL(n) TGEMM_PRAGMA(unroll n)
-
 namespace tgemm {
 namespace {
 
 constexpr int BM = kSimtBM, BN = kSimtBN;
-constexpr int BK = TGEMM_SIMT_BK;       // K depth of a shared-memory stage (8 or 16)
-// Paired fp32 FMA (two fused multiply-adds per instruction, each rounded once
-// as fmaf): halves the FMA instructions a warp issues per k step.
-constexpr bool FFMA2 = TGEMM_SIMT_FFMA2 != 0;
+constexpr int BK = kSimtBK;             // K depth of a shared-memory stage
 constexpr int APAD = BM + 4;
 constexpr int THREADS = 256;
 constexpr int NV = BK / 8;              // float4 loads of A (and of B) per thread per stage
@@ -120,25 +102,17 @@ __device__ __forceinline__ void load_frag(const float (*As)[APAD], const float (
 }
 
 // acc[i][j] holds columns 2j and 2j+1 of row i of the thread's 8 x 8 tile.
+// Each paired FMA is two fused multiply-adds, each rounded once as fmaf is.
 __device__ __forceinline__ void fma_frag(const Frag& f, float2 (&acc)[8][4]) {
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    if constexpr (FFMA2) {
+  for (int i = 0; i < 8; ++i)
 #pragma unroll
-      for (int j = 0; j < 4; ++j)
-        acc[i][j] = __ffma2_rn(f.a[i], make_float2(f.b[2 * j], f.b[2 * j + 1]), acc[i][j]);
-    } else {
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        acc[i][j].x = fmaf(f.a[i].x, f.b[2 * j], acc[i][j].x);
-        acc[i][j].y = fmaf(f.a[i].x, f.b[2 * j + 1], acc[i][j].y);
-      }
-    }
-  }
+    for (int j = 0; j < 4; ++j)
+      acc[i][j] = __ffma2_rn(f.a[i], make_float2(f.b[2 * j], f.b[2 * j + 1]), acc[i][j]);
 }
 
 template <bool VEC>
-__global__ void __launch_bounds__(THREADS, TGEMM_SIMT_MIN_BLOCKS) simt_sgemm_kernel(const SimtArgs p) {
+__global__ void __launch_bounds__(THREADS, 2) simt_sgemm_kernel(const SimtArgs p) {
   __shared__ __align__(16) float As[2][BK][APAD];
   __shared__ __align__(16) float Bs[2][BK][BN];
 
@@ -181,7 +155,7 @@ __global__ void __launch_bounds__(THREADS, TGEMM_SIMT_MIN_BLOCKS) simt_sgemm_ker
     const int buf = s & 1;
     const bool more = s + 1 < kstages;
     if (more) load_stage<VEC>(p, q, (s + 1) * BK, f);
-    TGEMM_UNROLL(TGEMM_SIMT_KUNROLL)
+#pragma unroll
     for (int k = 0; k < BK; ++k) {
       Frag fr;
       load_frag(As[buf], Bs[buf], k, m_in, n_in, fr);

@@ -127,6 +127,6 @@ cudaError_t launch_zero_fill(void* C, int64_t rows, int64_t cols, int64_t ldc, i
 // SIMT tile shape.
 constexpr int kSimtBM = 128;
 constexpr int kSimtBN = 128;
-constexpr int kSimtBK = 8;
+constexpr int kSimtBK = 16;
 
 }  // namespace tgemm
