@@ -126,7 +126,14 @@ typedef struct tgemm_options {
                            0 auto (currently off: on the measured shapes the
                            fix-up costs more than the idle tail), 1 off,
                            2 on whenever the tile count leaves a remainder */
-  int reserved[6];
+  int multicast;        /* clusters of two CTA pairs (CTA-pair kernel): 0 auto
+                           (currently off: measured no faster), 1 off, 2 on.  The two pairs of a 4-CTA cluster take
+                           vertically adjacent 256-row tiles of the same
+                           columns and fetch each B tile once, multicast into
+                           both (loads read this GPU's memory only).  Needs
+                           the bulk-tensor store and no stream-K split;
+                           forcing it otherwise is TGEMM_ERR_INVALID_VALUE */
+  int reserved[5];
 } tgemm_options;
 
 /* tgemm_gemm with explicit options (opts may be NULL).  A forced kernel that
@@ -157,6 +164,9 @@ typedef struct tgemm_plan_info {
   int dp_tiles;      /* tiles computed whole (all of them without stream-K) */
   int sk_iters;      /* k-stages of the remaining tiles split over the pairs */
   int workspace_bytes; /* workspace the call uses (0 without stream-K) */
+  int cluster_ctas;  /* CTAs per cluster: 1 (one-SM tiles), 2 (a pair) or 4
+                        (two pairs sharing B tiles; tiles_m still counts
+                        256-row tiles, scheduled two at a time) */
 } tgemm_plan_info;
 
 TGEMM_API int tgemm_plan(int64_t M, int64_t N, int64_t K,

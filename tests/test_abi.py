@@ -19,8 +19,11 @@ def tg():
     return tg
 
 
+HEADER = os.path.join(ROOT, "include", "tgemm.h")
+
+
 def declared_functions():
-    text = open(os.path.join(ROOT, "include", "tgemm.h")).read()
+    text = open(HEADER).read()
     return sorted(set(re.findall(r"^\s*TGEMM_API\s+(?:const\s+)?\w+\s*\*?\s*(tgemm_\w+)\s*\(", text, re.M)))
 
 
@@ -38,11 +41,31 @@ def test_library_exports_every_declared_symbol(tg):
     assert tg.version() == 10000
 
 
+def header_struct_fields(name):
+    """(field, element count) of `typedef struct name {...} name;` in the header,
+    which declares int fields only."""
+    text = open(HEADER).read()
+    body = re.search(r"typedef struct %s \{(.*?)\} %s;" % (name, name), text, re.S).group(1)
+    body = re.sub(r"/\*.*?\*/", "", body, flags=re.S)
+    fields = []
+    for decl in body.split(";"):
+        decl = decl.strip()
+        if not decl:
+            continue
+        assert decl.startswith("int "), decl
+        for part in decl[4:].split(","):
+            m = re.fullmatch(r"\s*(\w+)\s*(?:\[(\d+)\])?\s*", part)
+            fields.append((m.group(1), int(m.group(2) or 1)))
+    return fields
+
+
 def test_struct_layouts_match_header(tg):
-    assert ctypes.sizeof(tg.Options) == 16 * 4
-    assert [f for f, _ in tg.Options._fields_][:9] == ["kernel", "tile_n", "group_m", "max_ctas", "store_mode",
-                                                       "wait_timeout_us", "inject_fault", "cta_group", "tile_k"]
-    assert ctypes.sizeof(tg.PlanInfo) == 17 * 4
+    for cls, name in ((tg.Options, "tgemm_options"), (tg.PlanInfo, "tgemm_plan_info")):
+        want = header_struct_fields(name)
+        got = [(f, getattr(t, "_length_", 1)) for f, t in cls._fields_]
+        assert got == want, name
+        assert ctypes.sizeof(cls) == 4 * sum(n for _, n in want)
+    assert ctypes.sizeof(tg.Options) == 16 * 4  # the options struct keeps its size as fields are added
 
 
 def test_status_strings(tg):
@@ -139,6 +162,35 @@ def test_pair_planning(tg):
     assert st == tg.OK and p.tile_k == 128 and p.stages == 3 and p.smem_bytes <= 232448
     assert plan(tg, 4096, 4096, 4096, dtype=3, cta_group=1, tile_k=128)[0] == tg.ERR_INVALID_VALUE
     assert plan(tg, 4096, 4096, 4096, dtype=3, tile_k=96)[0] == tg.ERR_INVALID_VALUE
+
+
+def test_two_pair_cluster_planning(tg):
+    """Clusters of two CTA pairs sharing B (multicast): only when asked for,
+    with bulk-tensor operands and store, without stream-K; 512-row super-tiles
+    are scheduled, four CTAs per cluster."""
+    st, p = plan(tg, 4096, 4096, 4096, dtype=3, sms=152)
+    assert st == tg.OK and p.cluster_ctas == 2          # auto: one pair per cluster
+    st, p = plan(tg, 4096, 4096, 4096, dtype=3, sms=152, multicast=2)
+    assert st == tg.OK and p.cluster_ctas == 4 and p.cta_group == 2 and p.tile_m == 256
+    assert p.ctas == 152 and p.tiles_m == 16 and p.dp_tiles == 8 * p.tiles_n
+    # an odd count of 256-row tiles: the last super-tile has one pair's rows below C
+    st, p = plan(tg, 600, 512, 256, dtype=2, sms=152, multicast=2, tile_n=256)
+    assert st == tg.OK and (p.tiles_m, p.tiles_n, p.dp_tiles, p.ctas) == (3, 2, 4, 16)
+    # a CTA cap counts whole clusters of four
+    st, p = plan(tg, 4096, 4096, 4096, dtype=3, sms=152, multicast=2, max_ctas=10)
+    assert st == tg.OK and p.ctas == 8
+    assert plan(tg, 4096, 4096, 4096, dtype=3, sms=152, multicast=2, max_ctas=3)[0] == tg.ERR_INVALID_VALUE
+    # refused combinations
+    assert plan(tg, 4096, 4096, 4096, dtype=3, multicast=2, cta_group=1)[0] == tg.ERR_INVALID_VALUE
+    assert plan(tg, 4096, 4096, 4096, dtype=3, multicast=2, stream_k=2)[0] == tg.ERR_INVALID_VALUE
+    assert plan(tg, 4096, 4096, 4096, dtype=3, multicast=2, store_mode=2)[0] == tg.ERR_INVALID_VALUE
+    assert plan(tg, 4096, 4096, 4096, dtype=3, multicast=3)[0] == tg.ERR_INVALID_VALUE
+    assert plan(tg, 1000, 1500, 4096, dtype=2, multicast=2)[0] == tg.ERR_INVALID_VALUE  # per-thread copies
+    assert plan(tg, 512, 260, 512, dtype=2, multicast=2)[0] == tg.ERR_INVALID_VALUE     # C rows not 16-byte units
+    st, p = plan(tg, 4096, 4096, 4096, dtype=3, sms=152, multicast=1, cta_group=2)
+    assert st == tg.OK and p.cluster_ctas == 2
+    st, p = plan(tg, 300, 300, 300, dtype=0)
+    assert st == tg.OK and p.cluster_ctas == 1
 
 
 def test_dispatch_options(tg):

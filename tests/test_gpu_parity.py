@@ -53,6 +53,18 @@ def test_workload_sampled(name):
     H.check_sampled(res, A, B, w.K, w.dtype, rows, cols, name)
 
 
+@pytest.mark.parametrize("multicast", [1, 2], ids=["one_pair_clusters", "two_pair_clusters"])
+def test_headline_both_cluster_sizes(multicast):
+    """The bf16 4096^3 -> fp32 product on CTA pairs in 2-CTA clusters and in
+    4-CTA clusters sharing B tiles, sampled as above."""
+    w = wl.BY_NAME["bf16_4096x4096x4096_f32out"]
+    A, B = wl.make_inputs(w)
+    res = H.run_gpu(A, B, w.M, w.N, w.K, w.dtype, options={"cta_group": 2, "multicast": multicast})
+    assert res.plan.cluster_ctas == 2 * multicast
+    rows, cols = H.sample_positions(w.M, w.N, 4096, seed=98)
+    H.check_sampled(res, A, B, w.K, w.dtype, rows, cols, f"multicast {multicast}")
+
+
 # ------------------------------------------------------------ shape sweeps
 
 SHAPES = [(1, 1, 1), (7, 9, 5), (63, 65, 127), (128, 256, 64), (129, 257, 255), (300, 520, 200),
@@ -121,8 +133,10 @@ def test_pair_kernel(tile_n, dtype, store_mode):
     44 rows), ragged N and a K tail; staged bulk-tensor stores (store_mode 1)
     and the unstaged variant with a deeper ring (store_mode 2)."""
     M, N, K = 300, 520, 200
-    A, B, res = case(M, N, K, dtype, seed=34, options={"cta_group": 2, "tile_n": tile_n, "store_mode": store_mode})
+    A, B, res = case(M, N, K, dtype, seed=34, options={"cta_group": 2, "tile_n": tile_n, "store_mode": store_mode,
+                                                             "multicast": 1})
     assert res.plan.cta_group == 2 and res.plan.tile_m == 256 and res.plan.tile_n == tile_n
+    assert res.plan.cluster_ctas == 2
     H.check_full(res, A, B, M, N, K, dtype, f"pair tile_n {tile_n}")
 
 
@@ -135,8 +149,8 @@ def test_pair_kernel_persistent(store_mode, max_ctas, tile_k):
     M, N, K = 1100, 1300, 330
     A, B, res = case(M, N, K, wl.BF16_F32OUT, seed=35, lda=336, ldb=1304,
                      options={"cta_group": 2, "tile_n": 256, "max_ctas": max_ctas, "store_mode": store_mode,
-                              "tile_k": tile_k})
-    assert res.plan.cta_group == 2
+                              "tile_k": tile_k, "multicast": 1})
+    assert res.plan.cta_group == 2 and res.plan.cluster_ctas == 2
     if max_ctas:
         assert res.plan.ctas == max_ctas
     H.check_full(res, A, B, M, N, K, wl.BF16_F32OUT, f"pair ctas {max_ctas} store {store_mode}")
@@ -150,9 +164,53 @@ def test_pair_kernel_k_depths(K, tile_k):
     M, N = 257, 260
     lda = (K + 7) // 8 * 8   # 16-byte rows for the bulk-tensor loads of the pair kernel
     A, B, res = case(M, N, K, wl.BF16, seed=36, lda=lda, ldb=264,
-                     options={"cta_group": 2, "tile_n": 128, "tile_k": tile_k})
-    assert res.plan.tile_k == tile_k
+                     options={"cta_group": 2, "tile_n": 128, "tile_k": tile_k, "multicast": 1})
+    assert res.plan.tile_k == tile_k and res.plan.cluster_ctas == 2
     H.check_full(res, A, B, M, N, K, wl.BF16, f"pair K {K}")
+
+
+# ---------------------------------- clusters of two CTA pairs sharing B tiles
+
+@pytest.mark.parametrize("M", [300, 600])
+@pytest.mark.parametrize("tile_n", [128, 192, 224, 256])
+@pytest.mark.parametrize("dtype", TC_DTYPES, ids=lambda d: wl.DTYPE_NAMES[d])
+def test_quad_kernel(tile_n, dtype, M):
+    """Two pairs stacked along M sharing each B tile (multicast loads): ragged
+    N and a K tail; M = 300 puts 44 rows in the second pair's tile, M = 600
+    gives three 256-row tiles, so the second super-tile's lower pair lies
+    entirely below C (computed, never stored)."""
+    N, K = 520, 200
+    A, B, res = case(M, N, K, dtype, seed=37, options={"cta_group": 2, "tile_n": tile_n, "multicast": 2})
+    assert res.plan.cluster_ctas == 4 and res.plan.tile_m == 256 and res.plan.tile_n == tile_n
+    H.check_full(res, A, B, M, N, K, dtype, f"quad tile_n {tile_n} M {M}")
+
+
+@pytest.mark.parametrize("tile_k", [64, 128])
+@pytest.mark.parametrize("max_ctas,group_m", [(4, 0), (8, 1), (12, 2), (0, 0)])
+def test_quad_kernel_persistent(max_ctas, group_m, tile_k):
+    """One to three clusters walking many 512 x 256 super-tiles (every ring
+    and accumulator phase), with several raster groups, and the full grid."""
+    M, N, K = 1100, 1300, 330
+    A, B, res = case(M, N, K, wl.BF16_F32OUT, seed=38, lda=336, ldb=1304,
+                     options={"tile_n": 256, "max_ctas": max_ctas, "group_m": group_m, "tile_k": tile_k,
+                              "multicast": 2})
+    assert res.plan.cluster_ctas == 4
+    if max_ctas:
+        assert res.plan.ctas == max_ctas
+    H.check_full(res, A, B, M, N, K, wl.BF16_F32OUT, f"quad ctas {max_ctas} group {group_m}")
+
+
+@pytest.mark.parametrize("tile_k", [64, 128])
+@pytest.mark.parametrize("K", [16, 32, 33, 64, 96, 129, 448])
+def test_quad_kernel_k_depths(K, tile_k):
+    """K around the 32-row halves each pair loads of a 64-deep B sub-block
+    and around the stage depth."""
+    M, N = 600, 264  # rows of C in whole 16-byte units: the bulk-tensor store
+    lda = (K + 7) // 8 * 8
+    A, B, res = case(M, N, K, wl.BF16, seed=39, lda=lda,
+                     options={"tile_n": 128, "tile_k": tile_k, "multicast": 2})
+    assert res.plan.tile_k == tile_k and res.plan.cluster_ctas == 4
+    H.check_full(res, A, B, M, N, K, wl.BF16, f"quad K {K}")
 
 
 # ------------------------------------------------------- scheduler and edges

@@ -35,7 +35,8 @@ class Options(ctypes.Structure):
     _fields_ = [("kernel", ctypes.c_int), ("tile_n", ctypes.c_int), ("group_m", ctypes.c_int),
                 ("max_ctas", ctypes.c_int), ("store_mode", ctypes.c_int), ("wait_timeout_us", ctypes.c_int),
                 ("inject_fault", ctypes.c_int), ("cta_group", ctypes.c_int), ("tile_k", ctypes.c_int),
-                ("stream_k", ctypes.c_int), ("reserved", ctypes.c_int * 6)]
+                ("stream_k", ctypes.c_int), ("multicast", ctypes.c_int),
+                ("reserved", ctypes.c_int * 5)]
 
 
 class PlanInfo(ctypes.Structure):
@@ -45,7 +46,8 @@ class PlanInfo(ctypes.Structure):
                 ("tiles_n", ctypes.c_int), ("ctas", ctypes.c_int), ("group_m", ctypes.c_int),
                 ("a_copy_bytes", ctypes.c_int), ("b_copy_bytes", ctypes.c_int), ("store_bytes", ctypes.c_int),
                 ("smem_bytes", ctypes.c_int), ("cta_group", ctypes.c_int), ("dp_tiles", ctypes.c_int),
-                ("sk_iters", ctypes.c_int), ("workspace_bytes", ctypes.c_int)]
+                ("sk_iters", ctypes.c_int), ("workspace_bytes", ctypes.c_int),
+                ("cluster_ctas", ctypes.c_int)]
 
     def as_dict(self) -> dict:
         return {name: getattr(self, name) for name, _ in self._fields_ if name != "reserved"}

@@ -33,6 +33,7 @@ struct DeviceInfo {
   int sm_count = 0;
   unsigned int* status = nullptr;
   int pair_capacity = 0;  // resident CTA pairs of the pair kernel (0 = not queried)
+  int quad_capacity = 0;  // resident clusters of two CTA pairs (0 = not queried)
 };
 
 std::mutex g_mutex;
@@ -108,6 +109,7 @@ struct Plan {
   int kernel = TGEMM_KERNEL_AUTO;
   bool noop = false, zero = false;
   bool pair = false;
+  int cluster = 2;  // CTAs per cluster of the pair kernel: 2, or 4 (two pairs sharing B)
   int ksub = 1;  // 64-deep K sub-blocks per shared-memory stage (pair kernel)
   int bn = 256, stages = 4, tiles_m = 0, tiles_n = 0, ctas = 0, group_m = 1;
   int a_copy = 0, b_copy = 0, store = 0;
@@ -182,8 +184,26 @@ int pick_pair_tile_n(int64_t M, int64_t N, int pairs, bool stream_k, double* cos
   return best;
 }
 
+// Tile width of clusters of two pairs: each round runs `quads` 512 x BN
+// super-tiles; rows beyond the last 256-row tile are computed and dropped.
+int pick_quad_tile_n(int64_t M, int64_t N, int quads, double* cost) {
+  int best = 256;
+  double best_t = 1e300;
+  const int64_t super_rows = ((M + 2 * kTileM - 1) / (2 * kTileM) + 1) / 2;
+  for (int bn : {256, 224, 192, 128}) {
+    const int64_t units = super_rows * ((N + bn - 1) / bn);
+    const double t = static_cast<double>((units + quads - 1) / quads) * bn / pair_rate(bn);
+    if (t < best_t * 0.999) {
+      best_t = t;
+      best = bn;
+    }
+  }
+  if (cost) *cost = best_t;
+  return best;
+}
+
 int make_plan(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb,
-              const void* C, int64_t ldc, int dtype, const tgemm_options* o, int sms, int pair_cap,
+              const void* C, int64_t ldc, int dtype, const tgemm_options* o, int sms, int pair_cap, int quad_cap,
               int64_t workspace_bytes, Plan& p) {
   if (dtype < TGEMM_F32 || dtype > TGEMM_F16_F32OUT) return TGEMM_ERR_UNSUPPORTED_DTYPE;
   if (M < 0 || N < 0 || K < 0) return TGEMM_ERR_INVALID_VALUE;
@@ -197,7 +217,8 @@ int make_plan(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const
   if (opt.tile_n != 0 && !tc_valid_bn(opt.tile_n)) return TGEMM_ERR_INVALID_VALUE;
   if (opt.group_m < 0 || opt.max_ctas < 0 || opt.store_mode < 0 || opt.store_mode > 2 || opt.wait_timeout_us < 0 ||
       opt.cta_group < 0 || opt.cta_group > 2 || (opt.tile_k != 0 && opt.tile_k != 64 && opt.tile_k != 128) ||
-      opt.stream_k < 0 || opt.stream_k > 2)
+      opt.stream_k < 0 || opt.stream_k > 2 || opt.multicast < 0 || opt.multicast > 2 ||
+      (opt.multicast == 2 && (opt.stream_k == 2 || opt.cta_group == 1 || opt.store_mode == 2)))
     return TGEMM_ERR_INVALID_VALUE;
   if (M == 0 || N == 0) {
     p.noop = true;
@@ -260,27 +281,50 @@ int make_plan(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const
   }
   if (opt.store_mode == 1 && !c_tma) return TGEMM_ERR_INVALID_VALUE;
   p.store = (c_tma && opt.store_mode != 2) ? 0 : gc;
+  // a CTA cap limits every kind of worker (clusters of four need four CTAs)
+  if (opt.max_ctas) {
+    sms = std::min(sms, opt.max_ctas);
+    pair_cap = std::min(pair_cap, std::max(1, opt.max_ctas / 2));
+    quad_cap = std::min(quad_cap, opt.max_ctas / 4);
+  }
   // one SM per 128-row tile, or a CTA pair per 256-row tile (bulk-tensor
   // operands only)
   const bool pair_ok = p.kernel == TGEMM_KERNEL_TC_TMA && pair_cap > 0 &&
                        (opt.tile_n == 0 || tc2_valid_bn(opt.tile_n));
   if (opt.cta_group == 2 && !pair_ok) return TGEMM_ERR_INVALID_VALUE;
-  double cost1 = 0, cost2 = 1e300;
+  double cost1 = 0, cost2 = 1e300, cost4 = 1e300;
   const int bn1 = opt.tile_n ? opt.tile_n : pick_tile_n(M, N, sms, &cost1);
-  int bn2 = 0;
+  int bn2 = 0, bn4 = 0;
   if (pair_ok && opt.cta_group != 1) {
     // stream-K needs a workspace of at most sk_workspace_bytes(pairs, 256)
     const bool sk_possible = opt.stream_k == 2 && workspace_bytes >= sk_workspace_bytes(pair_cap, 256);
     bn2 = opt.tile_n ? opt.tile_n : pick_pair_tile_n(M, N, pair_cap, sk_possible, &cost2);
+    // Clusters of two pairs that share each B tile through multicast loads:
+    // bulk-tensor stores only, no stream-K split.  Auto leaves them off: on
+    // GB300 they halve the L2 reads of B but measured no faster (bf16 4096^3
+    // within 2 %, 8192^3 4 % slower), so the operand reads from L2 are not
+    // what bounds the pair kernel.
+    const bool quad_ok = quad_cap > 0 && p.store == 0 && opt.stream_k != 2 && opt.multicast == 2;
+    if (quad_ok) bn4 = opt.tile_n ? opt.tile_n : pick_quad_tile_n(M, N, quad_cap, &cost4);
     if (opt.tile_n) {
       const int64_t t1 = ((M + kTileM - 1) / kTileM) * ((N + bn1 - 1) / bn1);
       const int64_t t2 = ((M + 2 * kTileM - 1) / (2 * kTileM)) * ((N + bn2 - 1) / bn2);
       cost1 = static_cast<double>((t1 + sms - 1) / sms) * bn1 / width_rate(bn1);
       cost2 = static_cast<double>((t2 + pair_cap - 1) / pair_cap) * bn2 / pair_rate(bn2);
+      if (quad_ok) {
+        const int64_t t4 = (((M + 2 * kTileM - 1) / (2 * kTileM) + 1) / 2) * ((N + bn4 - 1) / bn4);
+        cost4 = static_cast<double>((t4 + quad_cap - 1) / quad_cap) * bn4 / pair_rate(bn4);
+      }
     }
   }
-  p.pair = opt.cta_group == 2 || (opt.cta_group == 0 && bn2 != 0 && cost2 < cost1);
+  p.pair = bn2 != 0 && (opt.cta_group == 2 || opt.multicast == 2 ||
+                        (opt.cta_group == 0 && std::min(cost2, cost4) < cost1));
   if (opt.tile_k == 128 && !p.pair) return TGEMM_ERR_INVALID_VALUE;
+  if (p.pair && bn4 != 0 && (opt.multicast == 2 || cost4 < cost2)) {
+    p.cluster = 4;
+    bn2 = bn4;
+  }
+  if (opt.multicast == 2 && p.cluster != 4) return TGEMM_ERR_INVALID_VALUE;
   // 128-deep stages halve the MMA completion signals per FLOP (measured faster
   // for long K); short K keeps 64 so the last stage wastes little.
   p.ksub = p.pair && (opt.tile_k == 128 || (opt.tile_k == 0 && K >= 512)) ? 2 : 1;
@@ -291,14 +335,18 @@ int make_plan(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const
   p.tiles_n = static_cast<int>((N + p.bn - 1) / p.bn);
   const int64_t tiles = int64_t(p.tiles_m) * p.tiles_n;
   if (tiles >= (int64_t(1) << 31)) return TGEMM_ERR_TOO_LARGE;
+  // rows of scheduling units: 512-row super-tiles for clusters of two pairs
+  const int sched_rows = p.cluster == 4 ? (p.tiles_m + 1) / 2 : p.tiles_m;
   p.group_m = opt.group_m ? opt.group_m : 8;
-  p.group_m = std::max(1, std::min(p.group_m, p.tiles_m));
+  p.group_m = std::max(1, std::min(p.group_m, sched_rows));
   p.k_blocks = static_cast<int>((K + kTileK * p.ksub - 1) / (kTileK * p.ksub));
-  p.dp_tiles = static_cast<int>(tiles);
+  p.dp_tiles = static_cast<int>(int64_t(sched_rows) * p.tiles_n);
   int64_t ctas;
-  if (p.pair) {
+  if (p.pair && p.cluster == 4) {
+    int64_t cap = quad_cap;
+    ctas = 4 * std::min<int64_t>(p.dp_tiles, cap);
+  } else if (p.pair) {
     int64_t cap = pair_cap;
-    if (opt.max_ctas) cap = std::min<int64_t>(cap, std::max(1, opt.max_ctas / 2));
     int64_t pairs = std::min<int64_t>(tiles, cap);
     // Stream-K tail: when the last round of tiles would leave pairs idle, the
     // remaining tiles' k-stages are spread over every pair.  Needs the
@@ -352,21 +400,24 @@ int encode_2d(CUtensorMap* map, CUtensorMapDataType type, const void* base, int6
   return TGEMM_OK;
 }
 
-// Resident CTA pairs of the pair kernel on the current device (queried once;
-// the 256-wide instantiation stands for all widths, which use the same shared
-// memory and threads).  0 when the query fails: the pair kernel is then not used.
-int pair_capacity(DeviceInfo* d) {
+// Resident clusters of the pair kernel on the current device, for clusters of
+// 2 CTAs (one pair) or 4 (two pairs), queried once.  0 when the query fails:
+// that cluster size is then not used.
+int cluster_capacity(DeviceInfo* d, int cluster) {
   std::lock_guard<std::mutex> lock(g_mutex);
-  if (d->pair_capacity == 0) {
-    int pairs = 0;
-    if (tc_pair_capacity(256, &pairs) != cudaSuccess || pairs < 1) {
+  int& cap = cluster == 4 ? d->quad_capacity : d->pair_capacity;
+  if (cap == 0) {
+    int n = 0;
+    if (tc_pair_capacity(cluster, &n) != cudaSuccess || n < 1) {
       cudaGetLastError();
-      pairs = -1;
+      n = -1;
     }
-    d->pair_capacity = pairs;
+    cap = n;
   }
-  return d->pair_capacity > 0 ? d->pair_capacity : 0;
+  return cap > 0 ? cap : 0;
 }
+int pair_capacity(DeviceInfo* d) { return cluster_capacity(d, 2); }
+int quad_capacity(DeviceInfo* d) { return cluster_capacity(d, 4); }
 
 // Epoch of stream-K flags: a flag equal to the current call's epoch marks a
 // partial sum written by this call.  Starts at a per-process pseudo-random
@@ -396,12 +447,13 @@ int run(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void*
   Plan p;
   if (workspace_bytes < 0 || (workspace_bytes > 0 && (!workspace || reinterpret_cast<uint64_t>(workspace) % 256)))
     return TGEMM_ERR_INVALID_VALUE;
-  int st = make_plan(M, N, K, A, lda, B, ldb, C, ldc, dtype, o, 1, 1, workspace_bytes, p);
+  int st = make_plan(M, N, K, A, lda, B, ldb, C, ldc, dtype, o, 1, 1, 1, workspace_bytes, p);
   if (st != TGEMM_OK || p.noop) return st;
   DeviceInfo* dev = nullptr;
   st = device_info(&dev);
   if (st != TGEMM_OK) return st;
-  st = make_plan(M, N, K, A, lda, B, ldb, C, ldc, dtype, o, dev->sm_count, pair_capacity(dev), workspace_bytes, p);
+  st = make_plan(M, N, K, A, lda, B, ldb, C, ldc, dtype, o, dev->sm_count, pair_capacity(dev), quad_capacity(dev),
+                 workspace_bytes, p);
   if (st != TGEMM_OK) return st;
   cudaError_t e;
   if (p.zero) {
@@ -431,7 +483,9 @@ int run(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void*
   std::memset(&mC, 0, sizeof mC);
   if (p.a_copy == 0 && (st = encode_2d(&mA, tmap_type(2, bf16), A, K, M, lda * 2, kTileK, kTileM)) != TGEMM_OK)
     return st;
-  if (p.b_copy == 0 && (st = encode_2d(&mB, tmap_type(2, bf16), B, N, K, ldb * 2, 64, kTileK)) != TGEMM_OK) return st;
+  // clusters of two pairs load each 64-row B atom as two 32-row halves
+  const uint32_t b_rows = p.cluster == 4 ? kTileK / 2 : kTileK;
+  if (p.b_copy == 0 && (st = encode_2d(&mB, tmap_type(2, bf16), B, N, K, ldb * 2, 64, b_rows)) != TGEMM_OK) return st;
   if (p.store == 0 && (st = encode_2d(&mC, tmap_type(eo, dtype == TGEMM_BF16), C, N, M, ldc * eo, 128 / eo, 32)) !=
                           TGEMM_OK)
     return st;
@@ -439,9 +493,9 @@ int run(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void*
   a.M = static_cast<int>(M);
   a.N = static_cast<int>(N);
   a.K = static_cast<int>(K);
-  a.tiles_m = p.tiles_m;
+  a.tiles_m = p.cluster == 4 ? (p.tiles_m + 1) / 2 : p.tiles_m;  // scheduling rows
   a.tiles_n = p.tiles_n;
-  a.num_tiles = p.tiles_m * p.tiles_n;
+  a.num_tiles = a.tiles_m * p.tiles_n;
   a.k_blocks = p.k_blocks;
   a.dp_tiles = p.dp_tiles;
   a.sk_iters = p.sk_iters;
@@ -478,7 +532,7 @@ int run(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void*
   a.timeout_ns = static_cast<unsigned long long>(to_us) * 1000ull;
   a.status = dev->status;
   if (p.pair)
-    e = launch_tc_pair(p.bn, p.store == 0, p.ksub, mA, mB, mC, a, p.ctas / 2, stream);
+    e = launch_tc_pair(p.bn, p.store == 0, p.ksub, p.cluster, mA, mB, mC, a, p.ctas / p.cluster, stream);
   else
     e = launch_tc(p.bn, p.kernel == TGEMM_KERNEL_TC_COPY, mA, mB, mC, a, p.ctas, stream);
   return e == cudaSuccess ? TGEMM_OK : cuda_fail(e, "tensor-core kernel launch");
@@ -512,13 +566,13 @@ int tgemm_workspace_size(int64_t M, int64_t N, int64_t K, const void* A, int64_t
   if (!bytes) return TGEMM_ERR_INVALID_VALUE;
   *bytes = 0;
   tgemm::Plan p;
-  int st = tgemm::make_plan(M, N, K, A, lda, B, ldb, C, ldc, dtype, opts, 1, 1, 0, p);
+  int st = tgemm::make_plan(M, N, K, A, lda, B, ldb, C, ldc, dtype, opts, 1, 1, 1, 0, p);
   if (st != TGEMM_OK || p.noop || p.zero) return st;
   tgemm::DeviceInfo* dev = nullptr;
   st = tgemm::device_info(&dev);
   if (st != TGEMM_OK) return st;
   st = tgemm::make_plan(M, N, K, A, lda, B, ldb, C, ldc, dtype, opts, dev->sm_count, tgemm::pair_capacity(dev),
-                        INT64_MAX, p);
+                        tgemm::quad_capacity(dev), INT64_MAX, p);
   if (st == TGEMM_OK) *bytes = static_cast<size_t>(p.workspace);
   return st;
 }
@@ -529,7 +583,7 @@ int tgemm_plan(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, cons
   tgemm::Plan p;
   const int sms = sm_count < 1 ? 1 : sm_count;
   const int64_t ws = workspace_bytes > static_cast<size_t>(INT64_MAX) ? INT64_MAX : static_cast<int64_t>(workspace_bytes);
-  const int st = tgemm::make_plan(M, N, K, A, lda, B, ldb, C, ldc, dtype, opts, sms, sms / 2, ws, p);
+  const int st = tgemm::make_plan(M, N, K, A, lda, B, ldb, C, ldc, dtype, opts, sms, sms / 2, sms / 4, ws, p);
   if (out) {
     std::memset(out, 0, sizeof *out);
     if (st == TGEMM_OK && !p.noop && !p.zero) {
@@ -547,6 +601,7 @@ int tgemm_plan(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, cons
       out->store_bytes = p.store;
       out->smem_bytes = p.smem;
       out->cta_group = p.pair ? 2 : 1;
+      out->cluster_ctas = p.pair ? p.cluster : 1;
       out->dp_tiles = p.dp_tiles;
       out->sk_iters = p.sk_iters;
       out->workspace_bytes = p.workspace;
@@ -641,14 +696,14 @@ extern "C" int tgemm_gemm_noalloc(int64_t M, int64_t N, int64_t K, const void* A
   if (o.stream_k == 0) o.stream_k = 2;  // this entry point is the stream-K variant
   // validation first (no CUDA call on bad arguments)
   tgemm::Plan p;
-  int st = tgemm::make_plan(M, N, K, A, lda, B, ldb, C, ldc, dtype, &o, 1, 1, 0, p);
+  int st = tgemm::make_plan(M, N, K, A, lda, B, ldb, C, ldc, dtype, &o, 1, 1, 1, 0, p);
   if (st != TGEMM_OK || p.noop) return st;
   tgemm::DeviceInfo* dev = nullptr;
   st = tgemm::device_info(&dev);
   if (st != TGEMM_OK) return st;
   // scratch the call would use with no limit; beyond the static array: rejected
   st = tgemm::make_plan(M, N, K, A, lda, B, ldb, C, ldc, dtype, &o, dev->sm_count, tgemm::pair_capacity(dev),
-                        INT64_MAX, p);
+                        tgemm::quad_capacity(dev), INT64_MAX, p);
   if (st != TGEMM_OK) return st;
   if (static_cast<size_t>(p.workspace) > kNoAllocScratchBytes) return TGEMM_ERR_TOO_LARGE;
   void* scratch = nullptr;

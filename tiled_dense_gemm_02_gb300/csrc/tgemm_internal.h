@@ -117,10 +117,15 @@ constexpr int tc2_smem_bytes(int bn, bool staged, int ksub = 1) {
 // Launchers (return the cudaError_t of the launch).
 cudaError_t launch_tc(int bn, bool copy, const CUtensorMap& mapA, const CUtensorMap& mapB, const CUtensorMap& mapC,
                       const TcArgs& args, int ctas, cudaStream_t stream);
-cudaError_t launch_tc_pair(int bn, bool staged, int ksub, const CUtensorMap& mapA, const CUtensorMap& mapB,
-                           const CUtensorMap& mapC, const TcArgs& args, int pairs, cudaStream_t stream);
-// Number of CTA pairs of the pair kernel that can be resident at once.
-cudaError_t tc_pair_capacity(int bn, int* pairs);
+// `cluster`: CTAs per cluster, 2 (one pair) or 4 (two pairs stacked along M
+// that share each B tile through multicast loads; mapB's box is then 32 rows
+// deep and args.tiles_m counts 512-row super-tiles).  `clusters` clusters.
+cudaError_t launch_tc_pair(int bn, bool staged, int ksub, int cluster, const CUtensorMap& mapA,
+                           const CUtensorMap& mapB, const CUtensorMap& mapC, const TcArgs& args, int clusters,
+                           cudaStream_t stream);
+// Number of clusters of `cluster` CTAs (2 or 4) of the pair kernel that can be
+// resident at once.
+cudaError_t tc_pair_capacity(int cluster, int* clusters);
 cudaError_t launch_simt(const SimtArgs& args, cudaStream_t stream);
 cudaError_t launch_zero_fill(void* C, int64_t rows, int64_t cols, int64_t ldc, int elem_bytes, cudaStream_t stream);
 
