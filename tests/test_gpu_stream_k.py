@@ -52,6 +52,20 @@ def test_stream_k_more_workers_than_tiles(max_ctas, K):
     H.check_full(res, A, B, M, N, K, wl.BF16_F32OUT, f"stream-K ctas {max_ctas} K {K}")
 
 
+@pytest.mark.parametrize("tile_k", [64, 128])
+@pytest.mark.parametrize("dtype", [wl.BF16, wl.BF16_F32OUT], ids=lambda d: wl.DTYPE_NAMES[d])
+@pytest.mark.parametrize("M,N", [(256, 256), (512, 256)])
+def test_stream_k_many_contributors(M, N, dtype, tile_k):
+    """One or two 256 x 256 tiles with a long K over every pair: each tile is
+    split across dozens of pairs, more partial sums than the finishing warp's
+    share of the ring holds, so they are added in several rounds."""
+    K = 16384
+    opts = {"cta_group": 2, "tile_n": 256, "tile_k": tile_k, "stream_k": 2}
+    A, B, res = case(M, N, K, dtype, opts, seed=74)
+    assert res.plan.sk_iters > 0 and res.plan.dp_tiles == 0
+    H.check_full(res, A, B, M, N, K, dtype, f"stream-K {M}x{N} K {K} tile_k {tile_k}")
+
+
 def test_stream_k_deterministic_and_workspace_reuse():
     """The same workspace serves consecutive calls without clearing; the
     fixed summation order makes repeated results bitwise equal."""

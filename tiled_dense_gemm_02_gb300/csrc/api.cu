@@ -477,15 +477,19 @@ int run(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void*
   }
   const bool bf16 = (dtype == TGEMM_BF16 || dtype == TGEMM_BF16_F32OUT);
   const int eo = out_bytes(dtype);
-  CUtensorMap mA, mB, mC;
+  CUtensorMap mA, mB, mBt, mC;
   std::memset(&mA, 0, sizeof mA);
   std::memset(&mB, 0, sizeof mB);
+  std::memset(&mBt, 0, sizeof mBt);
   std::memset(&mC, 0, sizeof mC);
   if (p.a_copy == 0 && (st = encode_2d(&mA, tmap_type(2, bf16), A, K, M, lda * 2, kTileK, kTileM)) != TGEMM_OK)
     return st;
   // clusters of two pairs load each 64-row B atom as two 32-row halves
   const uint32_t b_rows = p.cluster == 4 ? kTileK / 2 : kTileK;
   if (p.b_copy == 0 && (st = encode_2d(&mB, tmap_type(2, bf16), B, N, K, ldb * 2, 64, b_rows)) != TGEMM_OK) return st;
+  // the pair kernel's last, partial B atom (bn/2 = 96 or 112 columns per CTA)
+  const uint32_t b_tail = p.pair ? static_cast<uint32_t>((p.bn / 2) % 64) : 0u;
+  if (b_tail && (st = encode_2d(&mBt, tmap_type(2, bf16), B, N, K, ldb * 2, b_tail, b_rows)) != TGEMM_OK) return st;
   if (p.store == 0 && (st = encode_2d(&mC, tmap_type(eo, dtype == TGEMM_BF16), C, N, M, ldc * eo, 128 / eo, 32)) !=
                           TGEMM_OK)
     return st;
@@ -532,7 +536,7 @@ int run(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void*
   a.timeout_ns = static_cast<unsigned long long>(to_us) * 1000ull;
   a.status = dev->status;
   if (p.pair)
-    e = launch_tc_pair(p.bn, p.store == 0, p.ksub, p.cluster, mA, mB, mC, a, p.ctas / p.cluster, stream);
+    e = launch_tc_pair(p.bn, p.store == 0, p.ksub, p.cluster, mA, mB, mBt, mC, a, p.ctas / p.cluster, stream);
   else
     e = launch_tc(p.bn, p.kernel == TGEMM_KERNEL_TC_COPY, mA, mB, mC, a, p.ctas, stream);
   return e == cudaSuccess ? TGEMM_OK : cuda_fail(e, "tensor-core kernel launch");

@@ -250,60 +250,141 @@ __device__ __forceinline__ void epilogue_partial(uint32_t tbase, int lane, float
   }
 }
 
-// Epilogue of a finishing unit: the partial sums of `n_add` contributors are
-// brought into this warp's share of the idle shared-memory ring by bulk
-// copies (up to `slots` chunks of 4 KB in flight), added in contributor order
-// to the accumulator read from tensor memory, converted, and written with
-// per-thread stores, 32 columns at a time.  `bar` is this warp's mbarrier
-// (count 1); `bar_phase` carries its phase from call to call.  False if a
-// wait gave up.
-template <int BN>
-__device__ __forceinline__ bool epilogue_finish(uint32_t tbase, int row0, int col_base, const TcArgs& args, int lane,
+// Write one output chunk of a warp's 32 rows: 128 bytes per row (32 fp32 or
+// 64 16-bit columns), already converted into w.  With `tma_store` and a whole
+// chunk it goes through one of the warp's two 4 KB staging buffers and a
+// bulk-tensor store; otherwise (no staging, or the 32-column last chunk of a
+// 16-bit tile) by masked per-thread stores.
+__device__ __forceinline__ void store_chunk(const uint32_t (&w)[32], int row0, int col0, bool half, bool tma_store,
+                                            const TcArgs& args, const CUtensorMap* mapC, uint8_t* stage_base,
+                                            int& sbuf, int lane) {
+  const int es = args.out_fmt == OUT_F32 ? 4 : 2;
+  const int row = row0 + lane;
+  if (tma_store && !half) {
+    uint8_t* buf = stage_base + sbuf * 4096;
+    if (lane == 0) ptx::bulk_wait_group_read<1>();
+    __syncwarp();
+#pragma unroll
+    for (int ch = 0; ch < 8; ++ch)
+      *reinterpret_cast<uint4*>(buf + sw128_offset(lane, ch * 16)) =
+          make_uint4(w[4 * ch], w[4 * ch + 1], w[4 * ch + 2], w[4 * ch + 3]);
+    ptx::fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      ptx::tma_store_2d(mapC, col0, row0, ptx::smem_u32(buf));
+      ptx::bulk_commit_group();
+    }
+    sbuf ^= 1;
+  } else if (row < args.M && col0 < args.N) {
+    uint8_t* dst = static_cast<uint8_t*>(args.C) + (static_cast<int64_t>(row) * args.ldc + col0) * es;
+    const int width = half ? 32 : 128 / es;
+    const int valid = min(args.N - col0, width) * es;
+    // rows are 16-byte aligned whenever bulk stores are on
+    store_segment(dst, w, valid, tma_store ? 16 : args.store_granule, es);
+  }
+}
+
+// fp32 values of a chunk -> the output format, 128 bytes per row in w
+__device__ __forceinline__ void pack_chunk(const float (&lo)[32], const float (&hi)[32], bool half, int out_fmt,
+                                           uint32_t (&w)[32]) {
+  if (out_fmt == OUT_F32) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(lo[i]);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      w[i] = pack_pair(lo[2 * i], lo[2 * i + 1], out_fmt);
+      w[16 + i] = half ? 0u : pack_pair(hi[2 * i], hi[2 * i + 1], out_fmt);
+    }
+  }
+}
+
+// v += this lane's row of one 32 x 32 fp32 partial block in shared memory
+__device__ __forceinline__ void add_partial(float (&v)[32], const uint8_t* block, int lane) {
+  const float4* src = reinterpret_cast<const float4*>(block) + lane;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float4 q = src[i * 32];
+    v[4 * i] += q.x;
+    v[4 * i + 1] += q.y;
+    v[4 * i + 2] += q.z;
+    v[4 * i + 3] += q.w;
+  }
+}
+
+// Epilogue of a finishing unit: the fp32 partial sums of `n_add` contributors
+// (each 32 rows x BN, as epilogue_partial lays them out: 4 KB per 32 columns)
+// are brought into this warp's `slots` 4 KB slots of the idle shared-memory
+// ring by bulk copies, added in contributor order to the accumulator read from
+// tensor memory, converted and stored like epilogue_tile.  A round of copies
+// never exceeds `slots`: several whole chunks per round when all their
+// contributors fit, else one chunk per round over groups of contributors.
+// `bar` is this warp's mbarrier (count 1); `bar_phase` carries its phase from
+// call to call.  False if a wait gave up.
+template <int BN, bool kStaged>
+__device__ __forceinline__ bool epilogue_finish(uint32_t tbase, int row0, int col_base, const TcArgs& args,
+                                                const CUtensorMap* mapC, uint8_t* stage_base, int& sbuf, int lane,
                                                 const float* add0, int64_t add_stride, int n_add, uint8_t* ring,
                                                 int slots, uint32_t bar, uint32_t& bar_phase, const Ctl& ctl) {
   const int out_fmt = args.out_fmt;
   const int es = out_fmt == OUT_F32 ? 4 : 2;
-  const int granule = args.store_granule == 0 ? 16 : args.store_granule;
-  const int row = row0 + lane;
-  constexpr int SUBS = BN / 32;  // 32-column sub-chunks of the accumulator
-  const int per_batch = max(1, slots / max(n_add, 1));
+  const bool tma_store = kStaged && args.store_granule == 0;
+  const int cols_per_chunk = 128 / es;
+  const int spc = cols_per_chunk / 32;  // 32-column partial blocks per chunk: 1 or 2
+  const int chunks = (BN + cols_per_chunk - 1) / cols_per_chunk;
+  const int per_chunk = spc * n_add;
+  const int group = per_chunk <= slots ? n_add : max(1, slots / spc);  // contributors per round
+  const int cb = per_chunk <= slots ? max(1, slots / per_chunk) : 1;    // chunks per round
   ptx::fence_proxy_async_all();  // partial sums written by generic stores, read by bulk copies
-  for (int s0 = 0; s0 < SUBS; s0 += per_batch) {
-    const int s1 = min(SUBS, s0 + per_batch);
-    __syncwarp();
-    if (lane == 0) {
-      ptx::fence_proxy_async_smem();  // earlier reads of the slots precede the new copies
-      ptx::mbar_arrive_expect_tx(bar, static_cast<uint32_t>((s1 - s0) * n_add * 4096));
-      for (int s = s0; s < s1; ++s)
-        for (int k = 0; k < n_add; ++k)
-          ptx::bulk_load_g2s(ptx::smem_u32(ring + ((s - s0) * n_add + k) * 4096),
-                             add0 + k * add_stride + static_cast<int64_t>(s) * 1024, 4096, bar);
-    }
-    if (!warp_wait(bar, bar_phase, ctl, SITE_SK_FLAG)) return false;
-    bar_phase ^= 1u;
-    for (int s = s0; s < s1; ++s) {
-      uint32_t v[32];
-      ptx::tmem_ld_32x32b_x32(tbase + s * 32, v);
-      ptx::tmem_wait_ld();
-      for (int k = 0; k < n_add; ++k) {
-        const float4* src = reinterpret_cast<const float4*>(ring + ((s - s0) * n_add + k) * 4096) + lane;
+  float lo[32], hi[32];
+#pragma unroll 1
+  for (int c0 = 0; c0 < chunks; c0 += cb) {
+    const int c1 = min(chunks, c0 + cb);
+#pragma unroll 1
+    for (int k0 = 0; k0 < n_add; k0 += group) {
+      const int k1 = min(n_add, k0 + group);
+      __syncwarp();
+      if (lane == 0) {
+        ptx::fence_proxy_async_smem();  // earlier reads of the slots precede the new copies
+        int blocks = 0;
+        for (int c = c0; c < c1; ++c) blocks += min(spc, BN / 32 - c * spc);
+        ptx::mbar_arrive_expect_tx(bar, static_cast<uint32_t>(blocks * (k1 - k0) * 4096));
+        int slot = 0;
+        for (int c = c0; c < c1; ++c)
+          for (int sb = 0; sb < spc && c * spc + sb < BN / 32; ++sb)
+            for (int k = k0; k < k1; ++k, ++slot)
+              ptx::bulk_load_g2s(ptx::smem_u32(ring + slot * 4096),
+                                 add0 + k * add_stride + static_cast<int64_t>(c * spc + sb) * 1024, 4096, bar);
+      }
+      if (!warp_wait(bar, bar_phase, ctl, SITE_SK_FLAG)) return false;
+      bar_phase ^= 1u;
+      int slot = 0;
+#pragma unroll 1
+      for (int c = c0; c < c1; ++c) {
+        const int col_in_tile = c * cols_per_chunk;
+        const bool half = col_in_tile + cols_per_chunk > BN;
+        const int nsub = half ? 1 : spc;
+        if (k0 == 0) {  // the accumulator, on the chunk's first round
+          uint32_t t[32];
+          ptx::tmem_ld_32x32b_x32(tbase + col_in_tile, t);
+          ptx::tmem_wait_ld();
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float4 p = src[i * 32];
-          v[4 * i] = __float_as_uint(__uint_as_float(v[4 * i]) + p.x);
-          v[4 * i + 1] = __float_as_uint(__uint_as_float(v[4 * i + 1]) + p.y);
-          v[4 * i + 2] = __float_as_uint(__uint_as_float(v[4 * i + 2]) + p.z);
-          v[4 * i + 3] = __float_as_uint(__uint_as_float(v[4 * i + 3]) + p.w);
+          for (int i = 0; i < 32; ++i) lo[i] = __uint_as_float(t[i]);
+          if (nsub == 2) {
+            ptx::tmem_ld_32x32b_x32(tbase + col_in_tile + 32, t);
+            ptx::tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) hi[i] = __uint_as_float(t[i]);
+          }
         }
-      }
-      if (out_fmt != OUT_F32) {
-#pragma unroll
-        for (int i = 0; i < 16; ++i) v[i] = pack_pair(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]), out_fmt);
-      }
-      const int col0 = col_base + s * 32;
-      if (row < args.M && col0 < args.N) {
-        uint8_t* dst = static_cast<uint8_t*>(args.C) + (static_cast<int64_t>(row) * args.ldc + col0) * es;
-        store_segment(dst, v, min(args.N - col0, 32) * es, granule, es);
+        for (int k = k0; k < k1; ++k, ++slot) add_partial(lo, ring + slot * 4096, lane);
+        if (nsub == 2)
+          for (int k = k0; k < k1; ++k, ++slot) add_partial(hi, ring + slot * 4096, lane);
+        if (k1 == n_add) {
+          uint32_t w[32];
+          pack_chunk(lo, hi, half, out_fmt, w);
+          store_chunk(w, row0, col_base + col_in_tile, half, tma_store, args, mapC, stage_base, sbuf, lane);
+        }
       }
     }
   }
@@ -324,7 +405,6 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tbase, int row0, int col_
   const int es = out_fmt == OUT_F32 ? 4 : 2;
   // without staging buffers every chunk goes out by per-thread stores
   const bool tma_store = kStaged && args.store_granule == 0;
-  const int row = row0 + lane;
   const int cols_per_chunk = 128 / es;
   const int chunks = (BN + cols_per_chunk - 1) / cols_per_chunk;
 #pragma unroll 1
@@ -346,29 +426,7 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tbase, int row0, int col_
         w[16 + i] = half ? 0u : pack_pair(__uint_as_float(hi[2 * i]), __uint_as_float(hi[2 * i + 1]), out_fmt);
       }
     }
-    const int col0 = col_base + col_in_tile;
-    if (tma_store && !half) {
-      uint8_t* buf = stage_base + sbuf * 4096;
-      if (lane == 0) ptx::bulk_wait_group_read<1>();
-      __syncwarp();
-#pragma unroll
-      for (int ch = 0; ch < 8; ++ch)
-        *reinterpret_cast<uint4*>(buf + sw128_offset(lane, ch * 16)) =
-            make_uint4(w[4 * ch], w[4 * ch + 1], w[4 * ch + 2], w[4 * ch + 3]);
-      ptx::fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-        ptx::tma_store_2d(mapC, col0, row0, ptx::smem_u32(buf));
-        ptx::bulk_commit_group();
-      }
-      sbuf ^= 1;
-    } else if (row < args.M && col0 < args.N) {
-      uint8_t* dst = static_cast<uint8_t*>(args.C) + (static_cast<int64_t>(row) * args.ldc + col0) * es;
-      const int width = half ? 32 : cols_per_chunk;
-      const int valid = min(args.N - col0, width) * es;
-      // rows are 16-byte aligned whenever bulk stores are on
-      store_segment(dst, w, valid, tma_store ? 16 : args.store_granule, es);
-    }
+    store_chunk(w, row0, col_base + col_in_tile, half, tma_store, args, mapC, stage_base, sbuf, lane);
   }
 }
 

@@ -44,6 +44,7 @@ namespace {
 template <int BN, bool kStaged, int KSUB, int CL>
 __global__ void __launch_bounds__(32 * (2 + kEpiWarps), 1)
     tc_gemm_2sm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
+                       const __grid_constant__ CUtensorMap mapB_tail,
                        const __grid_constant__ CUtensorMap mapC, const TcArgs args) {
   constexpr int BNH = BN / 2;  // B columns staged by each CTA
   constexpr int STAGES = tc2_stages(BN, kStaged, KSUB);
@@ -51,6 +52,13 @@ __global__ void __launch_bounds__(32 * (2 + kEpiWarps), 1)
   constexpr int B_SUB = tc_b_atoms(BNH) * 8192;        // one 64-deep K sub-block of B
   constexpr int A_BYTES = KSUB * A_SUB;
   constexpr int B_BYTES = KSUB * B_SUB;
+  // A CTA's BN/2 columns of B are whole 64-column atoms plus, for BN = 192 and
+  // 224, a last atom of which only B_TAIL columns belong to the tile: that one
+  // comes through mapB_tail, whose box is B_TAIL columns wide, so no column of
+  // the neighbouring tile is fetched (the atom's other columns are never read).
+  constexpr int B_FULL = BNH / 64;
+  constexpr int B_TAIL = BNH % 64;
+  constexpr int B_LOAD = KSUB * BNH * kTileK * 2;  // bytes of B a CTA receives per stage
   constexpr int ACC = 256;
   constexpr uint32_t TMEM_COLS = 512;
   static_assert(tc2_valid_bn(BN), "pair tile width");
@@ -100,6 +108,7 @@ __global__ void __launch_bounds__(32 * (2 + kEpiWarps), 1)
   if (warp == 0 && lane == 0) {
     ptx::tma_prefetch_desc(&mapA);
     ptx::tma_prefetch_desc(&mapB);
+    if (B_TAIL) ptx::tma_prefetch_desc(&mapB_tail);
     if (kStaged && args.store_granule == 0) ptx::tma_prefetch_desc(&mapC);
   }
   if (warp == 1) {
@@ -117,7 +126,7 @@ __global__ void __launch_bounds__(32 * (2 + kEpiWarps), 1)
   if (warp == 0) {
     // ------------------------------------------------ bulk-tensor producer
     if (lane == 0 && !args.inject_fault) {
-      const uint32_t tx_pair = 2u * (A_BYTES + B_BYTES);
+      const uint32_t tx_pair = 2u * (A_BYTES + B_LOAD);
       int stage = 0;
       uint32_t phase = 0, filled = 0, last_parity = 0;
       bool ok = true;
@@ -144,12 +153,13 @@ __global__ void __launch_bounds__(32 * (2 + kEpiWarps), 1)
             for (int j = 0; j < tc_b_atoms(BNH); ++j) {
               const uint32_t dst = ptx::smem_u32(sB + stage * B_BYTES + s * B_SUB + j * 8192);
               const int col = nb * BN + static_cast<int>(half) * BNH + j * 64;
+              const CUtensorMap* map = j < B_FULL ? &mapB : &mapB_tail;
               if constexpr (CL == 2) {
-                ptx::tma_load_2d_pair(dst, &mapB, col, k0, fb);
+                ptx::tma_load_2d_pair(dst, map, col, k0, fb);
               } else {
                 // rows [32 sub, 32 sub + 32) of the 64-row atom (the swizzle
                 // pattern repeats every 8 rows, so the half lands in place)
-                ptx::tma_load_2d_pair_multicast(dst + sub * 4096u, &mapB, col, k0 + static_cast<int>(sub) * 32, fb,
+                ptx::tma_load_2d_pair_multicast(dst + sub * 4096u, map, col, k0 + static_cast<int>(sub) * 32, fb,
                                                 b_mask);
               }
             }
@@ -251,9 +261,11 @@ __global__ void __launch_bounds__(32 * (2 + kEpiWarps), 1)
                              SITE_SK_FLAG))
           break;
         constexpr int RING_SHARE = (STAGES * (A_BYTES + B_BYTES) / kEpiWarps) / 4096 * 4096;
-        if (!epilogue_finish<BN>(tbase, row0, nb * BN, args, lane, args.sk_partials + first * slot_floats + warp_off,
-                                 slot_floats, worker - first, sA + (warp - 2) * RING_SHARE, RING_SHARE / 4096,
-                                 ptx::smem_u32(&epi_bar[warp - 2]), epi_phase, ctl))
+        static_assert(RING_SHARE / 4096 >= 2, "a 16-bit output chunk needs two 4 KB slots");
+        if (!epilogue_finish<BN, kStaged>(tbase, row0, nb * BN, args, &mapC, stage_base, sbuf, lane,
+                                          args.sk_partials + first * slot_floats + warp_off, slot_floats,
+                                          worker - first, sA + (warp - 2) * RING_SHARE, RING_SHARE / 4096,
+                                          ptx::smem_u32(&epi_bar[warp - 2]), epi_phase, ctl))
           break;
       } else if (row0 < args.M) {  // a warp whose 32 rows all lie below C stores nothing
         epilogue_tile<BN, kStaged>(tbase, row0, nb * BN, args, &mapC, stage_base, sbuf, lane);
@@ -278,8 +290,8 @@ __global__ void __launch_bounds__(32 * (2 + kEpiWarps), 1)
 }
 
 template <int BN, bool kStaged, int KSUB, int CL>
-cudaError_t launch_pair(const CUtensorMap& mA, const CUtensorMap& mB, const CUtensorMap& mC, const TcArgs& args,
-                        int clusters, cudaStream_t stream) {
+cudaError_t launch_pair(const CUtensorMap& mA, const CUtensorMap& mB, const CUtensorMap& mBt, const CUtensorMap& mC,
+                        const TcArgs& args, int clusters, cudaStream_t stream) {
   constexpr int smem = tc2_smem_bytes(BN, kStaged, KSUB);
   auto kernel = tc_gemm_2sm_kernel<BN, kStaged, KSUB, CL>;
   static std::atomic<uint64_t> done_mask{0};
@@ -304,7 +316,7 @@ cudaError_t launch_pair(const CUtensorMap& mA, const CUtensorMap& mB, const CUte
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kernel, mA, mB, mC, args);
+  return cudaLaunchKernelEx(&cfg, kernel, mA, mB, mBt, mC, args);
 }
 
 // Resident clusters of the 256-wide instantiation, which stands for all
@@ -332,10 +344,11 @@ cudaError_t max_clusters(int* out) {
 }  // namespace
 
 cudaError_t launch_tc_pair(int bn, bool staged, int ksub, int cluster, const CUtensorMap& mA, const CUtensorMap& mB,
-                           const CUtensorMap& mC, const TcArgs& args, int clusters, cudaStream_t stream) {
+                           const CUtensorMap& mBt, const CUtensorMap& mC, const TcArgs& args, int clusters,
+                           cudaStream_t stream) {
   // clusters of two pairs are built for the bulk-tensor store only
   if (cluster == 4 && !staged) return cudaErrorInvalidValue;
-#define TGEMM_PAIR_LAUNCH(BNV, ST, KS, CLV) launch_pair<BNV, ST, KS, CLV>(mA, mB, mC, args, clusters, stream)
+#define TGEMM_PAIR_LAUNCH(BNV, ST, KS, CLV) launch_pair<BNV, ST, KS, CLV>(mA, mB, mBt, mC, args, clusters, stream)
 #define TGEMM_PAIR_BN(BNV)                                                                        \
   case BNV:                                                                                       \
     if (cluster == 4) return ksub == 2 ? TGEMM_PAIR_LAUNCH(BNV, true, 2, 4) : TGEMM_PAIR_LAUNCH(BNV, true, 1, 4); \

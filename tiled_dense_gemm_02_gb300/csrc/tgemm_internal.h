@@ -118,11 +118,13 @@ constexpr int tc2_smem_bytes(int bn, bool staged, int ksub = 1) {
 cudaError_t launch_tc(int bn, bool copy, const CUtensorMap& mapA, const CUtensorMap& mapB, const CUtensorMap& mapC,
                       const TcArgs& args, int ctas, cudaStream_t stream);
 // `cluster`: CTAs per cluster, 2 (one pair) or 4 (two pairs stacked along M
-// that share each B tile through multicast loads; mapB's box is then 32 rows
+// that share each B tile through multicast loads; the B boxes are then 32 rows
 // deep and args.tiles_m counts 512-row super-tiles).  `clusters` clusters.
+// mapB_tail: B with a box (bn/2) % 64 columns wide, for the last, partial
+// 64-column atom of a CTA's bn/2 columns (unused when bn/2 is a multiple of 64).
 cudaError_t launch_tc_pair(int bn, bool staged, int ksub, int cluster, const CUtensorMap& mapA,
-                           const CUtensorMap& mapB, const CUtensorMap& mapC, const TcArgs& args, int clusters,
-                           cudaStream_t stream);
+                           const CUtensorMap& mapB, const CUtensorMap& mapB_tail, const CUtensorMap& mapC,
+                           const TcArgs& args, int clusters, cudaStream_t stream);
 // Number of clusters of `cluster` CTAs (2 or 4) of the pair kernel that can be
 // resident at once.
 cudaError_t tc_pair_capacity(int cluster, int* clusters);
