@@ -41,10 +41,10 @@ sys.path.insert(0, ROOT)
 import workloads as wl  # noqa: E402
 
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
-PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "tc_gemm_2sm_bf16_4096x4096x4096_f32out.md")
-# sources of the kernel the headline workload runs (the CTA-pair kernel)
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "tc_gemm_2sm_swap_bf16_4096x4096x4096_f32out.md")
+# sources of the kernel the headline workload runs (the CTA-pair kernel with exchanged operands)
 KERNEL_SOURCES = [os.path.join(ROOT, "tiled_dense_gemm_02_gb300", "csrc", f)
-                  for f in ("tc_gemm_2sm.cu", "tc_common.cuh", "ptx.cuh", "tgemm_internal.h")]
+                  for f in ("tc_gemm_2sm_swap.cu", "tc_common.cuh", "ptx.cuh", "tgemm_internal.h")]
 
 
 def _build_library():

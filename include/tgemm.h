@@ -133,7 +133,15 @@ typedef struct tgemm_options {
                            both (loads read this GPU's memory only).  Needs
                            the bulk-tensor store and no stream-K split;
                            forcing it otherwise is TGEMM_ERR_INVALID_VALUE */
-  int reserved[5];
+  int swap_ab;          /* CTA pairs with the MMA's operands exchanged: 0 auto,
+                           1 off, 2 on.  Each pair computes a tile_m x 256
+                           tile of C as a tile of C^T = B^T A^T, so the tile
+                           height can be any of 128, 192, 224, 256 with no
+                           partly used shared-memory atoms.  Needs bulk-tensor
+                           operands and no stream-K split or multicast */
+  int tile_m;           /* tile height of swap_ab = 2 (0 auto): 128, 192, 224
+                           or 256; other kernels take 0 */
+  int reserved[3];
 } tgemm_options;
 
 /* tgemm_gemm with explicit options (opts may be NULL).  A forced kernel that
@@ -167,6 +175,8 @@ typedef struct tgemm_plan_info {
   int cluster_ctas;  /* CTAs per cluster: 1 (one-SM tiles), 2 (a pair) or 4
                         (two pairs sharing B tiles; tiles_m still counts
                         256-row tiles, scheduled two at a time) */
+  int swap_ab;       /* 1: pairs with the MMA's operands exchanged (tile_m x
+                        256 tiles of C computed as tiles of C^T) */
 } tgemm_plan_info;
 
 TGEMM_API int tgemm_plan(int64_t M, int64_t N, int64_t K,

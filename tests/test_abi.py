@@ -146,7 +146,7 @@ def test_bulk_store_needs_16_byte_row_extent(tg):
 
 
 def test_pair_planning(tg):
-    st, p = plan(tg, 4096, 4096, 4096, dtype=3, sms=152)
+    st, p = plan(tg, 4096, 4096, 4096, dtype=3, sms=152, swap_ab=1)
     assert st == tg.OK and p.cta_group == 2 and p.tile_m == 256 and p.ctas % 2 == 0 and p.ctas <= 152
     st, p = plan(tg, 4096, 4096, 4096, dtype=3, sms=152, cta_group=1)
     assert p.cta_group == 1 and p.tile_m == 128
@@ -162,6 +162,30 @@ def test_pair_planning(tg):
     assert st == tg.OK and p.tile_k == 128 and p.stages == 3 and p.smem_bytes <= 232448
     assert plan(tg, 4096, 4096, 4096, dtype=3, cta_group=1, tile_k=128)[0] == tg.ERR_INVALID_VALUE
     assert plan(tg, 4096, 4096, 4096, dtype=3, tile_k=96)[0] == tg.ERR_INVALID_VALUE
+
+
+def test_swapped_pair_planning(tg):
+    """Pairs with the MMA's operands exchanged: tile_m x 256 tiles; auto takes
+    them for large bulk-tensor products and picks the height by rounds."""
+    st, p = plan(tg, 4096, 4096, 4096, dtype=3, sms=152)
+    assert st == tg.OK and p.swap_ab == 1 and (p.tile_m, p.tile_n) == (224, 256)
+    assert (p.tiles_m, p.tiles_n, p.ctas, p.cta_group, p.cluster_ctas) == (19, 16, 152, 2, 2)
+    st, p = plan(tg, 8192, 8192, 8192, dtype=2, sms=152)
+    assert st == tg.OK and p.swap_ab == 1 and p.tile_m == 256 and p.group_m == 8
+    st, p = plan(tg, 4096, 4096, 4096, dtype=2, sms=152)
+    assert p.group_m == 4   # operands within half of L2
+    for tm in (128, 192, 224, 256):
+        st, p = plan(tg, 300, 520, 200, dtype=2, swap_ab=2, tile_m=tm)
+        assert st == tg.OK and p.swap_ab == 1 and p.tile_m == tm and p.tile_n == 256
+    # off when asked, or when another option excludes it
+    assert plan(tg, 4096, 4096, 4096, dtype=3, sms=152, swap_ab=1)[1].swap_ab == 0
+    assert plan(tg, 4096, 4096, 4096, dtype=3, sms=152, tile_n=224)[1].swap_ab == 0
+    assert plan(tg, 4096, 4096, 4096, dtype=3, sms=152, multicast=2)[1].swap_ab == 0
+    # refused combinations
+    for bad in ({"swap_ab": 2, "stream_k": 2}, {"swap_ab": 2, "multicast": 2}, {"swap_ab": 2, "cta_group": 1},
+                {"swap_ab": 2, "tile_n": 224}, {"swap_ab": 2, "tile_m": 160}, {"tile_m": 224}, {"swap_ab": 3}):
+        assert plan(tg, 4096, 4096, 4096, dtype=3, **bad)[0] == tg.ERR_INVALID_VALUE, bad
+    assert plan(tg, 1000, 1500, 4096, dtype=2, swap_ab=2)[0] == tg.ERR_INVALID_VALUE  # per-thread copies
 
 
 def test_two_pair_cluster_planning(tg):
@@ -187,8 +211,8 @@ def test_two_pair_cluster_planning(tg):
     assert plan(tg, 4096, 4096, 4096, dtype=3, multicast=3)[0] == tg.ERR_INVALID_VALUE
     assert plan(tg, 1000, 1500, 4096, dtype=2, multicast=2)[0] == tg.ERR_INVALID_VALUE  # per-thread copies
     assert plan(tg, 512, 260, 512, dtype=2, multicast=2)[0] == tg.ERR_INVALID_VALUE     # C rows not 16-byte units
-    st, p = plan(tg, 4096, 4096, 4096, dtype=3, sms=152, multicast=1, cta_group=2)
-    assert st == tg.OK and p.cluster_ctas == 2
+    st, p = plan(tg, 4096, 4096, 4096, dtype=3, sms=152, multicast=1, cta_group=2, swap_ab=1)
+    assert st == tg.OK and p.cluster_ctas == 2 and p.swap_ab == 0
     st, p = plan(tg, 300, 300, 300, dtype=0)
     assert st == tg.OK and p.cluster_ctas == 1
 

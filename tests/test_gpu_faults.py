@@ -25,9 +25,9 @@ def gpu():
     torch.cuda.set_device(0)
 
 
-@pytest.mark.parametrize("opts", [{"cta_group": 1}, {"cta_group": 2, "multicast": 1}, {"multicast": 2},
-                                  {"kernel": 2}],
-                         ids=["one_sm", "cta_pair", "two_pairs_multicast", "copy_producer"])
+@pytest.mark.parametrize("opts", [{"cta_group": 1}, {"cta_group": 2, "multicast": 1, "swap_ab": 1}, {"multicast": 2},
+                                  {"swap_ab": 2}, {"kernel": 2}],
+                         ids=["one_sm", "cta_pair", "two_pairs_multicast", "pair_swapped", "copy_producer"])
 def test_bounded_wait_reports_timeout_and_context_survives(opts):
     lib = H.tg()
     M, N, K = 512, 512, 256

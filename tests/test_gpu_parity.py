@@ -59,7 +59,7 @@ def test_headline_both_cluster_sizes(multicast):
     4-CTA clusters sharing B tiles, sampled as above."""
     w = wl.BY_NAME["bf16_4096x4096x4096_f32out"]
     A, B = wl.make_inputs(w)
-    res = H.run_gpu(A, B, w.M, w.N, w.K, w.dtype, options={"cta_group": 2, "multicast": multicast})
+    res = H.run_gpu(A, B, w.M, w.N, w.K, w.dtype, options={"cta_group": 2, "multicast": multicast, "swap_ab": 1})
     assert res.plan.cluster_ctas == 2 * multicast
     rows, cols = H.sample_positions(w.M, w.N, 4096, seed=98)
     H.check_sampled(res, A, B, w.K, w.dtype, rows, cols, f"multicast {multicast}")
@@ -134,7 +134,7 @@ def test_pair_kernel(tile_n, dtype, store_mode):
     and the unstaged variant with a deeper ring (store_mode 2)."""
     M, N, K = 300, 520, 200
     A, B, res = case(M, N, K, dtype, seed=34, options={"cta_group": 2, "tile_n": tile_n, "store_mode": store_mode,
-                                                             "multicast": 1})
+                                                             "multicast": 1, "swap_ab": 1})
     assert res.plan.cta_group == 2 and res.plan.tile_m == 256 and res.plan.tile_n == tile_n
     assert res.plan.cluster_ctas == 2
     H.check_full(res, A, B, M, N, K, dtype, f"pair tile_n {tile_n}")
@@ -149,7 +149,7 @@ def test_pair_kernel_persistent(store_mode, max_ctas, tile_k):
     M, N, K = 1100, 1300, 330
     A, B, res = case(M, N, K, wl.BF16_F32OUT, seed=35, lda=336, ldb=1304,
                      options={"cta_group": 2, "tile_n": 256, "max_ctas": max_ctas, "store_mode": store_mode,
-                              "tile_k": tile_k, "multicast": 1})
+                              "tile_k": tile_k, "multicast": 1, "swap_ab": 1})
     assert res.plan.cta_group == 2 and res.plan.cluster_ctas == 2
     if max_ctas:
         assert res.plan.ctas == max_ctas
@@ -164,7 +164,7 @@ def test_pair_kernel_k_depths(K, tile_k):
     M, N = 257, 260
     lda = (K + 7) // 8 * 8   # 16-byte rows for the bulk-tensor loads of the pair kernel
     A, B, res = case(M, N, K, wl.BF16, seed=36, lda=lda, ldb=264,
-                     options={"cta_group": 2, "tile_n": 128, "tile_k": tile_k, "multicast": 1})
+                     options={"cta_group": 2, "tile_n": 128, "tile_k": tile_k, "multicast": 1, "swap_ab": 1})
     assert res.plan.tile_k == tile_k and res.plan.cluster_ctas == 2
     H.check_full(res, A, B, M, N, K, wl.BF16, f"pair K {K}")
 
@@ -211,6 +211,59 @@ def test_quad_kernel_k_depths(K, tile_k):
                      options={"tile_n": 128, "tile_k": tile_k, "multicast": 2})
     assert res.plan.tile_k == tile_k and res.plan.cluster_ctas == 4
     H.check_full(res, A, B, M, N, K, wl.BF16, f"quad K {K}")
+
+
+# ------------------------------- pairs with the MMA's operands exchanged
+
+@pytest.mark.parametrize("store_mode", [1, 2])
+@pytest.mark.parametrize("tile_m", [128, 192, 224, 256])
+@pytest.mark.parametrize("dtype", TC_DTYPES, ids=lambda d: wl.DTYPE_NAMES[d])
+def test_swap_kernel(tile_m, dtype, store_mode):
+    """tile_m x 256 tiles computed as tiles of C^T: ragged M (a partial
+    second tile), ragged N (the second pair tile's upper CTA half lies past N),
+    a K tail; bulk-tensor stores of 32 x 32 blocks (store_mode 1) and
+    per-thread stores (store_mode 2)."""
+    M, N, K = 300, 520, 200
+    A, B, res = case(M, N, K, dtype, seed=40, options={"swap_ab": 2, "tile_m": tile_m, "store_mode": store_mode})
+    assert res.plan.swap_ab == 1 and res.plan.tile_m == tile_m and res.plan.tile_n == 256
+    assert (res.plan.store_bytes == 0) == (store_mode == 1)
+    H.check_full(res, A, B, M, N, K, dtype, f"swap tile_m {tile_m} store {store_mode}")
+
+
+@pytest.mark.parametrize("tile_k", [64, 128])
+@pytest.mark.parametrize("max_ctas,group_m", [(2, 0), (6, 3), (0, 0)])
+def test_swap_kernel_persistent(max_ctas, group_m, tile_k):
+    """One and three pairs walking many 224 x 256 tiles, and the full grid."""
+    M, N, K = 1100, 1300, 330
+    A, B, res = case(M, N, K, wl.BF16_F32OUT, seed=41, lda=336, ldb=1304,
+                     options={"swap_ab": 2, "tile_m": 224, "max_ctas": max_ctas, "group_m": group_m,
+                              "tile_k": tile_k})
+    assert res.plan.swap_ab == 1
+    if max_ctas:
+        assert res.plan.ctas == max_ctas
+    H.check_full(res, A, B, M, N, K, wl.BF16_F32OUT, f"swap ctas {max_ctas} group {group_m}")
+
+
+@pytest.mark.parametrize("tile_k", [64, 128])
+@pytest.mark.parametrize("K", [16, 64, 65, 128, 129, 384, 385, 448])
+def test_swap_kernel_k_depths(K, tile_k):
+    M, N = 257, 264
+    lda = (K + 7) // 8 * 8
+    A, B, res = case(M, N, K, wl.BF16, seed=42, lda=lda,
+                     options={"swap_ab": 2, "tile_m": 128, "tile_k": tile_k})
+    assert res.plan.tile_k == tile_k and res.plan.swap_ab == 1
+    H.check_full(res, A, B, M, N, K, wl.BF16, f"swap K {K}")
+
+
+@pytest.mark.parametrize("tile_m", [192, 224, 256])
+def test_swap_kernel_headline(tile_m):
+    """bf16 4096^3 -> fp32 in tile_m x 256 swapped tiles, sampled."""
+    w = wl.BY_NAME["bf16_4096x4096x4096_f32out"]
+    A, B = wl.make_inputs(w)
+    res = H.run_gpu(A, B, w.M, w.N, w.K, w.dtype, options={"swap_ab": 2, "tile_m": tile_m})
+    assert res.plan.swap_ab == 1 and res.plan.tile_m == tile_m
+    rows, cols = H.sample_positions(w.M, w.N, 4096, seed=97)
+    H.check_sampled(res, A, B, w.K, w.dtype, rows, cols, f"swap {tile_m}")
 
 
 # ------------------------------------------------------- scheduler and edges

@@ -109,6 +109,8 @@ struct Plan {
   int kernel = TGEMM_KERNEL_AUTO;
   bool noop = false, zero = false;
   bool pair = false;
+  bool swap = false;  // pair kernel with the MMA's operands exchanged (tile tm x 256)
+  int tm = 0;         // tile height of the swapped kernel
   int cluster = 2;  // CTAs per cluster of the pair kernel: 2, or 4 (two pairs sharing B)
   int ksub = 1;  // 64-deep K sub-blocks per shared-memory stage (pair kernel)
   int bn = 256, stages = 4, tiles_m = 0, tiles_n = 0, ctas = 0, group_m = 1;
@@ -202,6 +204,36 @@ int pick_quad_tile_n(int64_t M, int64_t N, int quads, double* cost) {
   return best;
 }
 
+// Per-SM throughput per tile row of the swapped pair kernel (tile tm x 256),
+// in the units of width_rate, measured on GB300 with bf16 8192^3 (1915, 1806,
+// 1653 and 1397 TFLOP/s for tm = 256, 224, 192, 128).  It falls with tm
+// because each SM stages and reads 128 columns of B per k-step whatever tm is.
+double swap_rate(int tm) {
+  switch (tm) {
+    case 256: return 1.16;
+    case 224: return 1.09;
+    case 192: return 1.0;
+    default: return 0.845;
+  }
+}
+
+// Tile height of the swapped pair kernel minimising rounds x tm / rate: each
+// round runs `pairs` tm x 256 tiles.
+int pick_swap_tile_m(int64_t M, int64_t N, int pairs, double* cost) {
+  int best = 256;
+  double best_t = 1e300;
+  for (int tm : {256, 224, 192, 128}) {
+    const int64_t tiles = ((M + tm - 1) / tm) * ((N + 255) / 256);
+    const double t = static_cast<double>((tiles + pairs - 1) / pairs) * tm / swap_rate(tm);
+    if (t < best_t * 0.999) {
+      best_t = t;
+      best = tm;
+    }
+  }
+  if (cost) *cost = best_t;
+  return best;
+}
+
 int make_plan(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb,
               const void* C, int64_t ldc, int dtype, const tgemm_options* o, int sms, int pair_cap, int quad_cap,
               int64_t workspace_bytes, Plan& p) {
@@ -218,7 +250,11 @@ int make_plan(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const
   if (opt.group_m < 0 || opt.max_ctas < 0 || opt.store_mode < 0 || opt.store_mode > 2 || opt.wait_timeout_us < 0 ||
       opt.cta_group < 0 || opt.cta_group > 2 || (opt.tile_k != 0 && opt.tile_k != 64 && opt.tile_k != 128) ||
       opt.stream_k < 0 || opt.stream_k > 2 || opt.multicast < 0 || opt.multicast > 2 ||
-      (opt.multicast == 2 && (opt.stream_k == 2 || opt.cta_group == 1 || opt.store_mode == 2)))
+      (opt.multicast == 2 && (opt.stream_k == 2 || opt.cta_group == 1 || opt.store_mode == 2)) ||
+      opt.swap_ab < 0 || opt.swap_ab > 2 ||
+      (opt.swap_ab == 2 && (opt.stream_k == 2 || opt.cta_group == 1 || opt.multicast == 2 ||
+                            (opt.tile_n != 0 && opt.tile_n != 256))) ||
+      (opt.tile_m != 0 && (opt.swap_ab != 2 || !tc2_valid_bn(opt.tile_m))))
     return TGEMM_ERR_INVALID_VALUE;
   if (M == 0 || N == 0) {
     p.noop = true;
@@ -292,9 +328,9 @@ int make_plan(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const
   const bool pair_ok = p.kernel == TGEMM_KERNEL_TC_TMA && pair_cap > 0 &&
                        (opt.tile_n == 0 || tc2_valid_bn(opt.tile_n));
   if (opt.cta_group == 2 && !pair_ok) return TGEMM_ERR_INVALID_VALUE;
-  double cost1 = 0, cost2 = 1e300, cost4 = 1e300;
+  double cost1 = 0, cost2 = 1e300, cost4 = 1e300, cost_s = 1e300;
   const int bn1 = opt.tile_n ? opt.tile_n : pick_tile_n(M, N, sms, &cost1);
-  int bn2 = 0, bn4 = 0;
+  int bn2 = 0, bn4 = 0, tm_s = 0;
   if (pair_ok && opt.cta_group != 1) {
     // stream-K needs a workspace of at most sk_workspace_bytes(pairs, 256)
     const bool sk_possible = opt.stream_k == 2 && workspace_bytes >= sk_workspace_bytes(pair_cap, 256);
@@ -306,6 +342,17 @@ int make_plan(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const
     // what bounds the pair kernel.
     const bool quad_ok = quad_cap > 0 && p.store == 0 && opt.stream_k != 2 && opt.multicast == 2;
     if (quad_ok) bn4 = opt.tile_n ? opt.tile_n : pick_quad_tile_n(M, N, quad_cap, &cost4);
+    // Pairs with the MMA's operands exchanged (tile tm x 256): no stream-K
+    // split, no multicast clusters.
+    const bool swap_ok = opt.stream_k != 2 && opt.multicast != 2 && opt.swap_ab != 1 &&
+                         (opt.tile_n == 0 || opt.tile_n == 256);
+    if (swap_ok) {
+      tm_s = opt.tile_m ? opt.tile_m : pick_swap_tile_m(M, N, pair_cap, &cost_s);
+      if (opt.tile_m) {
+        const int64_t ts = ((M + tm_s - 1) / tm_s) * ((N + 255) / 256);
+        cost_s = static_cast<double>((ts + pair_cap - 1) / pair_cap) * tm_s / swap_rate(tm_s);
+      }
+    }
     if (opt.tile_n) {
       const int64_t t1 = ((M + kTileM - 1) / kTileM) * ((N + bn1 - 1) / bn1);
       const int64_t t2 = ((M + 2 * kTileM - 1) / (2 * kTileM)) * ((N + bn2 - 1) / bn2);
@@ -317,27 +364,39 @@ int make_plan(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const
       }
     }
   }
-  p.pair = bn2 != 0 && (opt.cta_group == 2 || opt.multicast == 2 ||
-                        (opt.cta_group == 0 && std::min(cost2, cost4) < cost1));
-  if (opt.tile_k == 128 && !p.pair) return TGEMM_ERR_INVALID_VALUE;
-  if (p.pair && bn4 != 0 && (opt.multicast == 2 || cost4 < cost2)) {
+  p.pair = bn2 != 0 && (opt.cta_group == 2 || opt.multicast == 2 || opt.swap_ab == 2 ||
+                        (opt.cta_group == 0 && std::min(std::min(cost2, cost4), cost_s) < cost1));
+  if (p.pair && tm_s != 0 && (opt.swap_ab == 2 || (cost_s < cost2 && cost_s < cost4))) {
+    p.swap = true;
+    p.tm = tm_s;
+    bn2 = 256;
+  } else if (p.pair && bn4 != 0 && (opt.multicast == 2 || cost4 < cost2)) {
     p.cluster = 4;
     bn2 = bn4;
   }
   if (opt.multicast == 2 && p.cluster != 4) return TGEMM_ERR_INVALID_VALUE;
+  if (opt.swap_ab == 2 && !p.swap) return TGEMM_ERR_INVALID_VALUE;
+  if (opt.tile_k == 128 && !p.pair) return TGEMM_ERR_INVALID_VALUE;
   // 128-deep stages halve the MMA completion signals per FLOP (measured faster
   // for long K); short K keeps 64 so the last stage wastes little.
   p.ksub = p.pair && (opt.tile_k == 128 || (opt.tile_k == 0 && K >= 512)) ? 2 : 1;
   p.bn = p.pair ? bn2 : bn1;
-  p.stages = p.pair ? tc2_stages(p.bn, p.store == 0, p.ksub) : tc_stages(p.bn);
-  const int tm = p.pair ? 2 * kTileM : kTileM;
+  // the swapped kernel always keeps its staging buffers (sized by its height)
+  p.stages = p.swap ? tc2_stages(p.tm, true, p.ksub)
+                    : (p.pair ? tc2_stages(p.bn, p.store == 0, p.ksub) : tc_stages(p.bn));
+  const int tm = p.swap ? p.tm : (p.pair ? 2 * kTileM : kTileM);
   p.tiles_m = static_cast<int>((M + tm - 1) / tm);
   p.tiles_n = static_cast<int>((N + p.bn - 1) / p.bn);
   const int64_t tiles = int64_t(p.tiles_m) * p.tiles_n;
   if (tiles >= (int64_t(1) << 31)) return TGEMM_ERR_TOO_LARGE;
   // rows of scheduling units: 512-row super-tiles for clusters of two pairs
   const int sched_rows = p.cluster == 4 ? (p.tiles_m + 1) / 2 : p.tiles_m;
-  p.group_m = opt.group_m ? opt.group_m : 8;
+  // Raster group height.  8 keeps a round's A rows and B columns in L2 when
+  // the operands do not fit there; when they do (A + B within half of L2),
+  // 4 measured faster on GB300 (bf16 4096^3: +2.5 %; 8192^3 and
+  // 4096 x 8192 x 4096 prefer 8 or more).
+  const int64_t in_bytes = (M * K + K * N) * (dtype == TGEMM_F32 ? 4 : 2);
+  p.group_m = opt.group_m ? opt.group_m : (in_bytes <= (int64_t(64) << 20) ? 4 : 8);
   p.group_m = std::max(1, std::min(p.group_m, sched_rows));
   p.k_blocks = static_cast<int>((K + kTileK * p.ksub - 1) / (kTileK * p.ksub));
   p.dp_tiles = static_cast<int>(int64_t(sched_rows) * p.tiles_n);
@@ -373,7 +432,8 @@ int make_plan(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const
     if (opt.max_ctas) ctas = std::min<int64_t>(ctas, opt.max_ctas);
   }
   p.ctas = static_cast<int>(ctas);
-  p.smem = p.pair ? tc2_smem_bytes(p.bn, p.store == 0, p.ksub) : tc_smem_bytes(p.bn);
+  p.smem = p.swap ? tc2_smem_bytes(p.tm, true, p.ksub)
+                  : (p.pair ? tc2_smem_bytes(p.bn, p.store == 0, p.ksub) : tc_smem_bytes(p.bn));
   return TGEMM_OK;
 }
 
@@ -385,13 +445,14 @@ CUtensorMapDataType tmap_type(int fmt_bytes, bool bf16) {
 // 2-D row-major tensor (cols x rows, pitch in bytes), box of box_cols x box_rows,
 // 128-byte swizzle, zero fill outside the tensor.
 int encode_2d(CUtensorMap* map, CUtensorMapDataType type, const void* base, int64_t cols, int64_t rows,
-              int64_t pitch_bytes, uint32_t box_cols, uint32_t box_rows) {
+              int64_t pitch_bytes, uint32_t box_cols, uint32_t box_rows,
+              CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(pitch_bytes)};
   const cuuint32_t box[2] = {box_cols, box_rows};
   const cuuint32_t estr[2] = {1, 1};
   CUresult r = g_encode(map, type, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
     t_last_error = "cuTensorMapEncodeTiled failed with CUresult " + std::to_string(static_cast<int>(r));
@@ -482,7 +543,9 @@ int run(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void*
   std::memset(&mB, 0, sizeof mB);
   std::memset(&mBt, 0, sizeof mBt);
   std::memset(&mC, 0, sizeof mC);
-  if (p.a_copy == 0 && (st = encode_2d(&mA, tmap_type(2, bf16), A, K, M, lda * 2, kTileK, kTileM)) != TGEMM_OK)
+  // the swapped pair kernel stages tm/2 rows of A per CTA
+  const uint32_t a_rows = p.swap ? static_cast<uint32_t>(p.tm / 2) : static_cast<uint32_t>(kTileM);
+  if (p.a_copy == 0 && (st = encode_2d(&mA, tmap_type(2, bf16), A, K, M, lda * 2, kTileK, a_rows)) != TGEMM_OK)
     return st;
   // clusters of two pairs load each 64-row B atom as two 32-row halves
   const uint32_t b_rows = p.cluster == 4 ? kTileK / 2 : kTileK;
@@ -490,8 +553,11 @@ int run(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void*
   // the pair kernel's last, partial B atom (bn/2 = 96 or 112 columns per CTA)
   const uint32_t b_tail = p.pair ? static_cast<uint32_t>((p.bn / 2) % 64) : 0u;
   if (b_tail && (st = encode_2d(&mBt, tmap_type(2, bf16), B, N, K, ldb * 2, b_tail, b_rows)) != TGEMM_OK) return st;
-  if (p.store == 0 && (st = encode_2d(&mC, tmap_type(eo, dtype == TGEMM_BF16), C, N, M, ldc * eo, 128 / eo, 32)) !=
-                          TGEMM_OK)
+  // C: 128-byte swizzled 32-row boxes; the swapped kernel writes unswizzled 32 x 32 blocks
+  if (p.store == 0 &&
+      (st = p.swap ? encode_2d(&mC, tmap_type(eo, dtype == TGEMM_BF16), C, N, M, ldc * eo, 32, 32,
+                               CU_TENSOR_MAP_SWIZZLE_NONE)
+                   : encode_2d(&mC, tmap_type(eo, dtype == TGEMM_BF16), C, N, M, ldc * eo, 128 / eo, 32)) != TGEMM_OK)
     return st;
   TcArgs a;
   a.M = static_cast<int>(M);
@@ -524,9 +590,15 @@ int run(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void*
   // kind::f16 instruction descriptor: D fp32 (bits 4-5 = 1), A/B format
   // (bits 7-9, 10-12), A K-major (bit 15 = 0), B N-major (bit 16 = 1),
   // N >> 3 (bits 17-22), M >> 4 (bits 24-28).
+  // The swapped kernel's MMA takes B as its A operand (N-major, bit 15 = 1),
+  // A as its B operand (K-major, bit 16 = 0), M = 256 and N = tm.
   const uint32_t mma_m = p.pair ? 2 * kTileM : kTileM;
-  a.idesc = (1u << 4) | (ab << 7) | (ab << 10) | (1u << 16) | (static_cast<uint32_t>(p.bn >> 3) << 17) |
-            ((mma_m >> 4) << 24);
+  if (p.swap)
+    a.idesc = (1u << 4) | (ab << 7) | (ab << 10) | (1u << 15) | (static_cast<uint32_t>(p.tm >> 3) << 17) |
+              ((mma_m >> 4) << 24);
+  else
+    a.idesc = (1u << 4) | (ab << 7) | (ab << 10) | (1u << 16) | (static_cast<uint32_t>(p.bn >> 3) << 17) |
+              ((mma_m >> 4) << 24);
   a.out_fmt = eo == 4 ? OUT_F32 : (dtype == TGEMM_BF16 ? OUT_BF16 : OUT_F16);
   a.a_copy = p.a_copy;
   a.b_copy = p.b_copy;
@@ -535,7 +607,9 @@ int run(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void*
   const int to_us = (o && o->wait_timeout_us) ? o->wait_timeout_us : 2000000;
   a.timeout_ns = static_cast<unsigned long long>(to_us) * 1000ull;
   a.status = dev->status;
-  if (p.pair)
+  if (p.swap)
+    e = launch_tc_pair_swap(p.tm, p.ksub, mA, mB, mC, a, p.ctas / 2, stream);
+  else if (p.pair)
     e = launch_tc_pair(p.bn, p.store == 0, p.ksub, p.cluster, mA, mB, mBt, mC, a, p.ctas / p.cluster, stream);
   else
     e = launch_tc(p.bn, p.kernel == TGEMM_KERNEL_TC_COPY, mA, mB, mC, a, p.ctas, stream);
@@ -592,7 +666,7 @@ int tgemm_plan(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, cons
     std::memset(out, 0, sizeof *out);
     if (st == TGEMM_OK && !p.noop && !p.zero) {
       out->kernel = p.kernel;
-      out->tile_m = p.kernel == TGEMM_KERNEL_SIMT ? tgemm::kSimtBM : (p.pair ? 2 : 1) * tgemm::kTileM;
+      out->tile_m = p.kernel == TGEMM_KERNEL_SIMT ? tgemm::kSimtBM : (p.swap ? p.tm : (p.pair ? 2 : 1) * tgemm::kTileM);
       out->tile_n = p.bn;
       out->tile_k = p.kernel == TGEMM_KERNEL_SIMT ? tgemm::kSimtBK : tgemm::kTileK * p.ksub;
       out->stages = p.stages;
@@ -606,6 +680,7 @@ int tgemm_plan(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, cons
       out->smem_bytes = p.smem;
       out->cta_group = p.pair ? 2 : 1;
       out->cluster_ctas = p.pair ? p.cluster : 1;
+      out->swap_ab = p.swap ? 1 : 0;
       out->dp_tiles = p.dp_tiles;
       out->sk_iters = p.sk_iters;
       out->workspace_bytes = p.workspace;

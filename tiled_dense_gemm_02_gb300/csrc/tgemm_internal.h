@@ -125,6 +125,11 @@ cudaError_t launch_tc(int bn, bool copy, const CUtensorMap& mapA, const CUtensor
 cudaError_t launch_tc_pair(int bn, bool staged, int ksub, int cluster, const CUtensorMap& mapA,
                            const CUtensorMap& mapB, const CUtensorMap& mapB_tail, const CUtensorMap& mapC,
                            const TcArgs& args, int clusters, cudaStream_t stream);
+// CTA pairs computing TM x 256 tiles of C as tiles of C^T = B^T A^T (the MMA's
+// M along C's columns, its N = tm along C's rows).  mapA's box is tm/2 rows of
+// A, mapB's 64 columns x 64 k, mapC's an unswizzled 32 x 32 block.
+cudaError_t launch_tc_pair_swap(int tm, int ksub, const CUtensorMap& mapA, const CUtensorMap& mapB,
+                                const CUtensorMap& mapC, const TcArgs& args, int pairs, cudaStream_t stream);
 // Number of clusters of `cluster` CTAs (2 or 4) of the pair kernel that can be
 // resident at once.
 cudaError_t tc_pair_capacity(int cluster, int* clusters);
