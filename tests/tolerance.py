@@ -1,5 +1,10 @@
 """Parity tolerance of the GEMM tests.
 
+Fused epilogue (out = act(alpha A.B + beta C + bias), oracle/epilogue.py): the
+product's bound scales by |alpha|, and the fp32 epilogue arithmetic (a multiply,
+a fused multiply-add, an add; ReLU is exact and 1-Lipschitz) adds at most
+2^-22 T with T = |alpha| S + |beta C| + |bias|, before the final rounding.
+
 fp16/bf16 inputs (tensor-core path), any output format:
     |C_gpu - C_ref| <= 2^-10 * S + ulp_out(C_ref) / 2
 fp32 inputs (SIMT path):
@@ -29,10 +34,18 @@ def bound(C_ref: np.ndarray, S: np.ndarray, in_fmt: str, out_fmt: str) -> np.nda
     return 2.0 ** -10 * S + 0.5 * ulp(C_ref, out_fmt)
 
 
-def check(C_gpu: np.ndarray, C_ref: np.ndarray, S: np.ndarray, in_fmt: str, out_fmt: str):
-    """Returns (ok, worst error/bound ratio, index of the worst element or None)."""
+def bound_epilogue(Z_ref: np.ndarray, S: np.ndarray, T: np.ndarray, alpha: float, in_fmt: str,
+                   out_fmt: str) -> np.ndarray:
+    core = 2.0 ** -20 * S if in_fmt == "f32" else 2.0 ** -10 * S
+    return abs(alpha) * core + 2.0 ** -22 * T + 0.5 * ulp(Z_ref, out_fmt)
+
+
+def check(C_gpu: np.ndarray, C_ref: np.ndarray, S: np.ndarray, in_fmt: str, out_fmt: str, tol=None):
+    """Returns (ok, worst error/bound ratio, index of the worst element or None);
+    `tol` replaces the product bound (e.g. bound_epilogue)."""
     C_gpu = np.asarray(C_gpu, dtype=np.float64)
-    tol = bound(C_ref, S, in_fmt, out_fmt)
+    if tol is None:
+        tol = bound(C_ref, S, in_fmt, out_fmt)
     finite_ref = np.isfinite(C_ref)
     bad_finite = finite_ref & ~np.isfinite(C_gpu)
     err = np.where(finite_ref, np.abs(C_gpu - C_ref), 0.0)
