@@ -40,6 +40,10 @@ sys.path.insert(0, ROOT)
 
 import workloads as wl  # noqa: E402
 
+# fused epilogues the benchmark can time: (alpha, beta, bias?, activation)
+EPILOGUES = {"none": None, "bias_relu": (1.0, 0.0, True, 1), "axpby": (0.5, 1.0, False, 0),
+             "all": (2.0, 1.0, True, 1)}
+
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "tc_gemm_2sm_swap_bf16_4096x4096x4096_f32out.md")
 # sources of the kernel the headline workload runs (the CTA-pair kernel with exchanged operands)
@@ -66,6 +70,8 @@ def parse_args():
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU work of the oracle sample")
+    p.add_argument("--epilogue", default="none", choices=sorted(EPILOGUES),
+                   help="fused epilogue C = act(alpha A.B + beta C + bias) timed with the product")
     return p.parse_args()
 
 
@@ -246,8 +252,18 @@ def run_ours(args, w: wl.Workload):
     st, plan = tg.plan(w.M, w.N, w.K, a.data_ptr(), w.K, b.data_ptr(), w.N, c.data_ptr(), w.N, w.dtype, None, sms)
     assert st == tg.OK, tg.status_string(st)
 
+    epi = EPILOGUES[args.epilogue]
+    bias = torch.linspace(-1.0, 1.0, w.N, dtype=torch.float32, device=dev) if epi and epi[2] else None
+    epi_struct = None if epi is None else tg.Epilogue(alpha=epi[0], beta=epi[1],
+                                                     bias=bias.data_ptr() if bias is not None else None,
+                                                     activation=epi[3])
+
     def call():
-        s = tg.gemm(w.M, w.N, w.K, a.data_ptr(), w.K, b.data_ptr(), w.N, c.data_ptr(), w.N, w.dtype, sptr)
+        if epi_struct is None:
+            s = tg.gemm(w.M, w.N, w.K, a.data_ptr(), w.K, b.data_ptr(), w.N, c.data_ptr(), w.N, w.dtype, sptr)
+        else:
+            s = tg.gemm_epilogue(w.M, w.N, w.K, a.data_ptr(), w.K, b.data_ptr(), w.N, c.data_ptr(), w.N, w.dtype,
+                                 epi_struct, None, 0, 0, sptr)
         if s != tg.OK:
             raise RuntimeError(tg.status_string(s))
 
@@ -316,11 +332,20 @@ def run_ours(args, w: wl.Workload):
     peaks, peak_src = load_peaks()
     peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     if w.dtype == wl.F32:
-        roofline = None   # the fp32 SIMT path is bound by the FP32 pipe; reported by the fp32 workloads' notes
+        # the SIMT kernel is bound by the FP32 pipe: SMs x 128 FMA/clk x 2 FLOP x
+        # the SM clock (the maximum nvidia-smi reports for this GPU)
+        achieved = w.flops / (ms_per_step / 1e3) / 1e12
+        clk = clocks.get("sm_max_mhz") or 2070.0
+        fp32_peak = sms * 128 * 2 * clk * 1e6 / 1e12
+        roofline = {"bound": "alu", "achieved": achieved, "peak": fp32_peak, "unit": "TFLOP/s",
+                    "frac": achieved / fp32_peak, "traffic": None,
+                    "peak_source": f"derived: {sms} SMs x 128 fp32 FMA/clk x 2 x {clk:.0f} MHz",
+                    "algorithmic_flops_per_launch": w.flops}
     else:
         achieved = w.flops / (ms_per_step / 1e3) / 1e12
         roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                    "frac": achieved / peak, "traffic": profiled_traffic(w.name),
+                    "frac": achieved / peak,
+                    "traffic": profiled_traffic(w.name) if epi is None else None,
                     "peak_source": f"{peak_src} bf16_tflops (burst; kernel timed alone)",
                     "algorithmic_flops_per_launch": w.flops,
                     "compulsory_bytes_per_launch": w.compulsory_bytes}
@@ -333,7 +358,7 @@ def run_ours(args, w: wl.Workload):
         "vs_baseline": None, "dtype": fin, "data": "synthetic",
         "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "in": fin, "out": fout, "accumulate": "f32",
                    "l2": "flushed before every timed step (256 MiB write)", "parallelism": f"replicas{world}",
-                   "kernel": plan.as_dict(), "sms": sms, "step_ms_min": min(step_ms),
+                   "kernel": plan.as_dict(), "sms": sms, "epilogue": args.epilogue, "step_ms_min": min(step_ms),
                    "step_ms_median": statistics.median(step_ms), "wall_s": wall},
         "roofline": roofline,
         "cpu_baseline": cpu,

@@ -127,7 +127,8 @@ typedef struct tgemm_options {
                            fix-up costs more than the idle tail), 1 off,
                            2 on whenever the tile count leaves a remainder */
   int multicast;        /* clusters of two CTA pairs (CTA-pair kernel): 0 auto
-                           (currently off: measured no faster), 1 off, 2 on.  The two pairs of a 4-CTA cluster take
+                           (currently off: measured no faster), 1 off, 2 on.
+                           The two pairs of a 4-CTA cluster take
                            vertically adjacent 256-row tiles of the same
                            columns and fetch each B tile once, multicast into
                            both (loads read this GPU's memory only).  Needs
@@ -258,6 +259,47 @@ TGEMM_API int tgemm_gemm_noalloc(int64_t M, int64_t N, int64_t K,
                const void* B, int64_t ldb,
                void* C, int64_t ldc,
                int dtype, const tgemm_options* opts, void* stream);
+
+/*
+ * Fused epilogue ("Tiling 策略与内存层次优化", section "Tiling 贯穿编译器栈",
+ * Fusion stage: element-wise post-processing such as a bias add and ReLU is
+ * applied to a GEMM tile's output in place, before it is written back).
+ *
+ *   C[i][j] = act(alpha * sum_k A[i][k] B[k][j] + beta * C_prior[i][j] + bias[j])
+ *
+ * computed in fp32 on the fp32 accumulator and rounded once (RNE) to the output
+ * format.  act is the identity or ReLU (x < 0 ? 0 : x, which keeps a NaN).
+ *  - alpha: scale of the product (1 for the plain product).
+ *  - beta: scale of C's prior contents, read in C's own format.  With beta == 0
+ *    C is not read at all, so it may hold anything, NaN included.
+ *  - bias: NULL, or a device pointer to N fp32 values (4-byte aligned, owned by
+ *    the caller, not written), one per column of C.
+ *  - activation: TGEMM_ACT_NONE or TGEMM_ACT_RELU.
+ * With K = 0 the product is the empty sum 0 and C = act(beta C_prior + bias).
+ * Every kernel path applies it; `workspace`/`workspace_bytes` (NULL/0 allowed)
+ * serve the stream-K split as in tgemm_gemm_ws.
+ */
+enum tgemm_activation { TGEMM_ACT_NONE = 0, TGEMM_ACT_RELU = 1 };
+
+typedef struct tgemm_epilogue {
+  float alpha;
+  float beta;
+  const float* bias;
+  int activation;   /* enum tgemm_activation */
+  int reserved[3];  /* zero */
+} tgemm_epilogue;
+
+/* tgemm_gemm_ws with a fused epilogue (epi may be NULL: the plain product).
+ * Returns TGEMM_ERR_INVALID_VALUE for an unknown activation, nonzero reserved
+ * fields or a misaligned bias pointer, and TGEMM_ERR_ALIAS if the bias lies
+ * inside C.  Asynchronous on `stream`, like tgemm_gemm_ex. */
+TGEMM_API int tgemm_gemm_epilogue(int64_t M, int64_t N, int64_t K,
+               const void* A, int64_t lda,
+               const void* B, int64_t ldb,
+               void* C, int64_t ldc,
+               int dtype, const tgemm_epilogue* epi,
+               const tgemm_options* opts,
+               void* workspace, size_t workspace_bytes, void* stream);
 
 /* Waits for `stream`, then returns and clears the device-side status word
  * that bounded in-kernel waits set when they give up (TGEMM_OK or

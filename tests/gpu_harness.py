@@ -45,11 +45,15 @@ class Result:
 
 def run_gpu(A_bits: np.ndarray, B_bits: np.ndarray, M: int, N: int, K: int, dtype: int,
             ldc: int | None = None, a_off: int = 0, b_off: int = 0, c_off: int = 0,
-            options=None, dev=None, check_status: bool = True, workspace=None) -> Result:
+            options=None, dev=None, check_status: bool = True, workspace=None,
+            epilogue=None, c_prior: np.ndarray | None = None, bias: np.ndarray | None = None) -> Result:
     """C = A . B on the GPU through the C ABI; A/B given as [rows, ld] bit arrays.
 
     workspace: None (tgemm_gemm_ex), True (a fresh zeroed workspace of
-    tgemm_workspace_size bytes, tgemm_gemm_ws) or a torch uint8 tensor to reuse."""
+    tgemm_workspace_size bytes, tgemm_gemm_ws) or a torch uint8 tensor to reuse.
+    epilogue: a dict of tgemm_epilogue fields (alpha, beta, activation) for
+    tgemm_gemm_epilogue; c_prior (M x N storage bits of C's output format) is
+    C's content before the call, bias (N float32 values) goes to the device."""
     lib = tg()
     dev = dev or torch.device("cuda:0")
     fout = wl.OUT_FORMAT[dtype]
@@ -60,13 +64,33 @@ def run_gpu(A_bits: np.ndarray, B_bits: np.ndarray, M: int, N: int, K: int, dtyp
     b_buf, b_ptr = upload(B_bits, b_off, dev)
     c_elems = GUARD + M * ldc + GUARD
     c_init = np.full(c_elems, CANARY[fout], dtype=NP_BITS[fout])
+    if c_prior is not None:
+        window = c_init[GUARD:GUARD + M * ldc].reshape(M, ldc)
+        window[:, :N] = c_prior
     c_buf, c_base = upload(c_init, c_off, dev)
     c_ptr = c_base + GUARD * eo
     stream = torch.cuda.current_stream(dev).cuda_stream
     st_plan, plan = lib.plan(M, N, K, a_ptr, lda, b_ptr, ldb, c_ptr, ldc, dtype, options,
                              sm_count=torch.cuda.get_device_properties(dev).multi_processor_count)
     ws_tensor = None
-    if workspace is None:
+    bias_buf = None
+    if epilogue is not None:
+        ep = dict(epilogue)
+        if bias is not None:
+            bias_buf = torch.from_numpy(np.ascontiguousarray(bias, dtype=np.float32)).to(dev)
+            ep["bias"] = bias_buf.data_ptr()
+        ws_ptr, ws_n = 0, 0
+        if workspace is not None:
+            st_ws, nbytes = lib.workspace_size(M, N, K, a_ptr, lda, b_ptr, ldb, c_ptr, ldc, dtype, options)
+            assert st_ws == lib.OK, lib.status_string(st_ws)
+            ws_tensor = torch.zeros(max(nbytes, 1), dtype=torch.uint8, device=dev)
+            ws_ptr, ws_n = ws_tensor.data_ptr(), ws_tensor.numel()
+            st_plan, plan = lib.plan(M, N, K, a_ptr, lda, b_ptr, ldb, c_ptr, ldc, dtype, options,
+                                     sm_count=torch.cuda.get_device_properties(dev).multi_processor_count,
+                                     workspace_bytes=ws_n)
+        status = lib.gemm_epilogue(M, N, K, a_ptr, lda, b_ptr, ldb, c_ptr, ldc, dtype, ep, options, ws_ptr, ws_n,
+                                   stream)
+    elif workspace is None:
         status = lib.gemm_ex(M, N, K, a_ptr, lda, b_ptr, ldb, c_ptr, ldc, dtype, options, stream)
     else:
         st_ws, nbytes = lib.workspace_size(M, N, K, a_ptr, lda, b_ptr, ldb, c_ptr, ldc, dtype, options)

@@ -30,7 +30,8 @@ def declared_functions():
 def test_header_declares_the_abi():
     names = declared_functions()
     assert names == sorted(["tgemm_gemm", "tgemm_gemm_ex", "tgemm_gemm_ws", "tgemm_workspace_size", "tgemm_plan",
-                            "tgemm_gemm_noalloc", "tgemm_device_status", "tgemm_status_string", "tgemm_version"])
+                            "tgemm_gemm_noalloc", "tgemm_gemm_epilogue", "tgemm_device_status",
+                            "tgemm_status_string", "tgemm_version"])
 
 
 def test_library_exports_every_declared_symbol(tg):
@@ -57,6 +58,37 @@ def header_struct_fields(name):
             m = re.fullmatch(r"\s*(\w+)\s*(?:\[(\d+)\])?\s*", part)
             fields.append((m.group(1), int(m.group(2) or 1)))
     return fields
+
+
+def test_epilogue_struct_matches_header(tg):
+    text = open(HEADER).read()
+    body = re.search(r"typedef struct tgemm_epilogue \{(.*?)\} tgemm_epilogue;", text, re.S).group(1)
+    body = re.sub(r"/\*.*?\*/", "", body, flags=re.S)
+    decls = [d.strip() for d in body.split(";") if d.strip()]
+    assert decls == ["float alpha", "float beta", "const float* bias", "int activation", "int reserved[3]"]
+    assert [f for f, _ in tg.Epilogue._fields_] == ["alpha", "beta", "bias", "activation", "reserved"]
+    assert ctypes.sizeof(tg.Epilogue) == 32
+    assert tg.Epilogue.bias.offset == 8 and tg.Epilogue.activation.offset == 16
+
+
+def test_epilogue_validation_returns_before_the_device(tg):
+    """Bad epilogue arguments are refused on the host (these calls would
+    otherwise need a GPU)."""
+    lib = tg
+    C = 0x30000000
+    def call(**e):
+        ep = {"alpha": 1.0, "beta": 0.0, "bias": None, "activation": 0}
+        ep.update(e)
+        return lib.gemm_epilogue(64, 64, 64, 0x10000000, 64, 0x20000000, 64, C, 64, 2, ep)
+    assert call(activation=2) == lib.ERR_INVALID_VALUE
+    assert call(activation=-1) == lib.ERR_INVALID_VALUE
+    assert call(bias=0x40000002) == lib.ERR_INVALID_VALUE          # not 4-byte aligned
+    assert call(bias=C + 100) == lib.ERR_ALIAS                      # inside C
+    e = lib.Epilogue(alpha=1.0, beta=0.0, bias=None, activation=0)
+    e.reserved[1] = 7
+    assert lib.gemm_epilogue(64, 64, 64, 0x10000000, 64, 0x20000000, 64, C, 64, 2, e) == lib.ERR_INVALID_VALUE
+    # empty products return before looking at anything else
+    assert lib.gemm_epilogue(0, 64, 64, 0x10000000, 64, 0x20000000, 64, C, 64, 2, {"activation": 1}) == lib.OK
 
 
 def test_struct_layouts_match_header(tg):

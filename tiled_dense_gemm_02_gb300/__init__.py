@@ -23,9 +23,12 @@ OK, ERR_INVALID_VALUE, ERR_UNSUPPORTED_DTYPE, ERR_MISALIGNED, ERR_ALIAS = 0, 1, 
 ERR_UNSUPPORTED_DEVICE, ERR_LAUNCH, ERR_DEVICE_TIMEOUT, ERR_TOO_LARGE = 5, 6, 7, 8
 # enum tgemm_kernel
 KERNEL_AUTO, KERNEL_TC_TMA, KERNEL_TC_COPY, KERNEL_SIMT = 0, 1, 2, 3
+# enum tgemm_activation
+ACT_NONE, ACT_RELU = 0, 1
 
 EXPORTS = ("tgemm_gemm", "tgemm_gemm_ex", "tgemm_gemm_ws", "tgemm_workspace_size", "tgemm_plan",
-           "tgemm_gemm_noalloc", "tgemm_device_status", "tgemm_status_string", "tgemm_version")
+           "tgemm_gemm_noalloc", "tgemm_gemm_epilogue", "tgemm_device_status", "tgemm_status_string",
+           "tgemm_version")
 # bytes of the scratch array built into the library (TGEMM_NOALLOC_SCRATCH_BYTES)
 NOALLOC_SCRATCH_BYTES = 20 * 1024 * 1024 + 4096
 
@@ -37,6 +40,12 @@ class Options(ctypes.Structure):
                 ("inject_fault", ctypes.c_int), ("cta_group", ctypes.c_int), ("tile_k", ctypes.c_int),
                 ("stream_k", ctypes.c_int), ("multicast", ctypes.c_int),
                 ("swap_ab", ctypes.c_int), ("tile_m", ctypes.c_int), ("reserved", ctypes.c_int * 3)]
+
+
+class Epilogue(ctypes.Structure):
+    """struct tgemm_epilogue"""
+    _fields_ = [("alpha", ctypes.c_float), ("beta", ctypes.c_float), ("bias", ctypes.c_void_p),
+                ("activation", ctypes.c_int), ("reserved", ctypes.c_int * 3)]
 
 
 class PlanInfo(ctypes.Structure):
@@ -80,6 +89,9 @@ def _load():
     lib.tgemm_plan.restype = ip
     lib.tgemm_gemm_noalloc.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, ip, ctypes.POINTER(Options), vp]
     lib.tgemm_gemm_noalloc.restype = ip
+    lib.tgemm_gemm_epilogue.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, ip, ctypes.POINTER(Epilogue),
+                                        ctypes.POINTER(Options), vp, ctypes.c_size_t, vp]
+    lib.tgemm_gemm_epilogue.restype = ip
     lib.tgemm_device_status.argtypes = [vp]
     lib.tgemm_device_status.restype = ip
     lib.tgemm_status_string.argtypes = [ip]
@@ -128,6 +140,26 @@ def gemm_noalloc(M, N, K, A, lda, B, ldb, C, ldc, dtype, options=None, stream=0)
     """tgemm_gemm_noalloc: the stream-K variant with the library's built-in
     scratch array, for callers that cannot allocate device memory."""
     return _lib.tgemm_gemm_noalloc(M, N, K, A, lda, B, ldb, C, ldc, dtype, _opts(options), stream)
+
+
+def _epi(epilogue):
+    if epilogue is None:
+        return None
+    if isinstance(epilogue, Epilogue):
+        return ctypes.byref(epilogue)
+    e = Epilogue(alpha=1.0, beta=0.0, bias=None, activation=ACT_NONE)
+    for k, v in dict(epilogue).items():
+        setattr(e, k, v)
+    return ctypes.byref(e)
+
+
+def gemm_epilogue(M, N, K, A, lda, B, ldb, C, ldc, dtype, epilogue=None, options=None, workspace=0,
+                  workspace_bytes=0, stream=0) -> int:
+    """tgemm_gemm_epilogue: C = act(alpha A.B + beta C + bias) with an Epilogue
+    struct or a dict of its fields (alpha, beta, bias as a device pointer int,
+    activation); workspace as in gemm_ws."""
+    return _lib.tgemm_gemm_epilogue(M, N, K, A, lda, B, ldb, C, ldc, dtype, _epi(epilogue), _opts(options),
+                                    workspace, workspace_bytes, stream)
 
 
 def workspace_size(M, N, K, A, lda, B, ldb, C, ldc, dtype, options=None):

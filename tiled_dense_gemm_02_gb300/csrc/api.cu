@@ -501,15 +501,45 @@ uint32_t next_epoch() {
   return v;
 }
 
+// The fused epilogue of a call, validated (no device access).  `on` stays 0
+// for the plain product.
+int make_epilogue(const tgemm_epilogue* in, int64_t M, int64_t N, const void* C, int64_t ldc, int dtype,
+                  Epilogue& e) {
+  e = Epilogue{0, 0, 1.0f, 0.0f, nullptr};
+  if (!in) return TGEMM_OK;
+  if (in->activation < TGEMM_ACT_NONE || in->activation > TGEMM_ACT_RELU) return TGEMM_ERR_INVALID_VALUE;
+  for (int r : in->reserved)
+    if (r != 0) return TGEMM_ERR_INVALID_VALUE;
+  if (in->bias) {
+    const uint64_t b0 = reinterpret_cast<uint64_t>(in->bias);
+    if (b0 % 4) return TGEMM_ERR_INVALID_VALUE;
+    if (M > 0 && N > 0) {
+      const uint64_t c0 = reinterpret_cast<uint64_t>(C);
+      const uint64_t c1 = c0 + static_cast<uint64_t>((M - 1) * ldc + N) * out_bytes(dtype);
+      if (ranges_overlap(c0, c1, b0, b0 + static_cast<uint64_t>(N) * 4)) return TGEMM_ERR_ALIAS;
+    }
+  }
+  e.alpha = in->alpha;
+  e.beta = in->beta;
+  e.bias = in->bias;
+  e.act = in->activation;
+  e.on = !(in->alpha == 1.0f && in->beta == 0.0f && !in->bias && in->activation == TGEMM_ACT_NONE);
+  return TGEMM_OK;
+}
+
 int run(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb, void* C,
-        int64_t ldc, int dtype, const tgemm_options* o, void* workspace, int64_t workspace_bytes,
-        cudaStream_t stream) {
+        int64_t ldc, int dtype, const tgemm_options* o, const tgemm_epilogue* epi_in, void* workspace,
+        int64_t workspace_bytes, cudaStream_t stream) {
   // validation that needs no device first, so bad arguments never touch CUDA
   Plan p;
   if (workspace_bytes < 0 || (workspace_bytes > 0 && (!workspace || reinterpret_cast<uint64_t>(workspace) % 256)))
     return TGEMM_ERR_INVALID_VALUE;
   int st = make_plan(M, N, K, A, lda, B, ldb, C, ldc, dtype, o, 1, 1, 1, workspace_bytes, p);
   if (st != TGEMM_OK || p.noop) return st;
+  Epilogue ep;
+  st = make_epilogue(epi_in, M, N, C, ldc, dtype, ep);
+  if (st != TGEMM_OK) return st;
+  const int out_fmt = out_bytes(dtype) == 4 ? OUT_F32 : (dtype == TGEMM_BF16 ? OUT_BF16 : OUT_F16);
   DeviceInfo* dev = nullptr;
   st = device_info(&dev);
   if (st != TGEMM_OK) return st;
@@ -518,7 +548,8 @@ int run(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void*
   if (st != TGEMM_OK) return st;
   cudaError_t e;
   if (p.zero) {
-    e = launch_zero_fill(C, M, N, ldc, out_bytes(dtype), stream);
+    e = ep.on ? launch_epilogue_fill(C, M, N, ldc, out_fmt, ep, stream)
+              : launch_zero_fill(C, M, N, ldc, out_bytes(dtype), stream);
     return e == cudaSuccess ? TGEMM_OK : cuda_fail(e, "zero-fill launch");
   }
   if (p.kernel == TGEMM_KERNEL_SIMT) {
@@ -533,6 +564,7 @@ int run(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void*
     a.C = static_cast<float*>(C);
     a.ldc = ldc;
     a.vec = p.a_copy == 16 ? 1 : 0;
+    a.epi = ep;
     e = launch_simt(a, stream);
     return e == cudaSuccess ? TGEMM_OK : cuda_fail(e, "SIMT kernel launch");
   }
@@ -599,7 +631,8 @@ int run(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void*
   else
     a.idesc = (1u << 4) | (ab << 7) | (ab << 10) | (1u << 16) | (static_cast<uint32_t>(p.bn >> 3) << 17) |
               ((mma_m >> 4) << 24);
-  a.out_fmt = eo == 4 ? OUT_F32 : (dtype == TGEMM_BF16 ? OUT_BF16 : OUT_F16);
+  a.out_fmt = out_fmt;
+  a.epi = ep;
   a.a_copy = p.a_copy;
   a.b_copy = p.b_copy;
   a.store_granule = p.store;
@@ -623,20 +656,29 @@ extern "C" {
 
 int tgemm_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb, void* C,
                int64_t ldc, int dtype, void* stream) {
-  return tgemm::run(M, N, K, A, lda, B, ldb, C, ldc, dtype, nullptr, nullptr, 0, static_cast<cudaStream_t>(stream));
+  return tgemm::run(M, N, K, A, lda, B, ldb, C, ldc, dtype, nullptr, nullptr, nullptr, 0, static_cast<cudaStream_t>(stream));
 }
 
 int tgemm_gemm_ex(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb, void* C,
                   int64_t ldc, int dtype, const tgemm_options* opts, void* stream) {
-  return tgemm::run(M, N, K, A, lda, B, ldb, C, ldc, dtype, opts, nullptr, 0, static_cast<cudaStream_t>(stream));
+  return tgemm::run(M, N, K, A, lda, B, ldb, C, ldc, dtype, opts, nullptr, nullptr, 0, static_cast<cudaStream_t>(stream));
 }
 
 int tgemm_gemm_ws(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb, void* C,
                   int64_t ldc, int dtype, const tgemm_options* opts, void* workspace, size_t workspace_bytes,
                   void* stream) {
   if (workspace_bytes > static_cast<size_t>(INT64_MAX)) return TGEMM_ERR_INVALID_VALUE;
-  return tgemm::run(M, N, K, A, lda, B, ldb, C, ldc, dtype, opts, workspace, static_cast<int64_t>(workspace_bytes),
+  return tgemm::run(M, N, K, A, lda, B, ldb, C, ldc, dtype, opts, nullptr, workspace,
+                    static_cast<int64_t>(workspace_bytes),
                     static_cast<cudaStream_t>(stream));
+}
+
+int tgemm_gemm_epilogue(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb,
+                        void* C, int64_t ldc, int dtype, const tgemm_epilogue* epi, const tgemm_options* opts,
+                        void* workspace, size_t workspace_bytes, void* stream) {
+  if (workspace_bytes > static_cast<size_t>(INT64_MAX)) return TGEMM_ERR_INVALID_VALUE;
+  return tgemm::run(M, N, K, A, lda, B, ldb, C, ldc, dtype, opts, epi, workspace,
+                    static_cast<int64_t>(workspace_bytes), static_cast<cudaStream_t>(stream));
 }
 
 int tgemm_workspace_size(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb,
@@ -788,6 +830,7 @@ extern "C" int tgemm_gemm_noalloc(int64_t M, int64_t N, int64_t K, const void* A
   void* scratch = nullptr;
   st = noalloc_scratch(&scratch);
   if (st != TGEMM_OK) return st;
-  return tgemm::run(M, N, K, A, lda, B, ldb, C, ldc, dtype, &o, scratch, static_cast<int64_t>(kNoAllocScratchBytes),
+  return tgemm::run(M, N, K, A, lda, B, ldb, C, ldc, dtype, &o, nullptr, scratch,
+                    static_cast<int64_t>(kNoAllocScratchBytes),
                     static_cast<cudaStream_t>(stream));
 }

@@ -68,6 +68,14 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 }
 
 // --------------------------------------------------------- bulk-tensor copies
+// Bring a tile of a tensor into L2 ahead of its use (no shared memory, no
+// completion to wait for; coordinates outside the tensor fetch nothing).
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int32_t x, int32_t y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y)
+               : "memory");
+}
+
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }

@@ -111,7 +111,9 @@ __device__ __forceinline__ void fma_frag(const Frag& f, float2 (&acc)[8][4]) {
       acc[i][j] = __ffma2_rn(f.a[i], make_float2(f.b[2 * j], f.b[2 * j + 1]), acc[i][j]);
 }
 
-template <bool VEC>
+// EPI: the fused epilogue is compiled in (a separate instantiation, so the
+// plain product keeps its register allocation)
+template <bool VEC, bool EPI>
 __global__ void __launch_bounds__(THREADS, 2) simt_sgemm_kernel(const SimtArgs p) {
   __shared__ __align__(16) float As[2][BK][APAD];
   __shared__ __align__(16) float Bs[2][BK][BN];
@@ -174,7 +176,12 @@ __global__ void __launch_bounds__(THREADS, 2) simt_sgemm_kernel(const SimtArgs p
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int gn = n0 + n_in + h * 32;
-      const float v[4] = {acc[i][2 * h].x, acc[i][2 * h].y, acc[i][2 * h + 1].x, acc[i][2 * h + 1].y};
+      float v[4] = {acc[i][2 * h].x, acc[i][2 * h].y, acc[i][2 * h + 1].x, acc[i][2 * h + 1].y};
+      if (EPI) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (gn + j < p.N) v[j] = epi_apply(p.epi, v[j], gn + j, [&] { return crow[gn + j]; });
+      }
       if (VEC && gn + 3 < p.N) {
         *reinterpret_cast<float4*>(crow + gn) = make_float4(v[0], v[1], v[2], v[3]);
       } else {
@@ -190,10 +197,13 @@ __global__ void __launch_bounds__(THREADS, 2) simt_sgemm_kernel(const SimtArgs p
 
 cudaError_t launch_simt(const SimtArgs& args, cudaStream_t stream) {
   dim3 grid((args.N + BN - 1) / BN, (args.M + BM - 1) / BM);
+  const bool epi = args.epi.on != 0;
   if (args.vec)
-    simt_sgemm_kernel<true><<<grid, THREADS, 0, stream>>>(args);
+    epi ? simt_sgemm_kernel<true, true><<<grid, THREADS, 0, stream>>>(args)
+        : simt_sgemm_kernel<true, false><<<grid, THREADS, 0, stream>>>(args);
   else
-    simt_sgemm_kernel<false><<<grid, THREADS, 0, stream>>>(args);
+    epi ? simt_sgemm_kernel<false, true><<<grid, THREADS, 0, stream>>>(args)
+        : simt_sgemm_kernel<false, false><<<grid, THREADS, 0, stream>>>(args);
   return cudaGetLastError();
 }
 

@@ -78,6 +78,41 @@ __device__ __forceinline__ uint32_t pack_pair(float lo, float hi, int out_fmt) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// ------------------------------------------------------- fused epilogue
+// The prior C[row][col] in the output format (read before this kernel writes it:
+// each element is read and then written by the same thread).
+__device__ __forceinline__ float load_prior(const TcArgs& a, int row, int col) {
+  const int64_t idx = static_cast<int64_t>(row) * a.ldc + col;
+  if (a.out_fmt == OUT_F32) return static_cast<const float*>(a.C)[idx];
+  const uint16_t h = static_cast<const uint16_t*>(a.C)[idx];
+  if (a.out_fmt == OUT_BF16) return __uint_as_float(static_cast<uint32_t>(h) << 16);
+  return __half2float(__ushort_as_half(h));
+}
+
+// The epilogue on one row's 32 fp32 values v[i] = C[row][col0 + i].  The
+// prior C elements and biases are all loaded before any is used, so the loads
+// overlap; elements outside C are left alone (their stores are clipped).
+__device__ __forceinline__ void epi_row(float (&v)[32], int row, int col0, const TcArgs& a) {
+  float prior[32], bias[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const bool in = row < a.M && col0 + i < a.N;
+    prior[i] = (in && a.epi.beta != 0.0f) ? load_prior(a, row, col0 + i) : 0.0f;
+    bias[i] = (in && a.epi.bias) ? a.epi.bias[col0 + i] : 0.0f;
+  }
+#pragma unroll
+  for (int i = 0; i < 32; ++i)
+    if (row < a.M && col0 + i < a.N) v[i] = epi_combine(a.epi, v[i], prior[i], bias[i]);
+}
+__device__ __forceinline__ void epi_row(uint32_t (&v)[32], int row, int col0, const TcArgs& a) {
+  float f[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(v[i]);
+  epi_row(f, row, col0, a);
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(f[i]);
+}
+
 // Store a packed 128-byte row segment w[0..31] to global with the widest
 // access `granule` (16/8/4/2 bytes) allows; only the first `valid_bytes`
 // bytes are written (element size `es`).  Fully unrolled so w stays in
@@ -381,6 +416,10 @@ __device__ __forceinline__ bool epilogue_finish(uint32_t tbase, int row0, int co
         if (nsub == 2)
           for (int k = k0; k < k1; ++k, ++slot) add_partial(hi, ring + slot * 4096, lane);
         if (k1 == n_add) {
+          if (args.epi.on) {
+            epi_row(lo, row0 + lane, col_base + col_in_tile, args);
+            if (nsub == 2) epi_row(hi, row0 + lane, col_base + col_in_tile + 32, args);
+          }
           uint32_t w[32];
           pack_chunk(lo, hi, half, out_fmt, w);
           store_chunk(w, row0, col_base + col_in_tile, half, tma_store, args, mapC, stage_base, sbuf, lane);
@@ -412,14 +451,20 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tbase, int row0, int col_
     const int col_in_tile = c * cols_per_chunk;
     const bool half = col_in_tile + cols_per_chunk > BN;
     uint32_t w[32];
+    const int row = row0 + lane;
     if (out_fmt == OUT_F32) {
       ptx::tmem_ld_32x32b_x32(tbase + col_in_tile, w);
       ptx::tmem_wait_ld();
+      if (args.epi.on) epi_row(w, row, col_base + col_in_tile, args);
     } else {
       uint32_t lo[32], hi[32];
       ptx::tmem_ld_32x32b_x32(tbase + col_in_tile, lo);
       if (!half) ptx::tmem_ld_32x32b_x32(tbase + col_in_tile + 32, hi);
       ptx::tmem_wait_ld();
+      if (args.epi.on) {
+        epi_row(lo, row, col_base + col_in_tile, args);
+        if (!half) epi_row(hi, row, col_base + col_in_tile + 32, args);
+      }
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
         w[i] = pack_pair(__uint_as_float(lo[2 * i]), __uint_as_float(lo[2 * i + 1]), out_fmt);

@@ -354,6 +354,26 @@ __global__ void zero_fill_kernel(uint8_t* C, int64_t rows, int64_t row_bytes, in
   }
 }
 
+// K = 0 with a fused epilogue: C = act(alpha * 0 + beta * C + bias), element
+// by element (the empty sum is 0).
+__global__ void epilogue_fill_kernel(void* C, int64_t rows, int64_t cols, int64_t ldc, int out_fmt, Epilogue e) {
+  const int64_t total = rows * cols;
+  for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < total; i += int64_t(gridDim.x) * blockDim.x) {
+    const int64_t r = i / cols, c = i % cols;
+    const int64_t idx = r * ldc + c;
+    if (out_fmt == OUT_F32) {
+      float* p = static_cast<float*>(C) + idx;
+      *p = epi_apply(e, 0.0f, static_cast<int>(c), [&] { return *p; });
+    } else if (out_fmt == OUT_BF16) {
+      __nv_bfloat16* p = static_cast<__nv_bfloat16*>(C) + idx;
+      *p = __float2bfloat16_rn(epi_apply(e, 0.0f, static_cast<int>(c), [&] { return __bfloat162float(*p); }));
+    } else {
+      __half* p = static_cast<__half*>(C) + idx;
+      *p = __float2half_rn(epi_apply(e, 0.0f, static_cast<int>(c), [&] { return __half2float(*p); }));
+    }
+  }
+}
+
 template <int BN, bool kCopy>
 cudaError_t launch_one(const CUtensorMap& mA, const CUtensorMap& mB, const CUtensorMap& mC, const TcArgs& args,
                        int ctas, cudaStream_t stream) {
@@ -391,6 +411,14 @@ cudaError_t launch_tc(int bn, bool copy, const CUtensorMap& mA, const CUtensorMa
     default: return cudaErrorInvalidValue;
   }
 #undef TGEMM_LAUNCH_BN
+}
+
+cudaError_t launch_epilogue_fill(void* C, int64_t rows, int64_t cols, int64_t ldc, int out_fmt, const Epilogue& e,
+                                 cudaStream_t stream) {
+  int blocks = static_cast<int>(std::min<int64_t>((rows * cols + 255) / 256, 4096));
+  if (blocks < 1) blocks = 1;
+  epilogue_fill_kernel<<<blocks, 256, 0, stream>>>(C, rows, cols, ldc, out_fmt, e);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_zero_fill(void* C, int64_t rows, int64_t cols, int64_t ldc, int elem_bytes, cudaStream_t stream) {

@@ -32,11 +32,25 @@ namespace tgemm {
 namespace {
 
 // One 32 x 32 block of C (rows m0.., columns n0..) from the lanes' values:
-// lane l holds column n0 + l, v[i] is row m0 + i.
-__device__ __forceinline__ void store_block_t(const uint32_t (&v)[32], int m0, int n0, bool tma_store,
+// lane l holds column n0 + l, v[i] is row m0 + i (the fused epilogue, when on,
+// is applied in place first).
+template <bool EPI>
+__device__ __forceinline__ void store_block_t(uint32_t (&v)[32], int m0, int n0, bool tma_store,
                                               const TcArgs& args, const CUtensorMap* mapC, uint8_t* stage_base,
-                                              int& sbuf, int lane) {
+                                              int& sbuf, int lane, float bias_v) {
   const int out_fmt = args.out_fmt;
+  if constexpr (EPI) {
+    // lane = column (its bias is bias_v); the 32 prior rows are loaded (each
+    // row coalesced across the warp) before any is used
+    const int n = n0 + lane;
+    const bool col_in = n < args.N;
+    float prior[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      prior[i] = (col_in && m0 + i < args.M && args.epi.beta != 0.0f) ? load_prior(args, m0 + i, n) : 0.0f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(epi_combine(args.epi, __uint_as_float(v[i]), prior[i], bias_v));
+  }
   if (tma_store) {
     uint8_t* buf = stage_base + sbuf * 4096;
     if (lane == 0) ptx::bulk_wait_group_read<1>();
@@ -84,7 +98,9 @@ __device__ __forceinline__ void store_block_t(const uint32_t (&v)[32], int m0, i
   }
 }
 
-template <int TM, int KSUB>
+// EPI: the fused epilogue is compiled in (the plain product keeps its own
+// instantiation and registers)
+template <int TM, int KSUB, bool EPI>
 __global__ void __launch_bounds__(32 * (2 + kEpiWarps), 1)
     tc_gemm_2sm_swap_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
                             const __grid_constant__ CUtensorMap mapC, const TcArgs args) {
@@ -253,11 +269,20 @@ __global__ void __launch_bounds__(32 * (2 + kEpiWarps), 1)
     for (int t = pair; t < args.num_tiles; t += npairs) {
       int mb, nb;
       tile_coords(t, args, mb, nb);
+      // this warp's TMEM lanes are 32 columns of C
+      const int n0 = nb * TN + static_cast<int>(rank) * (TN / 2) + q * 32;
+      float bias_v = 0.0f;
+      if constexpr (EPI) {
+        // while the tile's MMAs run: the prior C this warp will read goes to
+        // L2, and the lane's column bias into a register
+        if (args.epi.beta != 0.0f && tma_store && lane == 0 && n0 < args.N)
+          for (int c = 0; c < TM / 32 && mb * TM + c * 32 < args.M; ++c)
+            ptx::tma_prefetch_l2_2d(&mapC, n0, mb * TM + c * 32);
+        if (args.epi.bias && n0 + lane < args.N) bias_v = args.epi.bias[n0 + lane];
+      }
       if (!warp_wait(ptx::smem_u32(&acc_full[acc]), acc_phase, ctl, SITE_EPI_ACC_FULL)) break;
       ptx::tc_fence_after_sync();
-      // this warp's TMEM lanes are 32 columns of C
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * ACC);
-      const int n0 = nb * TN + static_cast<int>(rank) * (TN / 2) + q * 32;
       if (n0 < args.N) {
 #pragma unroll 1
         for (int c = 0; c < TM / 32; ++c) {
@@ -266,7 +291,7 @@ __global__ void __launch_bounds__(32 * (2 + kEpiWarps), 1)
           uint32_t v[32];
           ptx::tmem_ld_32x32b_x32(tbase + c * 32, v);
           ptx::tmem_wait_ld();
-          store_block_t(v, m0, n0, tma_store, args, &mapC, stage_base, sbuf, lane);
+          store_block_t<EPI>(v, m0, n0, tma_store, args, &mapC, stage_base, sbuf, lane, bias_v);
         }
       }
       ptx::tc_fence_before_sync();
@@ -288,11 +313,11 @@ __global__ void __launch_bounds__(32 * (2 + kEpiWarps), 1)
   }
 }
 
-template <int TM, int KSUB>
+template <int TM, int KSUB, bool EPI>
 cudaError_t launch_swap(const CUtensorMap& mA, const CUtensorMap& mB, const CUtensorMap& mC, const TcArgs& args,
                         int pairs, cudaStream_t stream) {
   constexpr int smem = tc2_smem_bytes(TM, true, KSUB);
-  auto kernel = tc_gemm_2sm_swap_kernel<TM, KSUB>;
+  auto kernel = tc_gemm_2sm_swap_kernel<TM, KSUB, EPI>;
   static std::atomic<uint64_t> done_mask{0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -322,10 +347,14 @@ cudaError_t launch_swap(const CUtensorMap& mA, const CUtensorMap& mB, const CUte
 
 cudaError_t launch_tc_pair_swap(int tm, int ksub, const CUtensorMap& mA, const CUtensorMap& mB,
                                 const CUtensorMap& mC, const TcArgs& args, int pairs, cudaStream_t stream) {
+  const bool epi = args.epi.on != 0;
 #define TGEMM_SWAP_TM(TMV)                                                                            \
   case TMV:                                                                                           \
-    return ksub == 2 ? launch_swap<TMV, 2>(mA, mB, mC, args, pairs, stream)                           \
-                     : launch_swap<TMV, 1>(mA, mB, mC, args, pairs, stream);
+    if (epi)                                                                                          \
+      return ksub == 2 ? launch_swap<TMV, 2, true>(mA, mB, mC, args, pairs, stream)                   \
+                       : launch_swap<TMV, 1, true>(mA, mB, mC, args, pairs, stream);                  \
+    return ksub == 2 ? launch_swap<TMV, 2, false>(mA, mB, mC, args, pairs, stream)                    \
+                     : launch_swap<TMV, 1, false>(mA, mB, mC, args, pairs, stream);
   switch (tm) {
     TGEMM_SWAP_TM(128)
     TGEMM_SWAP_TM(192)

@@ -24,6 +24,39 @@ enum WaitSite : uint32_t {
 };
 constexpr uint32_t kTimeoutFlag = 0x7E000000u;
 
+// Fused epilogue, applied in fp32 to each accumulator value v of C[row][col]:
+//   z = alpha * v (+ beta * C_prior[row][col] when beta != 0) (+ bias[col]),
+//   ReLU when act == 1.  on == 0: the plain product (v as it is).
+struct Epilogue {
+  int on;
+  int act;              // 0 none, 1 ReLU
+  float alpha, beta;
+  const float* bias;    // N fp32 column biases, or null
+};
+
+#ifdef __CUDACC__
+// The fused epilogue on one value: alpha v (+ beta prior) (+ bias[col]), then
+// ReLU, which keeps a NaN.  `prior()` loads the prior C element; it is called
+// only when beta != 0, so C is never read otherwise.
+template <class Prior>
+__device__ __forceinline__ float epi_apply(const Epilogue& e, float v, int col, Prior prior) {
+  float z = e.alpha * v;
+  if (e.beta != 0.0f) z = fmaf(e.beta, prior(), z);
+  if (e.bias) z += e.bias[col];
+  if (e.act == 1) z = z < 0.0f ? 0.0f : z;
+  return z;
+}
+// The same with the prior C element and the bias already loaded (bias_v is 0
+// when there is no bias vector; prior is used only when beta != 0).
+__device__ __forceinline__ float epi_combine(const Epilogue& e, float v, float prior, float bias_v) {
+  float z = e.alpha * v;
+  if (e.beta != 0.0f) z = fmaf(e.beta, prior, z);
+  z += bias_v;
+  if (e.act == 1) z = z < 0.0f ? 0.0f : z;
+  return z;
+}
+#endif
+
 struct TcArgs {
   int M, N, K;
   int tiles_m, tiles_n, num_tiles, k_blocks;
@@ -50,6 +83,7 @@ struct TcArgs {
   float* sk_partials;   // per worker: 2 CTAs x 4 warps x (32 rows x BN) fp32
   unsigned int* sk_flags;  // per worker, CTA and epilogue warp
   unsigned int sk_epoch;   // value a flag holds once this call's partial is written
+  Epilogue epi;
 };
 
 // Workspace of the stream-K tail for `workers` CTA pairs and tile width bn.
@@ -69,6 +103,7 @@ struct SimtArgs {
   float* C;
   int64_t ldc;
   int vec;              // 1 when A/B/C rows allow 16-byte vector accesses
+  Epilogue epi;
 };
 
 // Tile shapes of the tensor-core kernel: 128 x BN output tiles, K stages of
@@ -135,6 +170,9 @@ cudaError_t launch_tc_pair_swap(int tm, int ksub, const CUtensorMap& mapA, const
 cudaError_t tc_pair_capacity(int cluster, int* clusters);
 cudaError_t launch_simt(const SimtArgs& args, cudaStream_t stream);
 cudaError_t launch_zero_fill(void* C, int64_t rows, int64_t cols, int64_t ldc, int elem_bytes, cudaStream_t stream);
+// K = 0 with a fused epilogue (out_fmt: OutFmt)
+cudaError_t launch_epilogue_fill(void* C, int64_t rows, int64_t cols, int64_t ldc, int out_fmt, const Epilogue& e,
+                                 cudaStream_t stream);
 
 // SIMT tile shape.
 constexpr int kSimtBM = 128;
