@@ -301,6 +301,41 @@ TGEMM_API int tgemm_gemm_epilogue(int64_t M, int64_t N, int64_t K,
                const tgemm_options* opts,
                void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * Strided batch of independent products ("矩阵乘法中的平铺", closing advice:
+ * where tensor cores are available, use a batched interface).
+ *
+ *   for b < batch:  C_b = act(alpha A_b . B_b + beta C_b + bias)
+ *   A_b = A + b * stride_a, B_b = B + b * stride_b, C_b = C + b * stride_c
+ *
+ * Strides are in elements of each operand's format.  stride_a or stride_b may
+ * be 0 (every product uses the same matrix); the C windows must not overlap
+ * (stride_c >= (M - 1) * ldc + N, else TGEMM_ERR_ALIAS), and no C window may
+ * overlap any A or B matrix.  epi (may be NULL) applies to every product, with
+ * one bias vector for all.  When every A_b and B_b starts on a 16-byte boundary
+ * and the operands suit bulk-tensor copies, the whole batch runs in one launch
+ * of the swapped-operand pair kernel, whose tile list spans all matrices.
+ * Otherwise each product is launched on its own.  batch == 0: nothing is done.
+ * Other arguments and errors: as tgemm_gemm_ex.
+ */
+TGEMM_API int tgemm_gemm_batched(int64_t batch, int64_t M, int64_t N, int64_t K,
+               const void* A, int64_t lda, int64_t stride_a,
+               const void* B, int64_t ldb, int64_t stride_b,
+               void* C, int64_t ldc, int64_t stride_c,
+               int dtype, const tgemm_epilogue* epi,
+               const tgemm_options* opts, void* stream);
+
+/* The plan of tgemm_gemm_batched without touching the GPU (pair counts
+ * modelled from sm_count as tgemm_plan does).  *launches: kernel launches the
+ * call makes (1 for an in-kernel batch, batch for one launch per product, 0
+ * when nothing is done).  out describes one launch. */
+TGEMM_API int tgemm_plan_batched(int64_t batch, int64_t M, int64_t N, int64_t K,
+               const void* A, int64_t lda, int64_t stride_a,
+               const void* B, int64_t ldb, int64_t stride_b,
+               const void* C, int64_t ldc, int64_t stride_c,
+               int dtype, const tgemm_options* opts, int sm_count,
+               tgemm_plan_info* out, int* launches);
+
 /* Waits for `stream`, then returns and clears the device-side status word
  * that bounded in-kernel waits set when they give up (TGEMM_OK or
  * TGEMM_ERR_DEVICE_TIMEOUT).  A CUDA error while synchronising returns

@@ -30,8 +30,8 @@ def declared_functions():
 def test_header_declares_the_abi():
     names = declared_functions()
     assert names == sorted(["tgemm_gemm", "tgemm_gemm_ex", "tgemm_gemm_ws", "tgemm_workspace_size", "tgemm_plan",
-                            "tgemm_gemm_noalloc", "tgemm_gemm_epilogue", "tgemm_device_status",
-                            "tgemm_status_string", "tgemm_version"])
+                            "tgemm_gemm_noalloc", "tgemm_gemm_epilogue", "tgemm_gemm_batched",
+                            "tgemm_plan_batched", "tgemm_device_status", "tgemm_status_string", "tgemm_version"])
 
 
 def test_library_exports_every_declared_symbol(tg):
@@ -218,6 +218,37 @@ def test_swapped_pair_planning(tg):
                 {"swap_ab": 2, "tile_n": 224}, {"swap_ab": 2, "tile_m": 160}, {"tile_m": 224}, {"swap_ab": 3}):
         assert plan(tg, 4096, 4096, 4096, dtype=3, **bad)[0] == tg.ERR_INVALID_VALUE, bad
     assert plan(tg, 1000, 1500, 4096, dtype=2, swap_ab=2)[0] == tg.ERR_INVALID_VALUE  # per-thread copies
+
+
+def test_batched_planning(tg):
+    """A strided batch: one launch of the swapped kernel over all matrices when
+    every matrix starts on a 16-byte boundary, else one launch per product."""
+    A, B, C = 0x10000000, 0x40000000, 0x80000000
+    M = N = K = 512
+    st, p, n = tg.plan_batched(64, M, N, K, A, K, M * K, B, N, K * N, C, N, M * N, 2, sm_count=152)
+    assert st == tg.OK and n == 1 and p.swap_ab == 1 and p.tile_n == 256
+    assert p.dp_tiles == 64 * p.tiles_m * p.tiles_n and p.ctas == 152
+    # B shared by every product (stride 0)
+    st, p, n = tg.plan_batched(8, M, N, K, A, K, M * K, B, N, 0, C, N, M * N, 3, sm_count=152)
+    assert st == tg.OK and n == 1
+    # a stride that breaks 16-byte alignment of the later matrices: one launch each
+    st, p, n = tg.plan_batched(8, M, N, K, A, K, M * K + 4, B, N, K * N, C, N, M * N, 2, sm_count=152)
+    assert st == tg.OK and n == 8
+    # fp32 runs the SIMT kernel once per product; batch 1 and 0
+    assert tg.plan_batched(5, 64, 64, 64, A, 64, 4096, B, 64, 4096, C, 64, 4096, 0, sm_count=152)[2] == 5
+    assert tg.plan_batched(1, M, N, K, A, K, 0, B, N, 0, C, N, 0, 2, sm_count=152)[2] == 1
+    assert tg.plan_batched(0, M, N, K, A, K, 0, B, N, 0, C, N, 0, 2, sm_count=152)[2] == 0
+    # options that exclude the swapped kernel loop over the products
+    assert tg.plan_batched(4, M, N, K, A, K, M * K, B, N, K * N, C, N, M * N, 2, {"swap_ab": 1},
+                           sm_count=152)[2] == 4
+    # refused: overlapping C windows, C overlapping A's batch, negative values
+    assert tg.plan_batched(4, M, N, K, A, K, M * K, B, N, K * N, C, N, M * N - 1, 2)[0] == tg.ERR_ALIAS
+    assert tg.plan_batched(4, M, N, K, A, K, M * K, B, N, K * N, A + 3 * M * K * 2, N, M * N, 2)[0] == tg.ERR_ALIAS
+    assert tg.plan_batched(-1, M, N, K, A, K, 0, B, N, 0, C, N, 0, 2)[0] == tg.ERR_INVALID_VALUE
+    assert tg.plan_batched(2, M, N, K, A, K, -1, B, N, 0, C, N, M * N, 2)[0] == tg.ERR_INVALID_VALUE
+    # the call validates on the host as well (no GPU here)
+    assert tg.gemm_batched(4, M, N, K, A, K, M * K, B, N, K * N, C, N, 5, 2) == tg.ERR_ALIAS
+    assert tg.gemm_batched(0, M, N, K, A, K, 0, B, N, 0, C, N, 0, 2) == tg.OK
 
 
 def test_two_pair_cluster_planning(tg):

@@ -27,8 +27,8 @@ KERNEL_AUTO, KERNEL_TC_TMA, KERNEL_TC_COPY, KERNEL_SIMT = 0, 1, 2, 3
 ACT_NONE, ACT_RELU = 0, 1
 
 EXPORTS = ("tgemm_gemm", "tgemm_gemm_ex", "tgemm_gemm_ws", "tgemm_workspace_size", "tgemm_plan",
-           "tgemm_gemm_noalloc", "tgemm_gemm_epilogue", "tgemm_device_status", "tgemm_status_string",
-           "tgemm_version")
+           "tgemm_gemm_noalloc", "tgemm_gemm_epilogue", "tgemm_gemm_batched", "tgemm_plan_batched",
+           "tgemm_device_status", "tgemm_status_string", "tgemm_version")
 # bytes of the scratch array built into the library (TGEMM_NOALLOC_SCRATCH_BYTES)
 NOALLOC_SCRATCH_BYTES = 20 * 1024 * 1024 + 4096
 
@@ -92,6 +92,13 @@ def _load():
     lib.tgemm_gemm_epilogue.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, ip, ctypes.POINTER(Epilogue),
                                         ctypes.POINTER(Options), vp, ctypes.c_size_t, vp]
     lib.tgemm_gemm_epilogue.restype = ip
+    lib.tgemm_gemm_batched.argtypes = [i64, i64, i64, i64, vp, i64, i64, vp, i64, i64, vp, i64, i64, ip,
+                                       ctypes.POINTER(Epilogue), ctypes.POINTER(Options), vp]
+    lib.tgemm_gemm_batched.restype = ip
+    lib.tgemm_plan_batched.argtypes = [i64, i64, i64, i64, vp, i64, i64, vp, i64, i64, vp, i64, i64, ip,
+                                       ctypes.POINTER(Options), ip, ctypes.POINTER(PlanInfo),
+                                       ctypes.POINTER(ctypes.c_int)]
+    lib.tgemm_plan_batched.restype = ip
     lib.tgemm_device_status.argtypes = [vp]
     lib.tgemm_device_status.restype = ip
     lib.tgemm_status_string.argtypes = [ip]
@@ -160,6 +167,23 @@ def gemm_epilogue(M, N, K, A, lda, B, ldb, C, ldc, dtype, epilogue=None, options
     activation); workspace as in gemm_ws."""
     return _lib.tgemm_gemm_epilogue(M, N, K, A, lda, B, ldb, C, ldc, dtype, _epi(epilogue), _opts(options),
                                     workspace, workspace_bytes, stream)
+
+
+def gemm_batched(batch, M, N, K, A, lda, stride_a, B, ldb, stride_b, C, ldc, stride_c, dtype, epilogue=None,
+                 options=None, stream=0) -> int:
+    """tgemm_gemm_batched: `batch` products with element strides between matrices."""
+    return _lib.tgemm_gemm_batched(batch, M, N, K, A, lda, stride_a, B, ldb, stride_b, C, ldc, stride_c, dtype,
+                                   _epi(epilogue), _opts(options), stream)
+
+
+def plan_batched(batch, M, N, K, A, lda, stride_a, B, ldb, stride_b, C, ldc, stride_c, dtype, options=None,
+                 sm_count=148):
+    """tgemm_plan_batched: (status, PlanInfo of one launch, kernel launches of the call)."""
+    info = PlanInfo()
+    n = ctypes.c_int(0)
+    st = _lib.tgemm_plan_batched(batch, M, N, K, A, lda, stride_a, B, ldb, stride_b, C, ldc, stride_c, dtype,
+                                 _opts(options), sm_count, ctypes.byref(info), ctypes.byref(n))
+    return st, info, n.value
 
 
 def workspace_size(M, N, K, A, lda, B, ldb, C, ldc, dtype, options=None):

@@ -119,6 +119,8 @@ struct Plan {
   int k_blocks = 0;               // k-stages per tile
   int dp_tiles = 0, sk_iters = 0;  // stream-K split (sk_iters == 0: whole tiles only)
   int64_t workspace = 0;          // bytes of workspace the stream-K split uses
+  int64_t batch = 1;              // matrices computed by one launch (strided batch, swapped kernel)
+  bool batch_loop = false;        // a batch the kernels cannot index: one launch per matrix
 };
 
 // Relative throughput of one SM per output column for each tile width,
@@ -219,11 +221,11 @@ double swap_rate(int tm) {
 
 // Tile height of the swapped pair kernel minimising rounds x tm / rate: each
 // round runs `pairs` tm x 256 tiles.
-int pick_swap_tile_m(int64_t M, int64_t N, int pairs, double* cost) {
+int pick_swap_tile_m(int64_t M, int64_t N, int pairs, double* cost, int64_t batch = 1) {
   int best = 256;
   double best_t = 1e300;
   for (int tm : {256, 224, 192, 128}) {
-    const int64_t tiles = ((M + tm - 1) / tm) * ((N + 255) / 256);
+    const int64_t tiles = ((M + tm - 1) / tm) * ((N + 255) / 256) * batch;
     const double t = static_cast<double>((tiles + pairs - 1) / pairs) * tm / swap_rate(tm);
     if (t < best_t * 0.999) {
       best_t = t;
@@ -236,7 +238,7 @@ int pick_swap_tile_m(int64_t M, int64_t N, int pairs, double* cost) {
 
 int make_plan(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb,
               const void* C, int64_t ldc, int dtype, const tgemm_options* o, int sms, int pair_cap, int quad_cap,
-              int64_t workspace_bytes, Plan& p) {
+              int64_t workspace_bytes, Plan& p, int64_t batch = 1) {
   if (dtype < TGEMM_F32 || dtype > TGEMM_F16_F32OUT) return TGEMM_ERR_UNSUPPORTED_DTYPE;
   if (M < 0 || N < 0 || K < 0) return TGEMM_ERR_INVALID_VALUE;
   if (M >= (int64_t(1) << 31) || N >= (int64_t(1) << 31) || K >= (int64_t(1) << 31)) return TGEMM_ERR_TOO_LARGE;
@@ -376,6 +378,23 @@ int make_plan(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const
   }
   if (opt.multicast == 2 && p.cluster != 4) return TGEMM_ERR_INVALID_VALUE;
   if (opt.swap_ab == 2 && !p.swap) return TGEMM_ERR_INVALID_VALUE;
+  // A strided batch runs in one launch of the swapped kernel, whose tile list
+  // spans all matrices; when that kernel cannot serve it, each matrix is
+  // launched on its own with the plan of a single product.
+  if (batch > 1) {
+    const bool in_kernel = pair_ok && opt.cta_group != 1 && opt.stream_k != 2 && opt.multicast != 2 &&
+                           opt.swap_ab != 1 && (opt.tile_n == 0 || opt.tile_n == 256);
+    if (in_kernel) {
+      p.pair = true;
+      p.swap = true;
+      p.cluster = 2;
+      p.tm = opt.tile_m ? opt.tile_m : pick_swap_tile_m(M, N, pair_cap, nullptr, batch);
+      bn2 = 256;
+      p.batch = batch;
+    } else {
+      p.batch_loop = true;
+    }
+  }
   if (opt.tile_k == 128 && !p.pair) return TGEMM_ERR_INVALID_VALUE;
   // 128-deep stages halve the MMA completion signals per FLOP (measured faster
   // for long K); short K keeps 64 so the last stage wastes little.
@@ -387,7 +406,7 @@ int make_plan(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const
   const int tm = p.swap ? p.tm : (p.pair ? 2 * kTileM : kTileM);
   p.tiles_m = static_cast<int>((M + tm - 1) / tm);
   p.tiles_n = static_cast<int>((N + p.bn - 1) / p.bn);
-  const int64_t tiles = int64_t(p.tiles_m) * p.tiles_n;
+  const int64_t tiles = int64_t(p.tiles_m) * p.tiles_n * p.batch;
   if (tiles >= (int64_t(1) << 31)) return TGEMM_ERR_TOO_LARGE;
   // rows of scheduling units: 512-row super-tiles for clusters of two pairs
   const int sched_rows = p.cluster == 4 ? (p.tiles_m + 1) / 2 : p.tiles_m;
@@ -399,7 +418,7 @@ int make_plan(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const
   p.group_m = opt.group_m ? opt.group_m : (in_bytes <= (int64_t(64) << 20) ? 4 : 8);
   p.group_m = std::max(1, std::min(p.group_m, sched_rows));
   p.k_blocks = static_cast<int>((K + kTileK * p.ksub - 1) / (kTileK * p.ksub));
-  p.dp_tiles = static_cast<int>(int64_t(sched_rows) * p.tiles_n);
+  p.dp_tiles = static_cast<int>(int64_t(sched_rows) * p.tiles_n * p.batch);
   int64_t ctas;
   if (p.pair && p.cluster == 4) {
     int64_t cap = quad_cap;
@@ -456,6 +475,27 @@ int encode_2d(CUtensorMap* map, CUtensorMapDataType type, const void* base, int6
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
     t_last_error = "cuTensorMapEncodeTiled failed with CUresult " + std::to_string(static_cast<int>(r));
+    return TGEMM_ERR_LAUNCH;
+  }
+  return TGEMM_OK;
+}
+
+// 3-D row-major tensor: `depth` matrices of cols x rows, `depth_bytes` apart
+// (a depth of 1 for one matrix or for a batch stride of 0), box box_cols x
+// box_rows x 1.
+int encode_3d(CUtensorMap* map, CUtensorMapDataType type, const void* base, int64_t cols, int64_t rows,
+              int64_t depth, int64_t pitch_bytes, int64_t depth_bytes, uint32_t box_cols, uint32_t box_rows,
+              CUtensorMapSwizzle swizzle) {
+  if (depth <= 1) depth_bytes = (rows * pitch_bytes + 15) / 16 * 16;  // unused, but must be valid
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows),
+                              static_cast<cuuint64_t>(depth < 1 ? 1 : depth)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(pitch_bytes), static_cast<cuuint64_t>(depth_bytes)};
+  const cuuint32_t box[3] = {box_cols, box_rows, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(map, type, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    t_last_error = "cuTensorMapEncodeTiled (3-D) failed with CUresult " + std::to_string(static_cast<int>(r));
     return TGEMM_ERR_LAUNCH;
   }
   return TGEMM_OK;
@@ -527,14 +567,28 @@ int make_epilogue(const tgemm_epilogue* in, int64_t M, int64_t N, const void* C,
   return TGEMM_OK;
 }
 
+// A strided batch: `count` products, operands of matrix b at element offsets
+// b * stride_a, b * stride_b, b * stride_c.  Validated by batch_validate.
+struct Batch {
+  int64_t count = 1, stride_a = 0, stride_b = 0, stride_c = 0;
+};
+
+// Bulk-tensor copies need every matrix of a batch to start on a 16-byte
+// boundary: the swapped kernel's 3-D maps can take the batch only then.
+bool batch_tma_ok(const Batch& bt, int dtype) {
+  const int ei = in_bytes(dtype);
+  return (bt.stride_a * ei) % 16 == 0 && (bt.stride_b * ei) % 16 == 0;
+}
+
 int run(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb, void* C,
         int64_t ldc, int dtype, const tgemm_options* o, const tgemm_epilogue* epi_in, void* workspace,
-        int64_t workspace_bytes, cudaStream_t stream) {
+        int64_t workspace_bytes, cudaStream_t stream, const Batch& bt = Batch()) {
   // validation that needs no device first, so bad arguments never touch CUDA
   Plan p;
   if (workspace_bytes < 0 || (workspace_bytes > 0 && (!workspace || reinterpret_cast<uint64_t>(workspace) % 256)))
     return TGEMM_ERR_INVALID_VALUE;
-  int st = make_plan(M, N, K, A, lda, B, ldb, C, ldc, dtype, o, 1, 1, 1, workspace_bytes, p);
+  const int64_t in_batch = (bt.count > 1 && batch_tma_ok(bt, dtype)) ? bt.count : 1;
+  int st = make_plan(M, N, K, A, lda, B, ldb, C, ldc, dtype, o, 1, 1, 1, workspace_bytes, p, in_batch);
   if (st != TGEMM_OK || p.noop) return st;
   Epilogue ep;
   st = make_epilogue(epi_in, M, N, C, ldc, dtype, ep);
@@ -544,8 +598,19 @@ int run(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void*
   st = device_info(&dev);
   if (st != TGEMM_OK) return st;
   st = make_plan(M, N, K, A, lda, B, ldb, C, ldc, dtype, o, dev->sm_count, pair_capacity(dev), quad_capacity(dev),
-                 workspace_bytes, p);
+                 workspace_bytes, p, in_batch);
   if (st != TGEMM_OK) return st;
+  if (bt.count > 1 && p.batch == 1) {
+    // no kernel indexes this batch: one launch per matrix, each a single product
+    const int ei = in_bytes(dtype), eo = out_bytes(dtype);
+    for (int64_t b = 0; b < bt.count; ++b) {
+      st = run(M, N, K, static_cast<const char*>(A) + b * bt.stride_a * ei, lda,
+               static_cast<const char*>(B) + b * bt.stride_b * ei, ldb, static_cast<char*>(C) + b * bt.stride_c * eo,
+               ldc, dtype, o, epi_in, workspace, workspace_bytes, stream);
+      if (st != TGEMM_OK) return st;
+    }
+    return TGEMM_OK;
+  }
   cudaError_t e;
   if (p.zero) {
     e = ep.on ? launch_epilogue_fill(C, M, N, ldc, out_fmt, ep, stream)
@@ -575,21 +640,36 @@ int run(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void*
   std::memset(&mB, 0, sizeof mB);
   std::memset(&mBt, 0, sizeof mBt);
   std::memset(&mC, 0, sizeof mC);
-  // the swapped pair kernel stages tm/2 rows of A per CTA
-  const uint32_t a_rows = p.swap ? static_cast<uint32_t>(p.tm / 2) : static_cast<uint32_t>(kTileM);
-  if (p.a_copy == 0 && (st = encode_2d(&mA, tmap_type(2, bf16), A, K, M, lda * 2, kTileK, a_rows)) != TGEMM_OK)
+  // The swapped pair kernel: 3-D maps (the batch is the third dimension), tm/2
+  // rows of A per CTA, C in unswizzled 32 x 32 blocks (bulk stores only when
+  // every matrix of C starts on a 16-byte boundary).
+  if (p.swap && p.batch > 1 && p.store == 0 && (bt.stride_c * eo) % 16 != 0) p.store = eo;
+  if (p.swap) {
+    const int64_t nb = p.batch;
+    if ((st = encode_3d(&mA, tmap_type(2, bf16), A, K, M, bt.stride_a ? nb : 1, lda * 2, bt.stride_a * 2, kTileK,
+                        static_cast<uint32_t>(p.tm / 2), CU_TENSOR_MAP_SWIZZLE_128B)) != TGEMM_OK)
+      return st;
+    if ((st = encode_3d(&mB, tmap_type(2, bf16), B, N, K, bt.stride_b ? nb : 1, ldb * 2, bt.stride_b * 2, 64, kTileK,
+                        CU_TENSOR_MAP_SWIZZLE_128B)) != TGEMM_OK)
+      return st;
+    if (p.store == 0 && (st = encode_3d(&mC, tmap_type(eo, dtype == TGEMM_BF16), C, N, M, nb, ldc * eo,
+                                        bt.stride_c * eo, 32, 32, CU_TENSOR_MAP_SWIZZLE_NONE)) != TGEMM_OK)
+      return st;
+  }
+  if (!p.swap && p.a_copy == 0 &&
+      (st = encode_2d(&mA, tmap_type(2, bf16), A, K, M, lda * 2, kTileK, kTileM)) != TGEMM_OK)
     return st;
   // clusters of two pairs load each 64-row B atom as two 32-row halves
   const uint32_t b_rows = p.cluster == 4 ? kTileK / 2 : kTileK;
-  if (p.b_copy == 0 && (st = encode_2d(&mB, tmap_type(2, bf16), B, N, K, ldb * 2, 64, b_rows)) != TGEMM_OK) return st;
+  if (!p.swap && p.b_copy == 0 &&
+      (st = encode_2d(&mB, tmap_type(2, bf16), B, N, K, ldb * 2, 64, b_rows)) != TGEMM_OK)
+    return st;
   // the pair kernel's last, partial B atom (bn/2 = 96 or 112 columns per CTA)
-  const uint32_t b_tail = p.pair ? static_cast<uint32_t>((p.bn / 2) % 64) : 0u;
+  const uint32_t b_tail = (p.pair && !p.swap) ? static_cast<uint32_t>((p.bn / 2) % 64) : 0u;
   if (b_tail && (st = encode_2d(&mBt, tmap_type(2, bf16), B, N, K, ldb * 2, b_tail, b_rows)) != TGEMM_OK) return st;
   // C: 128-byte swizzled 32-row boxes; the swapped kernel writes unswizzled 32 x 32 blocks
-  if (p.store == 0 &&
-      (st = p.swap ? encode_2d(&mC, tmap_type(eo, dtype == TGEMM_BF16), C, N, M, ldc * eo, 32, 32,
-                               CU_TENSOR_MAP_SWIZZLE_NONE)
-                   : encode_2d(&mC, tmap_type(eo, dtype == TGEMM_BF16), C, N, M, ldc * eo, 128 / eo, 32)) != TGEMM_OK)
+  if (!p.swap && p.store == 0 &&
+      (st = encode_2d(&mC, tmap_type(eo, dtype == TGEMM_BF16), C, N, M, ldc * eo, 128 / eo, 32)) != TGEMM_OK)
     return st;
   TcArgs a;
   a.M = static_cast<int>(M);
@@ -597,7 +677,11 @@ int run(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void*
   a.K = static_cast<int>(K);
   a.tiles_m = p.cluster == 4 ? (p.tiles_m + 1) / 2 : p.tiles_m;  // scheduling rows
   a.tiles_n = p.tiles_n;
-  a.num_tiles = a.tiles_m * p.tiles_n;
+  a.tiles_per = a.tiles_m * p.tiles_n;
+  a.num_tiles = static_cast<int>(a.tiles_per * p.batch);
+  a.stride_a = p.batch > 1 ? bt.stride_a : 0;
+  a.stride_b = p.batch > 1 ? bt.stride_b : 0;
+  a.stride_c = p.batch > 1 ? bt.stride_c : 0;
   a.k_blocks = p.k_blocks;
   a.dp_tiles = p.dp_tiles;
   a.sk_iters = p.sk_iters;
@@ -679,6 +763,89 @@ int tgemm_gemm_epilogue(int64_t M, int64_t N, int64_t K, const void* A, int64_t 
   if (workspace_bytes > static_cast<size_t>(INT64_MAX)) return TGEMM_ERR_INVALID_VALUE;
   return tgemm::run(M, N, K, A, lda, B, ldb, C, ldc, dtype, opts, epi, workspace,
                     static_cast<int64_t>(workspace_bytes), static_cast<cudaStream_t>(stream));
+}
+
+namespace tgemm {
+namespace {
+// Host checks of a strided batch: sizes, strides, disjoint C windows, and no
+// overlap between the whole of C and the whole of A or B.
+int batch_validate(int64_t batch, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, int64_t sa,
+                   const void* B, int64_t ldb, int64_t sb, const void* C, int64_t ldc, int64_t sc, int dtype) {
+  if (batch < 0 || sa < 0 || sb < 0 || sc < 0) return TGEMM_ERR_INVALID_VALUE;
+  if (dtype < TGEMM_F32 || dtype > TGEMM_F16_F32OUT) return TGEMM_ERR_UNSUPPORTED_DTYPE;
+  if (batch <= 1 || M <= 0 || N <= 0) return TGEMM_OK;  // the single-product checks cover the rest
+  if (batch >= (int64_t(1) << 31) || sa >= (int64_t(1) << 40) || sb >= (int64_t(1) << 40) ||
+      sc >= (int64_t(1) << 40))
+    return TGEMM_ERR_TOO_LARGE;
+  const int64_t c_span = (M - 1) * ldc + N;  // elements of one matrix's window of C
+  if (sc < c_span) return TGEMM_ERR_ALIAS;    // the products would write the same elements
+  if (K > 0 && A && B && C) {
+    const int ei = in_bytes(dtype), eo = out_bytes(dtype);
+    const uint64_t c0 = reinterpret_cast<uint64_t>(C), c1 = c0 + static_cast<uint64_t>((batch - 1) * sc + c_span) * eo;
+    const uint64_t a0 = reinterpret_cast<uint64_t>(A);
+    const uint64_t a1 = a0 + static_cast<uint64_t>((batch - 1) * sa + (M - 1) * lda + K) * ei;
+    const uint64_t b0 = reinterpret_cast<uint64_t>(B);
+    const uint64_t b1 = b0 + static_cast<uint64_t>((batch - 1) * sb + (K - 1) * ldb + N) * ei;
+    if (ranges_overlap(c0, c1, a0, a1) || ranges_overlap(c0, c1, b0, b1)) return TGEMM_ERR_ALIAS;
+  }
+  return TGEMM_OK;
+}
+}  // namespace
+}  // namespace tgemm
+
+int tgemm_gemm_batched(int64_t batch, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, int64_t stride_a,
+                       const void* B, int64_t ldb, int64_t stride_b, void* C, int64_t ldc, int64_t stride_c, int dtype,
+                       const tgemm_epilogue* epi, const tgemm_options* opts, void* stream) {
+  int st = tgemm::batch_validate(batch, M, N, K, A, lda, stride_a, B, ldb, stride_b, C, ldc, stride_c, dtype);
+  if (st != TGEMM_OK || batch == 0) return st;
+  tgemm::Batch bt;
+  bt.count = batch;
+  bt.stride_a = stride_a;
+  bt.stride_b = stride_b;
+  bt.stride_c = stride_c;
+  return tgemm::run(M, N, K, A, lda, B, ldb, C, ldc, dtype, opts, epi, nullptr, 0, static_cast<cudaStream_t>(stream),
+                    bt);
+}
+
+int tgemm_plan_batched(int64_t batch, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, int64_t stride_a,
+                       const void* B, int64_t ldb, int64_t stride_b, const void* C, int64_t ldc, int64_t stride_c,
+                       int dtype, const tgemm_options* opts, int sm_count, tgemm_plan_info* out, int* launches) {
+  if (out) std::memset(out, 0, sizeof *out);
+  if (launches) *launches = 0;
+  int st = tgemm::batch_validate(batch, M, N, K, A, lda, stride_a, B, ldb, stride_b, C, ldc, stride_c, dtype);
+  if (st != TGEMM_OK || batch == 0) return st;
+  tgemm::Batch bt;
+  bt.count = batch;
+  bt.stride_a = stride_a;
+  bt.stride_b = stride_b;
+  const int64_t in_batch = (batch > 1 && tgemm::batch_tma_ok(bt, dtype)) ? batch : 1;
+  const int sms = sm_count < 1 ? 1 : sm_count;
+  tgemm::Plan p;
+  st = tgemm::make_plan(M, N, K, A, lda, B, ldb, C, ldc, dtype, opts, sms, sms / 2, sms / 4, 0, p, in_batch);
+  if (st != TGEMM_OK) return st;
+  if (launches) *launches = p.noop ? 0 : (batch > 1 && p.batch == 1 ? static_cast<int>(batch) : 1);
+  if (out) {
+    st = tgemm_plan(M, N, K, A, lda, B, ldb, C, ldc, dtype, opts, 0, sm_count, out);
+    if (st == TGEMM_OK && p.batch > 1) {
+      out->tile_m = p.tm;
+      out->tile_n = p.bn;
+      out->stages = p.stages;
+      out->tiles_m = p.tiles_m;
+      out->tiles_n = p.tiles_n;
+      out->ctas = p.ctas;
+      out->dp_tiles = p.dp_tiles;
+      out->cta_group = 2;
+      out->cluster_ctas = 2;
+      out->swap_ab = 1;
+      out->smem_bytes = p.smem;
+      out->group_m = p.group_m;
+      out->tile_k = tgemm::kTileK * p.ksub;
+      // C windows that do not all start on a 16-byte boundary are stored per thread
+      if (out->store_bytes == 0 && (stride_c * tgemm::out_bytes(dtype)) % 16 != 0)
+        out->store_bytes = tgemm::out_bytes(dtype);
+    }
+  }
+  return st;
 }
 
 int tgemm_workspace_size(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb,

@@ -81,8 +81,8 @@ __device__ __forceinline__ uint32_t pack_pair(float lo, float hi, int out_fmt) {
 // ------------------------------------------------------- fused epilogue
 // The prior C[row][col] in the output format (read before this kernel writes it:
 // each element is read and then written by the same thread).
-__device__ __forceinline__ float load_prior(const TcArgs& a, int row, int col) {
-  const int64_t idx = static_cast<int64_t>(row) * a.ldc + col;
+__device__ __forceinline__ float load_prior(const TcArgs& a, int row, int col, int64_t c_off = 0) {
+  const int64_t idx = c_off + static_cast<int64_t>(row) * a.ldc + col;
   if (a.out_fmt == OUT_F32) return static_cast<const float*>(a.C)[idx];
   const uint16_t h = static_cast<const uint16_t*>(a.C)[idx];
   if (a.out_fmt == OUT_BF16) return __uint_as_float(static_cast<uint32_t>(h) << 16);

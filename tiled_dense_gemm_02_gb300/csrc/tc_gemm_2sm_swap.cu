@@ -35,9 +35,9 @@ namespace {
 // lane l holds column n0 + l, v[i] is row m0 + i (the fused epilogue, when on,
 // is applied in place first).
 template <bool EPI>
-__device__ __forceinline__ void store_block_t(uint32_t (&v)[32], int m0, int n0, bool tma_store,
-                                              const TcArgs& args, const CUtensorMap* mapC, uint8_t* stage_base,
-                                              int& sbuf, int lane, float bias_v) {
+__device__ __forceinline__ void store_block_t(uint32_t (&v)[32], int m0, int n0, int zc, int64_t c_off,
+                                              bool tma_store, const TcArgs& args, const CUtensorMap* mapC,
+                                              uint8_t* stage_base, int& sbuf, int lane, float bias_v) {
   const int out_fmt = args.out_fmt;
   if constexpr (EPI) {
     // lane = column (its bias is bias_v); the 32 prior rows are loaded (each
@@ -47,7 +47,7 @@ __device__ __forceinline__ void store_block_t(uint32_t (&v)[32], int m0, int n0,
     float prior[32];
 #pragma unroll
     for (int i = 0; i < 32; ++i)
-      prior[i] = (col_in && m0 + i < args.M && args.epi.beta != 0.0f) ? load_prior(args, m0 + i, n) : 0.0f;
+      prior[i] = (col_in && m0 + i < args.M && args.epi.beta != 0.0f) ? load_prior(args, m0 + i, n, c_off) : 0.0f;
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(epi_combine(args.epi, __uint_as_float(v[i]), prior[i], bias_v));
   }
@@ -74,7 +74,7 @@ __device__ __forceinline__ void store_block_t(uint32_t (&v)[32], int m0, int n0,
     ptx::fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) {
-      ptx::tma_store_2d(mapC, n0, m0, ptx::smem_u32(buf));
+      ptx::tma_store_3d(mapC, n0, m0, zc, ptx::smem_u32(buf));
       ptx::bulk_commit_group();
     }
     sbuf ^= 1;
@@ -83,12 +83,12 @@ __device__ __forceinline__ void store_block_t(uint32_t (&v)[32], int m0, int n0,
     if (n >= args.N) return;
     const int rows = min(32, args.M - m0);
     if (out_fmt == OUT_F32) {
-      float* c = static_cast<float*>(args.C) + static_cast<int64_t>(m0) * args.ldc + n;
+      float* c = static_cast<float*>(args.C) + c_off + static_cast<int64_t>(m0) * args.ldc + n;
 #pragma unroll
       for (int i = 0; i < 32; ++i)
         if (i < rows) c[static_cast<int64_t>(i) * args.ldc] = __uint_as_float(v[i]);
     } else {
-      uint16_t* c = static_cast<uint16_t*>(args.C) + static_cast<int64_t>(m0) * args.ldc + n;
+      uint16_t* c = static_cast<uint16_t*>(args.C) + c_off + static_cast<int64_t>(m0) * args.ldc + n;
 #pragma unroll
       for (int i = 0; i < 32; ++i)
         if (i < rows)
@@ -177,8 +177,10 @@ __global__ void __launch_bounds__(32 * (2 + kEpiWarps), 1)
       uint32_t phase = 0, filled = 0, last_parity = 0;
       bool ok = true;
       for (int t = pair; ok && t < args.num_tiles; t += npairs) {
+        const int b = t / args.tiles_per;  // matrix of the batch
         int mb, nb;
-        tile_coords(t, args, mb, nb);
+        tile_coords(t - b * args.tiles_per, args, mb, nb);
+        const int za = args.stride_a ? b : 0, zb = args.stride_b ? b : 0;
         const int a_row = mb * TM + static_cast<int>(rank) * TMH;
         const int b_col = nb * TN + static_cast<int>(rank) * (TN / 2);
         for (int kb = 0; kb < args.k_blocks; ++kb) {
@@ -194,9 +196,9 @@ __global__ void __launch_bounds__(32 * (2 + kEpiWarps), 1)
             const int k0 = (kb * KSUB + s) * kTileK;  // sub-blocks past K load zeros
 #pragma unroll
             for (int j = 0; j < 2; ++j)
-              ptx::tma_load_2d_pair(ptx::smem_u32(sA + stage * A_BYTES + s * A_SUB + j * 8192), &mapB,
-                                    b_col + j * 64, k0, fb);
-            ptx::tma_load_2d_pair(ptx::smem_u32(sB + stage * B_BYTES + s * B_SUB), &mapA, k0, a_row, fb);
+              ptx::tma_load_3d_pair(ptx::smem_u32(sA + stage * A_BYTES + s * A_SUB + j * 8192), &mapB,
+                                    b_col + j * 64, k0, zb, fb);
+            ptx::tma_load_3d_pair(ptx::smem_u32(sB + stage * B_BYTES + s * B_SUB), &mapA, k0, a_row, za, fb);
           }
           filled |= 1u << stage;
           last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
@@ -267,8 +269,10 @@ __global__ void __launch_bounds__(32 * (2 + kEpiWarps), 1)
     int acc = 0, sbuf = 0;
     uint32_t acc_phase = 0;
     for (int t = pair; t < args.num_tiles; t += npairs) {
+      const int b = t / args.tiles_per;  // matrix of the batch
+      const int64_t c_off = b * args.stride_c;
       int mb, nb;
-      tile_coords(t, args, mb, nb);
+      tile_coords(t - b * args.tiles_per, args, mb, nb);
       // this warp's TMEM lanes are 32 columns of C
       const int n0 = nb * TN + static_cast<int>(rank) * (TN / 2) + q * 32;
       float bias_v = 0.0f;
@@ -277,7 +281,7 @@ __global__ void __launch_bounds__(32 * (2 + kEpiWarps), 1)
         // L2, and the lane's column bias into a register
         if (args.epi.beta != 0.0f && tma_store && lane == 0 && n0 < args.N)
           for (int c = 0; c < TM / 32 && mb * TM + c * 32 < args.M; ++c)
-            ptx::tma_prefetch_l2_2d(&mapC, n0, mb * TM + c * 32);
+            ptx::tma_prefetch_l2_3d(&mapC, n0, mb * TM + c * 32, b);
         if (args.epi.bias && n0 + lane < args.N) bias_v = args.epi.bias[n0 + lane];
       }
       if (!warp_wait(ptx::smem_u32(&acc_full[acc]), acc_phase, ctl, SITE_EPI_ACC_FULL)) break;
@@ -291,7 +295,7 @@ __global__ void __launch_bounds__(32 * (2 + kEpiWarps), 1)
           uint32_t v[32];
           ptx::tmem_ld_32x32b_x32(tbase + c * 32, v);
           ptx::tmem_wait_ld();
-          store_block_t<EPI>(v, m0, n0, tma_store, args, &mapC, stage_base, sbuf, lane, bias_v);
+          store_block_t<EPI>(v, m0, n0, b, c_off, tma_store, args, &mapC, stage_base, sbuf, lane, bias_v);
         }
       }
       ptx::tc_fence_before_sync();

@@ -84,6 +84,12 @@ struct TcArgs {
   unsigned int* sk_flags;  // per worker, CTA and epilogue warp
   unsigned int sk_epoch;   // value a flag holds once this call's partial is written
   Epilogue epi;
+  // Strided batch (swapped-operand pair kernel): tiles [b * tiles_per,
+  // (b + 1) * tiles_per) belong to matrix b, whose operands start stride_*
+  // elements after matrix b - 1's (a stride of 0 repeats one matrix).  A plain
+  // product is a batch of one.
+  int tiles_per;
+  int64_t stride_a, stride_b, stride_c;
 };
 
 // Workspace of the stream-K tail for `workers` CTA pairs and tile width bn.
@@ -161,8 +167,9 @@ cudaError_t launch_tc_pair(int bn, bool staged, int ksub, int cluster, const CUt
                            const CUtensorMap& mapB, const CUtensorMap& mapB_tail, const CUtensorMap& mapC,
                            const TcArgs& args, int clusters, cudaStream_t stream);
 // CTA pairs computing TM x 256 tiles of C as tiles of C^T = B^T A^T (the MMA's
-// M along C's columns, its N = tm along C's rows).  mapA's box is tm/2 rows of
-// A, mapB's 64 columns x 64 k, mapC's an unswizzled 32 x 32 block.
+// M along C's columns, its N = tm along C's rows).  The maps are 3-D (matrix
+// index last, extent 1 for an operand whose batch stride is 0): mapA's box is
+// tm/2 rows of A, mapB's 64 columns x 64 k, mapC's an unswizzled 32 x 32 block.
 cudaError_t launch_tc_pair_swap(int tm, int ksub, const CUtensorMap& mapA, const CUtensorMap& mapB,
                                 const CUtensorMap& mapC, const TcArgs& args, int pairs, cudaStream_t stream);
 // Number of clusters of `cluster` CTAs (2 or 4) of the pair kernel that can be
