@@ -66,7 +66,7 @@ def parse_args():
     p.add_argument("--gpus", type=int, default=1)
     p.add_argument("--steps", type=int, default=50)
     p.add_argument("--warmup", type=int, default=5)
-    p.add_argument("--workload", default=wl.HEADLINE.name, choices=sorted(wl.BY_NAME))
+    p.add_argument("--workload", default=wl.HEADLINE.name, choices=sorted(wl.BY_NAME) + sorted(wl.TRANSPOSE_BY_NAME))
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU work of the oracle sample")
@@ -372,8 +372,153 @@ def run_ours(args, w: wl.Workload):
         torch.distributed.destroy_process_group()
 
 
+def transpose_oracle_sample(w, target_seconds: float):
+    """The oracle's transpose on host cores over a bounded slice of the
+    workload's rows (grown until about target_seconds of work): GB/s of the
+    same traffic measure (each element read and written once)."""
+    import numpy as np
+    from oracle import transpose as ot
+    rng = np.random.default_rng(w.seed)
+    bits = np.uint32 if w.elem_bytes == 4 else np.uint16
+    rows = 256
+    while True:
+        src = rng.integers(0, 2 ** 16, size=(rows, w.cols), dtype=np.uint64).astype(bits)
+        t0 = time.perf_counter()
+        ot.transpose(src, rows, w.cols)
+        dt = time.perf_counter() - t0
+        if dt >= target_seconds or rows >= w.rows:
+            break
+        rows = min(w.rows, rows * 2 if dt < target_seconds / 4 else int(rows * target_seconds / max(dt, 1e-6)) + 1)
+    moved = 2 * rows * w.cols * w.elem_bytes
+    return {"value": moved / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"rows 0..{rows - 1} of the {w.rows}x{w.cols} transpose ({dt:.2f} s, numpy column copies, "
+                      f"one thread)"}
+
+
+def run_transpose_reference(args, w):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    per = max(0.5, min(args.cpu_seconds, 60.0) / max(args.steps + args.warmup, 1))
+    for _ in range(args.warmup):
+        transpose_oracle_sample(w, per)
+    vals = [transpose_oracle_sample(w, per) for _ in range(args.steps)]
+    value = statistics.median(v["value"] for v in vals)
+    print(json.dumps({
+        "impl": "reference", "metric": "transpose GB/s", "value": value, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "u32" if w.elem_bytes == 4 else "u16", "data": "synthetic",
+        "config": {"workload": w.name, "rows": w.rows, "cols": w.cols, "elem_bytes": w.elem_bytes},
+        "cpu_baseline": {**vals[-1], "value": value},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}), flush=True)
+
+
+def run_transpose(args, w):
+    """The tiled transpose: GB/s of HBM traffic (each element read once and
+    written once), against the measured copy bandwidth."""
+    import torch
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    _build_library()
+    import tiled_dense_gemm_02_gb300 as tg
+    tdt = torch.int32 if w.elem_bytes == 4 else torch.int16
+    gen = torch.Generator(device="cpu").manual_seed(w.seed)
+    src_host = torch.randint(-2 ** 15, 2 ** 15, (w.rows, w.cols), generator=gen, dtype=torch.int32).to(tdt).pin_memory()
+    dst_host = torch.empty((w.cols, w.rows), dtype=tdt).pin_memory()
+    src = src_host.to(dev)
+    dst = torch.empty((w.cols, w.rows), dtype=tdt, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sptr = stream.cuda_stream
+
+    def call():
+        st = tg.transpose(w.rows, w.cols, src.data_ptr(), w.cols, dst.data_ptr(), w.rows, w.elem_bytes, sptr)
+        if st != tg.OK:
+            raise RuntimeError(tg.status_string(st))
+
+    for _ in range(max(args.warmup, 3)):
+        call()
+    torch.cuda.synchronize(dev)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    sampler.start()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    wall0 = time.perf_counter()
+    for i in range(args.steps):   # 2 GiB (fp32) per step: inputs far larger than L2
+        starts[i].record(stream)
+        call()
+        ends[i].record(stream)
+    torch.cuda.synchronize(dev)
+    wall = time.perf_counter() - wall0
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop()
+    step_ms = [s_.elapsed_time(e_) for s_, e_ in zip(starts, ends)]
+    total_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms = total_ms / args.steps
+    value = world * w.bytes_moved * args.steps / (total_ms / 1e3) / 1e9
+    # end to end: host -> device copy of the input, the transpose, device -> host copy of the result
+    e2e = []
+    for i in range(5):
+        s_, e_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s_.record(stream)
+        src.copy_(src_host, non_blocking=True)
+        call()
+        dst_host.copy_(dst, non_blocking=True)
+        e_.record(stream)
+        torch.cuda.synchronize(dev)
+        if i >= 2:
+            e2e.append(s_.elapsed_time(e_))
+    e2e_ms = sum(e2e) / len(e2e)
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
+    peaks, peak_src = load_peaks()
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    achieved = w.bytes_moved / (ms / 1e3) / 1e9
+    line = {
+        "metric": "transpose GB/s", "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "u32" if w.elem_bytes == 4 else "u16", "data": "synthetic",
+        "config": {"workload": w.name, "rows": w.rows, "cols": w.cols, "elem_bytes": w.elem_bytes,
+                   "l2": f"inputs {w.rows * w.cols * w.elem_bytes >> 20} MiB, far larger than L2 (no flush)",
+                   "parallelism": f"replicas{world}", "step_ms_min": min(step_ms),
+                   "step_ms_median": statistics.median(step_ms), "wall_s": wall},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                     "traffic": None, "peak_source": f"{peak_src} hbm_gbs (copy)",
+                     "algorithmic_bytes_per_launch": w.bytes_moved},
+        "cpu_baseline": None if (args.no_cpu_baseline or world > 1) else transpose_oracle_sample(w, args.cpu_seconds),
+        "clocks": clocks,
+        "e2e": {"value": world * w.bytes_moved / (e2e_ms / 1e3) / 1e9, "unit": "GB/s", "ms_per_step": e2e_ms,
+                "h2d_bytes_per_step": w.rows * w.cols * w.elem_bytes,
+                "d2h_bytes_per_step": w.rows * w.cols * w.elem_bytes},
+        "gpu_launches": args.steps,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
 def main():
     args = parse_args()
+    if args.workload in wl.TRANSPOSE_BY_NAME:
+        if args.impl == "reference":
+            run_transpose_reference(args, wl.TRANSPOSE_BY_NAME[args.workload])
+        else:
+            run_transpose(args, wl.TRANSPOSE_BY_NAME[args.workload])
+        return
     w = wl.BY_NAME[args.workload]
     if args.impl == "reference":
         run_reference(args, w)

@@ -178,6 +178,9 @@ typedef struct tgemm_plan_info {
                         256-row tiles, scheduled two at a time) */
   int swap_ab;       /* 1: pairs with the MMA's operands exchanged (tile_m x
                         256 tiles of C computed as tiles of C^T) */
+  int tuned;         /* 1: options from the library's table of measured
+                        shapes (the call left every tuned option at 0 and its
+                        shape and dtype match an entry exactly) */
 } tgemm_plan_info;
 
 TGEMM_API int tgemm_plan(int64_t M, int64_t N, int64_t K,
@@ -335,6 +338,24 @@ TGEMM_API int tgemm_plan_batched(int64_t batch, int64_t M, int64_t N, int64_t K,
                const void* C, int64_t ldc, int64_t stride_c,
                int dtype, const tgemm_options* opts, int sm_count,
                tgemm_plan_info* out, int* launches);
+
+/*
+ * Tiled transpose ("CUDA tile", section 三: a tile read along the rows of the
+ * input and written along the rows of the output, so both sides coalesce):
+ *
+ *   dst[j * ld_dst + i] = src[i * ld_src + j]   for i < rows, j < cols
+ *
+ * src is rows x cols (ld_src >= max(1, cols)), dst is cols x rows
+ * (ld_dst >= max(1, rows)); elements are moved as raw elem_bytes-byte units
+ * (2 or 4: fp16/bf16 or fp32), so the result is bit-exact.  Elements of dst
+ * past `rows` in each row are not written.  src and dst must not overlap
+ * (TGEMM_ERR_ALIAS; no in-place transpose).  rows or cols == 0: nothing is
+ * done.  Asynchronous on `stream`; allocates nothing.
+ */
+TGEMM_API int tgemm_transpose(int64_t rows, int64_t cols,
+               const void* src, int64_t ld_src,
+               void* dst, int64_t ld_dst,
+               int elem_bytes, void* stream);
 
 /* Waits for `stream`, then returns and clears the device-side status word
  * that bounded in-kernel waits set when they give up (TGEMM_OK or

@@ -31,7 +31,8 @@ def test_header_declares_the_abi():
     names = declared_functions()
     assert names == sorted(["tgemm_gemm", "tgemm_gemm_ex", "tgemm_gemm_ws", "tgemm_workspace_size", "tgemm_plan",
                             "tgemm_gemm_noalloc", "tgemm_gemm_epilogue", "tgemm_gemm_batched",
-                            "tgemm_plan_batched", "tgemm_device_status", "tgemm_status_string", "tgemm_version"])
+                            "tgemm_plan_batched", "tgemm_transpose", "tgemm_device_status", "tgemm_status_string",
+                            "tgemm_version"])
 
 
 def test_library_exports_every_declared_symbol(tg):
@@ -249,6 +250,19 @@ def test_batched_planning(tg):
     # the call validates on the host as well (no GPU here)
     assert tg.gemm_batched(4, M, N, K, A, K, M * K, B, N, K * N, C, N, 5, 2) == tg.ERR_ALIAS
     assert tg.gemm_batched(0, M, N, K, A, K, 0, B, N, 0, C, N, 0, 2) == tg.OK
+
+
+def test_transpose_validation_returns_before_the_device(tg):
+    S, D = 0x10000000, 0x20000000
+    assert tg.transpose(-1, 4, S, 4, D, 4, 4) == tg.ERR_INVALID_VALUE
+    assert tg.transpose(4, 4, S, 3, D, 4, 4) == tg.ERR_INVALID_VALUE     # ld_src < cols
+    assert tg.transpose(4, 5, S, 5, D, 3, 4) == tg.ERR_INVALID_VALUE     # ld_dst < rows
+    assert tg.transpose(4, 4, S, 4, D, 4, 8) == tg.ERR_UNSUPPORTED_DTYPE
+    assert tg.transpose(4, 4, S + 2, 4, D, 4, 4) == tg.ERR_MISALIGNED
+    assert tg.transpose(64, 64, S, 64, S + 4 * 64 * 10, 64, 4) == tg.ERR_ALIAS
+    assert tg.transpose(4, 4, 0, 4, D, 4, 4) == tg.ERR_INVALID_VALUE
+    assert tg.transpose(0, 4, S, 4, D, 1, 4) == tg.OK
+    assert tg.transpose(1 << 31, 4, S, 4, D, 1 << 31, 2) == tg.ERR_TOO_LARGE
 
 
 def test_two_pair_cluster_planning(tg):

@@ -34,7 +34,7 @@ def case(M, N, K, dtype, dist="uniform", seed=20, lda=None, ldb=None, ldc=None, 
 # ------------------------------------------------------------------ workloads
 
 @pytest.mark.parametrize("name", ["f32_64x64x64", "f16_1024x1024x1024", "bf16_2048x2048x2048",
-                                  "bf16_1000x1500x4096_ragged"])
+                                  "bf16_1000x1500x4096_ragged", "f16_512x512x512"])
 def test_workload_full_product(name):
     w = wl.BY_NAME[name]
     A, B = wl.make_inputs(w)
@@ -42,7 +42,8 @@ def test_workload_full_product(name):
     H.check_full(res, A, B, w.M, w.N, w.K, w.dtype, name)
 
 
-@pytest.mark.parametrize("name", ["bf16_4096x4096x4096_f32out", "f32_4096x4096x4096", "f32_2048x2048x2048"])
+@pytest.mark.parametrize("name", ["bf16_4096x4096x4096_f32out", "f32_4096x4096x4096", "f32_2048x2048x2048",
+                                  "f16_8192x8192x8192"])
 def test_workload_sampled(name):
     """Full-size products in the launch configuration the benchmark times,
     checked on every element of the border rows/columns and random samples."""

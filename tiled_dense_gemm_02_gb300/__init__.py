@@ -28,7 +28,7 @@ ACT_NONE, ACT_RELU = 0, 1
 
 EXPORTS = ("tgemm_gemm", "tgemm_gemm_ex", "tgemm_gemm_ws", "tgemm_workspace_size", "tgemm_plan",
            "tgemm_gemm_noalloc", "tgemm_gemm_epilogue", "tgemm_gemm_batched", "tgemm_plan_batched",
-           "tgemm_device_status", "tgemm_status_string", "tgemm_version")
+           "tgemm_transpose", "tgemm_device_status", "tgemm_status_string", "tgemm_version")
 # bytes of the scratch array built into the library (TGEMM_NOALLOC_SCRATCH_BYTES)
 NOALLOC_SCRATCH_BYTES = 20 * 1024 * 1024 + 4096
 
@@ -56,7 +56,7 @@ class PlanInfo(ctypes.Structure):
                 ("a_copy_bytes", ctypes.c_int), ("b_copy_bytes", ctypes.c_int), ("store_bytes", ctypes.c_int),
                 ("smem_bytes", ctypes.c_int), ("cta_group", ctypes.c_int), ("dp_tiles", ctypes.c_int),
                 ("sk_iters", ctypes.c_int), ("workspace_bytes", ctypes.c_int),
-                ("cluster_ctas", ctypes.c_int), ("swap_ab", ctypes.c_int)]
+                ("cluster_ctas", ctypes.c_int), ("swap_ab", ctypes.c_int), ("tuned", ctypes.c_int)]
 
     def as_dict(self) -> dict:
         return {name: getattr(self, name) for name, _ in self._fields_ if name != "reserved"}
@@ -99,6 +99,8 @@ def _load():
                                        ctypes.POINTER(Options), ip, ctypes.POINTER(PlanInfo),
                                        ctypes.POINTER(ctypes.c_int)]
     lib.tgemm_plan_batched.restype = ip
+    lib.tgemm_transpose.argtypes = [i64, i64, vp, i64, vp, i64, ip, vp]
+    lib.tgemm_transpose.restype = ip
     lib.tgemm_device_status.argtypes = [vp]
     lib.tgemm_device_status.restype = ip
     lib.tgemm_status_string.argtypes = [ip]
@@ -184,6 +186,11 @@ def plan_batched(batch, M, N, K, A, lda, stride_a, B, ldb, stride_b, C, ldc, str
     st = _lib.tgemm_plan_batched(batch, M, N, K, A, lda, stride_a, B, ldb, stride_b, C, ldc, stride_c, dtype,
                                  _opts(options), sm_count, ctypes.byref(info), ctypes.byref(n))
     return st, info, n.value
+
+
+def transpose(rows, cols, src, ld_src, dst, ld_dst, elem_bytes, stream=0) -> int:
+    """tgemm_transpose: dst (cols x rows) = src (rows x cols) transposed."""
+    return _lib.tgemm_transpose(rows, cols, src, ld_src, dst, ld_dst, elem_bytes, stream)
 
 
 def workspace_size(M, N, K, A, lda, B, ldb, C, ldc, dtype, options=None):

@@ -121,6 +121,7 @@ struct Plan {
   int64_t workspace = 0;          // bytes of workspace the stream-K split uses
   int64_t batch = 1;              // matrices computed by one launch (strided batch, swapped kernel)
   bool batch_loop = false;        // a batch the kernels cannot index: one launch per matrix
+  bool tuned = false;             // options from the tuned-shape table
 };
 
 // Relative throughput of one SM per output column for each tile width,
@@ -236,9 +237,64 @@ int pick_swap_tile_m(int64_t M, int64_t N, int pairs, double* cost, int64_t batc
   return best;
 }
 
+// Launch options measured fastest per shape (tiled_dense_gemm_02_gb300/tune.py),
+// used when a call leaves every tuned option at 0.
+struct TunedShape {
+  int64_t M, N, K;
+  int dtype;
+  int kernel, cta_group, tile_n, tile_m, swap_ab, tile_k, group_m;
+};
+const TunedShape kTuned[] = {
+#include "tuned_shapes.inc"
+    {0, 0, 0, -1, 0, 0, 0, 0, 0, 0, 0}  // end
+};
+
+const TunedShape* tuned_entry(int64_t M, int64_t N, int64_t K, int dtype, const tgemm_options& o) {
+  if (o.kernel || o.tile_n || o.group_m || o.max_ctas || o.cta_group || o.tile_k || o.stream_k || o.multicast ||
+      o.swap_ab || o.tile_m)
+    return nullptr;
+  for (const TunedShape& t : kTuned)
+    if (t.dtype == dtype && t.M == M && t.N == N && t.K == K) return &t;
+  return nullptr;
+}
+
+int make_plan_core(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb,
+                   const void* C, int64_t ldc, int dtype, const tgemm_options* o, int sms, int pair_cap, int quad_cap,
+                   int64_t workspace_bytes, Plan& p, int64_t batch);
+
+// The plan of a call: the tuned options of its shape when there is an entry
+// and they suit this call (pointers, alignment), else the heuristics.
 int make_plan(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb,
               const void* C, int64_t ldc, int dtype, const tgemm_options* o, int sms, int pair_cap, int quad_cap,
               int64_t workspace_bytes, Plan& p, int64_t batch = 1) {
+  tgemm_options opt;
+  std::memset(&opt, 0, sizeof opt);
+  if (o) opt = *o;
+  if (batch == 1) {
+    if (const TunedShape* t = tuned_entry(M, N, K, dtype, opt)) {
+      tgemm_options tuned = opt;
+      tuned.kernel = t->kernel;
+      tuned.cta_group = t->cta_group;
+      tuned.tile_n = t->tile_n;
+      tuned.tile_m = t->tile_m;
+      tuned.swap_ab = t->swap_ab;
+      tuned.tile_k = t->tile_k;
+      tuned.group_m = t->group_m;
+      Plan q;
+      if (make_plan_core(M, N, K, A, lda, B, ldb, C, ldc, dtype, &tuned, sms, pair_cap, quad_cap, workspace_bytes, q,
+                         batch) == TGEMM_OK) {
+        p = q;
+        p.tuned = true;
+        return TGEMM_OK;
+      }
+    }
+  }
+  return make_plan_core(M, N, K, A, lda, B, ldb, C, ldc, dtype, o, sms, pair_cap, quad_cap, workspace_bytes, p, batch);
+}
+
+int make_plan_core(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb,
+                   const void* C, int64_t ldc, int dtype, const tgemm_options* o, int sms, int pair_cap, int quad_cap,
+                   int64_t workspace_bytes, Plan& p, int64_t batch) {
   if (dtype < TGEMM_F32 || dtype > TGEMM_F16_F32OUT) return TGEMM_ERR_UNSUPPORTED_DTYPE;
   if (M < 0 || N < 0 || K < 0) return TGEMM_ERR_INVALID_VALUE;
   if (M >= (int64_t(1) << 31) || N >= (int64_t(1) << 31) || K >= (int64_t(1) << 31)) return TGEMM_ERR_TOO_LARGE;
@@ -848,6 +904,28 @@ int tgemm_plan_batched(int64_t batch, int64_t M, int64_t N, int64_t K, const voi
   return st;
 }
 
+int tgemm_transpose(int64_t rows, int64_t cols, const void* src, int64_t ld_src, void* dst, int64_t ld_dst,
+                    int elem_bytes, void* stream) {
+  if (rows < 0 || cols < 0) return TGEMM_ERR_INVALID_VALUE;
+  if (elem_bytes != 2 && elem_bytes != 4) return TGEMM_ERR_UNSUPPORTED_DTYPE;
+  if (rows >= (int64_t(1) << 31) || cols >= (int64_t(1) << 31) || (rows + 63) / 64 > 65535) return TGEMM_ERR_TOO_LARGE;
+  if (ld_src < std::max<int64_t>(1, cols) || ld_dst < std::max<int64_t>(1, rows)) return TGEMM_ERR_INVALID_VALUE;
+  if (rows == 0 || cols == 0) return TGEMM_OK;
+  if (!src || !dst) return TGEMM_ERR_INVALID_VALUE;
+  const uint64_t s0 = reinterpret_cast<uint64_t>(src), d0 = reinterpret_cast<uint64_t>(dst);
+  if (s0 % elem_bytes || d0 % elem_bytes) return TGEMM_ERR_MISALIGNED;
+  const uint64_t s1 = s0 + static_cast<uint64_t>((rows - 1) * ld_src + cols) * elem_bytes;
+  const uint64_t d1 = d0 + static_cast<uint64_t>((cols - 1) * ld_dst + rows) * elem_bytes;
+  if (tgemm::ranges_overlap(s0, s1, d0, d1)) return TGEMM_ERR_ALIAS;
+  tgemm::DeviceInfo* dev = nullptr;
+  int st = tgemm::device_info(&dev);
+  if (st != TGEMM_OK) return st;
+  const bool vec = s0 % 16 == 0 && d0 % 16 == 0 && (ld_src * elem_bytes) % 16 == 0 && (ld_dst * elem_bytes) % 16 == 0;
+  const cudaError_t e = tgemm::launch_transpose(src, ld_src, dst, ld_dst, static_cast<int>(rows), static_cast<int>(cols),
+                                                elem_bytes, vec, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? TGEMM_OK : tgemm::cuda_fail(e, "transpose launch");
+}
+
 int tgemm_workspace_size(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb,
                          const void* C, int64_t ldc, int dtype, const tgemm_options* opts, size_t* bytes) {
   if (!bytes) return TGEMM_ERR_INVALID_VALUE;
@@ -890,6 +968,7 @@ int tgemm_plan(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, cons
       out->cta_group = p.pair ? 2 : 1;
       out->cluster_ctas = p.pair ? p.cluster : 1;
       out->swap_ab = p.swap ? 1 : 0;
+      out->tuned = p.tuned ? 1 : 0;
       out->dp_tiles = p.dp_tiles;
       out->sk_iters = p.sk_iters;
       out->workspace_bytes = p.workspace;

@@ -177,6 +177,10 @@ cudaError_t launch_tc_pair_swap(int tm, int ksub, const CUtensorMap& mapA, const
 cudaError_t tc_pair_capacity(int cluster, int* clusters);
 cudaError_t launch_simt(const SimtArgs& args, cudaStream_t stream);
 cudaError_t launch_zero_fill(void* C, int64_t rows, int64_t cols, int64_t ldc, int elem_bytes, cudaStream_t stream);
+// out[j][i] = in[i][j], in rows x cols; elem_bytes 2 or 4; vec: every row of
+// in and out starts on a 16-byte boundary (16-byte accesses)
+cudaError_t launch_transpose(const void* in, int64_t ld_in, void* out, int64_t ld_out, int rows, int cols,
+                             int elem_bytes, bool vec, cudaStream_t stream);
 // K = 0 with a fused epilogue (out_fmt: OutFmt)
 cudaError_t launch_epilogue_fill(void* C, int64_t rows, int64_t cols, int64_t ldc, int out_fmt, const Epilogue& e,
                                  cudaStream_t stream);

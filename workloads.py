@@ -90,8 +90,35 @@ WORKLOADS = [
     # fp32 shapes large enough to load the FP32 pipe
     Workload("f32_4096x4096x4096", 4096, 4096, 4096, F32, "uniform", 5),
     Workload("f32_2048x2048x2048", 2048, 2048, 2048, F32, "uniform", 6),
+    # the two shapes "GPU Kernel 的 Tile、Grid、Wave 与 Launch Overhead" sets as exercises
+    # (too few tiles to fill the GPU, and so many that the tile count must shrink)
+    Workload("f16_512x512x512", 512, 512, 512, F16, "normal", 7),
+    Workload("f16_8192x8192x8192", 8192, 8192, 8192, F16, "normal", 8),
 ]
 BY_NAME = {w.name: w for w in WORKLOADS}
+
+
+@dataclass(frozen=True)
+class TransposeWorkload:
+    """out = in^T for an in matrix of rows x cols ("CUDA tile", section 三),
+    elements of elem_bytes moved as raw bits; inputs are seeded random bits."""
+    name: str
+    rows: int
+    cols: int
+    elem_bytes: int
+    seed: int
+
+    @property
+    def bytes_moved(self) -> int:
+        return 2 * self.rows * self.cols * self.elem_bytes
+
+
+# Far larger than L2 (1 GiB per matrix for fp32), so every step streams HBM.
+TRANSPOSE_WORKLOADS = [
+    TransposeWorkload("transpose_f32_16384x16384", 16384, 16384, 4, 0x7A05E000),
+    TransposeWorkload("transpose_bf16_16384x16384", 16384, 16384, 2, 0x7A05E001),
+]
+TRANSPOSE_BY_NAME = {w.name: w for w in TRANSPOSE_WORKLOADS}
 HEADLINE = BY_NAME["bf16_4096x4096x4096_f32out"]
 
 
