@@ -82,6 +82,29 @@ def dist_env():
     return world, rank, local
 
 
+def init_replicas(local: int, backend: str | None = None):
+    """One process per GPU, each an independent replica: the process group
+    carries only the start/stop barriers and the max-over-ranks timing (no data
+    exchange).  nccl on a GPU machine, gloo where there is none (tests)."""
+    import torch
+    import torch.distributed as dist
+    if backend is None:
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+    if backend == "nccl":
+        torch.cuda.set_device(local)
+    dist.init_process_group(backend)
+    return backend
+
+
+def max_over_ranks(value: float, device) -> float:
+    """The largest `value` over all ranks (the slowest replica sets the time)."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -226,9 +249,7 @@ def run_ours(args, w: wl.Workload):
     import torch
     world, rank, local = dist_env()
     if world > 1:
-        import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl")
+        init_replicas(local, "nccl")
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
 
@@ -295,9 +316,7 @@ def run_ours(args, w: wl.Workload):
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     total_ms = sum(step_ms)
     if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+        total_ms = max_over_ranks(total_ms, dev)
     assert tg.device_status(sptr) == tg.OK
     ms_per_step = total_ms / args.steps
     value = world * w.flops * args.steps / (total_ms / 1e3) / 1e12
@@ -319,9 +338,7 @@ def run_ours(args, w: wl.Workload):
         torch.cuda.synchronize(dev)
     e2e_ms = sum(s.elapsed_time(e) for s, e in zip(e_s, e_e)) / e2e_steps
     if world > 1:
-        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+        e2e_ms = max_over_ranks(e2e_ms, dev)
     e2e_value = world * w.flops / (e2e_ms / 1e3) / 1e12
 
     if rank != 0:
@@ -419,9 +436,7 @@ def run_transpose(args, w):
     import torch
     world, rank, local = dist_env()
     if world > 1:
-        import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl")
+        init_replicas(local, "nccl")
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     _build_library()
@@ -463,9 +478,7 @@ def run_transpose(args, w):
     step_ms = [s_.elapsed_time(e_) for s_, e_ in zip(starts, ends)]
     total_ms = sum(step_ms)
     if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+        total_ms = max_over_ranks(total_ms, dev)
     ms = total_ms / args.steps
     value = world * w.bytes_moved * args.steps / (total_ms / 1e3) / 1e9
     # end to end: host -> device copy of the input, the transpose, device -> host copy of the result

@@ -1,0 +1,59 @@
+"""The N > 1 path of bench.py on CPU: the product has no exchange step, so N
+GPUs run N independent replicas; the process group carries only barriers and
+the max-over-ranks timing.  These tests run that host logic as world-size-2
+gloo groups (no GPU), and the reference arm under torchrun, where rank 0
+alone works and prints."""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def free_port() -> int:
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _replica(rank, world, port, out_path):
+    os.environ.update({"MASTER_ADDR": "127.0.0.1", "MASTER_PORT": str(port), "RANK": str(rank),
+                       "WORLD_SIZE": str(world), "LOCAL_RANK": str(rank)})
+    sys.path.insert(0, ROOT)
+    import bench
+    import torch.distributed as dist
+    backend = bench.init_replicas(rank, "gloo")
+    assert backend == "gloo"
+    # each replica "timed" its own steps; the slowest one sets the job's time
+    local_ms = 10.0 + 5.0 * rank
+    total = bench.max_over_ranks(local_ms, "cpu")
+    dist.barrier()
+    with open(f"{out_path}.{rank}", "w") as f:
+        json.dump({"rank": rank, "max_ms": total}, f)
+    dist.destroy_process_group()
+
+
+def test_max_over_ranks_with_gloo(tmp_path):
+    port = free_port()
+    out = str(tmp_path / "r")
+    mp.spawn(_replica, args=(2, port, out), nprocs=2, join=True)
+    got = [json.load(open(f"{out}.{r}")) for r in range(2)]
+    assert all(g["max_ms"] == 15.0 for g in got)
+
+
+def test_reference_arm_under_torchrun_prints_once_from_rank_0():
+    port = free_port()
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+           "--master-addr", "127.0.0.1", "--master-port", str(port), "bench.py", "--impl", "reference",
+           "--gpus", "2", "--workload", "f32_64x64x64", "--steps", "1", "--warmup", "0"]
+    p = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=300)
+    assert p.returncode == 0, p.stderr[-2000:]
+    lines = [l for l in p.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1, p.stdout
+    line = json.loads(lines[0])
+    assert line["impl"] == "reference" and line["n_gpus"] == 2 and line["value"] > 0
