@@ -153,7 +153,7 @@ def test_dispatch_aligned_uses_bulk_tensor_copies(tg):
     st, p = plan(tg, 4096, 4096, 4096, dtype=3, sms=148)
     assert st == tg.OK
     assert p.kernel == tg.KERNEL_TC_TMA and p.a_copy_bytes == 0 and p.b_copy_bytes == 0 and p.store_bytes == 0
-    assert p.tile_m in (128, 256) and p.tile_k in (64, 128)
+    assert p.tile_m in (128, 192, 224, 256) and p.tile_k in (64, 128)
     assert p.tiles_m * p.tile_m >= 4096 and p.tiles_n * p.tile_n >= 4096
     assert p.ctas == min(148, p.tiles_m * p.tiles_n)
     assert p.smem_bytes <= 232448
@@ -195,6 +195,24 @@ def test_pair_planning(tg):
     assert st == tg.OK and p.tile_k == 128 and p.stages == 3 and p.smem_bytes <= 232448
     assert plan(tg, 4096, 4096, 4096, dtype=3, cta_group=1, tile_k=128)[0] == tg.ERR_INVALID_VALUE
     assert plan(tg, 4096, 4096, 4096, dtype=3, tile_k=96)[0] == tg.ERR_INVALID_VALUE
+
+
+def test_tuned_shape_table(tg):
+    """Calls that leave every tuned option at 0 and match a measured shape take
+    the table's options; any tuned option set, another shape, or pointers the
+    entry cannot serve keep the heuristics."""
+    st, p = plan(tg, 1024, 1024, 1024, dtype=1, sms=152)
+    assert st == tg.OK and p.tuned == 1 and (p.cta_group, p.tile_n, p.group_m) == (1, 64, 4)
+    st, p = plan(tg, 1024, 1024, 1024, dtype=1, sms=152, group_m=8)
+    assert st == tg.OK and p.tuned == 0 and p.group_m == 8
+    st, p = plan(tg, 1024, 1024, 1000, dtype=1, sms=152)
+    assert p.tuned == 0
+    st, p = plan(tg, 4096, 4096, 4096, dtype=3, sms=152)
+    assert p.tuned == 1 and p.swap_ab == 1 and p.tile_m == 224
+    # the 2048^3 bf16 entry asks for the swapped kernel, which needs bulk-tensor rows:
+    # with 2-byte-misaligned A the table is skipped and the heuristics pick a copy kernel
+    st, p = plan(tg, 2048, 2048, 2048, dtype=2, sms=152, A=A0 + 2)
+    assert st == tg.OK and p.tuned == 0 and p.kernel == tg.KERNEL_TC_COPY
 
 
 def test_swapped_pair_planning(tg):

@@ -44,7 +44,8 @@ def sources() -> list[str]:
 
 def inputs() -> list[str]:
     return sources() + sorted(glob.glob(os.path.join(CSRC, "*.cuh"))) + \
-        sorted(glob.glob(os.path.join(CSRC, "*.h"))) + [HEADER, os.path.abspath(__file__)]
+        sorted(glob.glob(os.path.join(CSRC, "*.h"))) + sorted(glob.glob(os.path.join(CSRC, "*.inc"))) + \
+        [HEADER, os.path.abspath(__file__)]
 
 
 def stale() -> bool:

@@ -40,16 +40,31 @@ __device__ __forceinline__ void store_block_t(uint32_t (&v)[32], int m0, int n0,
                                               uint8_t* stage_base, int& sbuf, int lane, float bias_v) {
   const int out_fmt = args.out_fmt;
   if constexpr (EPI) {
-    // lane = column (its bias is bias_v); the 32 prior rows are loaded (each
-    // row coalesced across the warp) before any is used
-    const int n = n0 + lane;
-    const bool col_in = n < args.N;
-    float prior[32];
+    // lane = column (its bias is bias_v).  Each step is one uniform branch
+    // over the 32 rows, so the per-element work is only the arithmetic (the
+    // epilogue warps share issue slots with the producer and MMA threads).
+    const float alpha = args.epi.alpha, beta = args.epi.beta;
+    float z[32];
 #pragma unroll
-    for (int i = 0; i < 32; ++i)
-      prior[i] = (col_in && m0 + i < args.M && args.epi.beta != 0.0f) ? load_prior(args, m0 + i, n, c_off) : 0.0f;
+    for (int i = 0; i < 32; ++i) z[i] = alpha * __uint_as_float(v[i]);
+    if (beta != 0.0f) {
+      // the 32 prior rows (each coalesced across the warp) are loaded before any is used
+      const int n = n0 + lane;
+      const bool col_in = n < args.N;
+      float prior[32];
 #pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(epi_combine(args.epi, __uint_as_float(v[i]), prior[i], bias_v));
+      for (int i = 0; i < 32; ++i) prior[i] = (col_in && m0 + i < args.M) ? load_prior(args, m0 + i, n, c_off) : 0.0f;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) z[i] = fmaf(beta, prior[i], z[i]);
+    }
+#pragma unroll
+    for (int i = 0; i < 32; ++i) z[i] += bias_v;
+    if (args.epi.act == 1) {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) z[i] = z[i] < 0.0f ? 0.0f : z[i];
+    }
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(z[i]);
   }
   if (tma_store) {
     uint8_t* buf = stage_base + sbuf * 4096;
