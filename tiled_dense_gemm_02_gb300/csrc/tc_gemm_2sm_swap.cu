@@ -115,6 +115,54 @@ __device__ __forceinline__ void store_block_t(uint32_t (&v)[32], int m0, int n0,
 
 // EPI: the fused epilogue is compiled in (the plain product keeps its own
 // instantiation and registers)
+// The fused epilogue with beta != 0 and bulk-tensor stores: the 32 x 32 block's
+// prior C already sits in `buf` (a bulk-tensor load of the same box, in the
+// layout the store reads), so each lane reads its column of it, the results
+// overwrite it in place, and the block goes out as in store_block_t.
+__device__ __forceinline__ void store_block_staged_prior(const uint32_t (&v)[32], uint8_t* buf, int m0, int n0, int zc,
+                                                         const TcArgs& args, const CUtensorMap* mapC, int lane,
+                                                         float bias_v) {
+  const int out_fmt = args.out_fmt;
+  const float alpha = args.epi.alpha, beta = args.epi.beta;
+  float z[32];
+  if (out_fmt == OUT_F32) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) z[i] = *reinterpret_cast<const float*>(buf + i * 128 + lane * 4);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const uint16_t h = *reinterpret_cast<const uint16_t*>(buf + i * 64 + lane * 2);
+      z[i] = out_fmt == OUT_BF16 ? __uint_as_float(static_cast<uint32_t>(h) << 16) : __half2float(__ushort_as_half(h));
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 32; ++i) z[i] = fmaf(beta, z[i], alpha * __uint_as_float(v[i])) + bias_v;
+  if (args.epi.act == 1) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) z[i] = z[i] < 0.0f ? 0.0f : z[i];
+  }
+  __syncwarp();  // every lane has read its prior column before any result overwrites the buffer
+  if (out_fmt == OUT_F32) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) *reinterpret_cast<float*>(buf + i * 128 + lane * 4) = z[i];
+  } else {
+    const bool odd = lane & 1;
+#pragma unroll
+    for (int i = 0; i < 32; i += 2) {
+      const float mine = odd ? z[i + 1] : z[i];
+      const float other = __shfl_xor_sync(0xffffffffu, odd ? z[i] : z[i + 1], 1);
+      const uint32_t word = odd ? pack_pair(other, mine, out_fmt) : pack_pair(mine, other, out_fmt);
+      *reinterpret_cast<uint32_t*>(buf + (odd ? i + 1 : i) * 64 + (lane & ~1) * 2) = word;
+    }
+  }
+  ptx::fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    ptx::tma_store_3d(mapC, n0, m0, zc, ptx::smem_u32(buf));
+    ptx::bulk_commit_group();
+  }
+}
+
 template <int TM, int KSUB, bool EPI>
 __global__ void __launch_bounds__(32 * (2 + kEpiWarps), 1)
     tc_gemm_2sm_swap_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
@@ -144,8 +192,9 @@ __global__ void __launch_bounds__(32 * (2 + kEpiWarps), 1)
   uint64_t* acc_full = empty + STAGES;
   uint64_t* acc_empty = acc_full + 2;
   uint64_t* drain = acc_empty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
-  static_assert((2 * STAGES + 5) * 8 + 8 <= kBarrierBytes, "barrier area");
+  uint64_t* prior_bar = drain + 1;  // two per epilogue warp: prior C blocks staged for beta != 0
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(prior_bar + 2 * kEpiWarps);
+  static_assert((2 * STAGES + 5 + 2 * kEpiWarps) * 8 + 8 <= kBarrierBytes, "barrier area");
   volatile uint32_t* abort_flag = tmem_slot + 1;
 
   const int warp = threadIdx.x >> 5;
@@ -165,6 +214,7 @@ __global__ void __launch_bounds__(32 * (2 + kEpiWarps), 1)
       ptx::mbar_init(ptx::smem_u32(&acc_empty[b]), 2 * kEpiWarps);  // leader only: both CTAs' epilogues
     }
     ptx::mbar_init(ptx::smem_u32(drain), 1);
+    for (int i = 0; i < 2 * kEpiWarps; ++i) ptx::mbar_init(ptx::smem_u32(&prior_bar[i]), 1);
     *abort_flag = 0u;
     ptx::fence_barrier_init();
   }
@@ -283,6 +333,13 @@ __global__ void __launch_bounds__(32 * (2 + kEpiWarps), 1)
     const bool tma_store = args.store_granule == 0;
     int acc = 0, sbuf = 0;
     uint32_t acc_phase = 0;
+    // beta != 0 with bulk-tensor stores: the prior C blocks come through this
+    // warp's two staging buffers by bulk-tensor loads, one block ahead
+    const bool staged_prior = EPI && tma_store && args.epi.beta != 0.0f;
+    const uint32_t pbar0 = ptx::smem_u32(&prior_bar[2 * (warp - 2)]), pbar1 = pbar0 + 8;
+    const uint32_t blk_bytes = args.out_fmt == OUT_F32 ? 4096u : 2048u;
+    uint32_t pphase = 0u;   // bit i: phase of buffer i's barrier
+    uint32_t pending = 0u;  // bit i: a load into buffer i is in flight
     for (int t = pair; t < args.num_tiles; t += npairs) {
       const int b = t / args.tiles_per;  // matrix of the batch
       const int64_t c_off = b * args.stride_c;
@@ -299,19 +356,56 @@ __global__ void __launch_bounds__(32 * (2 + kEpiWarps), 1)
             ptx::tma_prefetch_l2_3d(&mapC, n0, mb * TM + c * 32, b);
         if (args.epi.bias && n0 + lane < args.N) bias_v = args.epi.bias[n0 + lane];
       }
+      const int nblk = min(TM / 32, (args.M - mb * TM + 31) / 32);  // blocks of rows inside C
+      if (staged_prior && n0 < args.N) {
+        // the first block's prior C, loaded while the tile's MMAs run (after
+        // the previous tile's stores have read the buffers)
+        sbuf = 0;
+        if (lane == 0) {
+          ptx::bulk_wait_group_read<0>();
+          ptx::mbar_arrive_expect_tx(pbar0, blk_bytes);
+          ptx::tma_load_3d(ptx::smem_u32(stage_base), &mapC, n0, mb * TM, b, pbar0);
+        }
+        pending |= 1u;
+      }
       if (!warp_wait(ptx::smem_u32(&acc_full[acc]), acc_phase, ctl, SITE_EPI_ACC_FULL)) break;
       ptx::tc_fence_after_sync();
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * ACC);
       if (n0 < args.N) {
+        bool ok = true;
 #pragma unroll 1
-        for (int c = 0; c < TM / 32; ++c) {
+        for (int c = 0; c < nblk; ++c) {
           const int m0 = mb * TM + c * 32;
-          if (m0 >= args.M) break;
           uint32_t v[32];
-          ptx::tmem_ld_32x32b_x32(tbase + c * 32, v);
-          ptx::tmem_wait_ld();
-          store_block_t<EPI>(v, m0, n0, b, c_off, tma_store, args, &mapC, stage_base, sbuf, lane, bias_v);
+          if (staged_prior) {
+            const int cur = c & 1, nxt = cur ^ 1;
+            const uint32_t bar_cur = cur ? pbar1 : pbar0, bar_nxt = cur ? pbar0 : pbar1;
+            if (c + 1 < nblk) {
+              // block c+1's prior into the other buffer, once the store of
+              // block c-1 (its last user) has read it
+              if (lane == 0) {
+                ptx::bulk_wait_group_read<0>();
+                ptx::mbar_arrive_expect_tx(bar_nxt, blk_bytes);
+                ptx::tma_load_3d(ptx::smem_u32(stage_base + nxt * 4096), &mapC, n0, m0 + 32, b, bar_nxt);
+              }
+              pending |= 1u << nxt;
+            }
+            if (!warp_wait(bar_cur, (pphase >> cur) & 1u, ctl, SITE_EPI_PRIOR)) {
+              ok = false;
+              break;
+            }
+            pphase ^= 1u << cur;
+            pending &= ~(1u << cur);
+            ptx::tmem_ld_32x32b_x32(tbase + c * 32, v);
+            ptx::tmem_wait_ld();
+            store_block_staged_prior(v, stage_base + cur * 4096, m0, n0, b, args, &mapC, lane, bias_v);
+          } else {
+            ptx::tmem_ld_32x32b_x32(tbase + c * 32, v);
+            ptx::tmem_wait_ld();
+            store_block_t<EPI>(v, m0, n0, b, c_off, tma_store, args, &mapC, stage_base, sbuf, lane, bias_v);
+          }
         }
+        if (!ok) break;
       }
       ptx::tc_fence_before_sync();
       __syncwarp();
@@ -319,6 +413,9 @@ __global__ void __launch_bounds__(32 * (2 + kEpiWarps), 1)
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
     }
+    // a prior-C load still in flight (a wait gave up) lands before shared memory is released
+    for (int i = 0; i < 2; ++i)
+      if (((pending >> i) & 1u) && lane == 0) wait_teardown(i ? pbar1 : pbar0, (pphase >> i) & 1u, ctl, SITE_TEARDOWN);
     if (lane == 0) ptx::bulk_wait_group<0>();
     __syncwarp();
   }

@@ -21,6 +21,7 @@ enum WaitSite : uint32_t {
   SITE_DRAIN = 6,
   SITE_TEARDOWN = 7,
   SITE_SK_FLAG = 8,
+  SITE_EPI_PRIOR = 9,   // epilogue: the prior C block staged for beta != 0
 };
 constexpr uint32_t kTimeoutFlag = 0x7E000000u;
 
