@@ -158,6 +158,11 @@ __device__ __forceinline__ void cp_async(uint32_t dst, const void* src, uint32_t
   }
 }
 
+// Plain 2-byte store to shared memory (the per-thread copy path's 2-byte granule).
+__device__ __forceinline__ void st_shared_u16(uint32_t addr, uint16_t v) {
+  asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
+}
+
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 
 template <int N>
