@@ -158,6 +158,13 @@ __device__ __forceinline__ void cp_async(uint32_t dst, const void* src, uint32_t
   }
 }
 
+// Arrive on `bar` once every cp.async this thread has issued so far has
+// completed.  The arrival is asynchronous and not pre-counted (.noinc): the
+// barrier's expected count must include it.
+__device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
 // Plain 2-byte store to shared memory (the per-thread copy path's 2-byte granule).
 __device__ __forceinline__ void st_shared_u16(uint32_t addr, uint16_t v) {
   asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");

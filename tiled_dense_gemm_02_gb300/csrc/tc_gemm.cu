@@ -162,10 +162,8 @@ __global__ void __launch_bounds__(tc_threads(kCopy), 1)
   constexpr int B_BYTES = tc_b_atoms(BN) * 8192;
   constexpr int ACC = tc_acc_stride(BN);
   constexpr uint32_t TMEM_COLS = 2 * ACC;
-  // copy producers signal a stage once the copies LAG stages later are issued
-  constexpr int LAG = STAGES - 2;
   static_assert(tc_valid_bn(BN), "tile width");
-  static_assert(STAGES >= 3 && LAG >= 1, "ring depth");
+  static_assert(STAGES >= 3, "ring depth");
   static_assert(tc_smem_bytes(BN) <= kSmemLimit, "shared memory per CTA");
 
   extern __shared__ uint8_t smem_raw[];
@@ -285,9 +283,13 @@ __global__ void __launch_bounds__(tc_threads(kCopy), 1)
             ok = false;
             break;
           }
-          if (has_copy && !wait_bounded(ptx::smem_u32(&full_copy[stage]), phase, ctl, SITE_MMA_FULL)) {
-            ok = false;
-            break;
+          if (has_copy) {
+            if (!wait_bounded(ptx::smem_u32(&full_copy[stage]), phase, ctl, SITE_MMA_FULL)) {
+              ok = false;
+              break;
+            }
+            // the copies wrote through the generic proxy; the MMA reads through the async one
+            ptx::fence_proxy_async_smem();
           }
           ptx::tc_fence_after_sync();
           const uint32_t a0 = ptx::smem_u32(sA + stage * A_BYTES);
@@ -354,7 +356,8 @@ __global__ void __launch_bounds__(tc_threads(kCopy), 1)
                       args.M, args.N, args.K, args.a_copy, args.b_copy};
     const uint32_t sA_u = ptx::smem_u32(sA), sB_u = ptx::smem_u32(sB);
     if (has_copy && !args.inject_fault) {
-      int stage = 0, pending = 0;
+      const bool sync_arrive = ops.a_copy == 2 || ops.b_copy == 2;
+      int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
@@ -367,13 +370,16 @@ __global__ void __launch_bounds__(tc_threads(kCopy), 1)
           }
           if (ops.a_copy) copy_a_dispatch(sA_u + stage * A_BYTES, ops, mb * kTileM, kb * kTileK, ct);
           if (ops.b_copy) copy_b_dispatch<BN>(sB_u + stage * B_BYTES, ops, kb * kTileK, nb * BN, ct);
-          ptx::cp_async_commit();
-          if (pending == LAG) {
-            ptx::cp_async_wait<LAG>();
+          const uint32_t fb = ptx::smem_u32(&full_copy[stage]);
+          if (sync_arrive) {
+            // 2-byte granules are plain stores: finish every copy, then arrive
+            ptx::cp_async_commit();
+            ptx::cp_async_wait<0>();
             ptx::fence_proxy_async_smem();
-            ptx::mbar_arrive(ptx::smem_u32(&full_copy[(stage + STAGES - LAG) % STAGES]));
+            ptx::mbar_arrive(fb);
           } else {
-            ++pending;
+            // the stage's arrival fires by itself once this thread's copies land
+            ptx::cp_async_mbar_arrive_noinc(fb);
           }
           if (++stage == STAGES) {
             stage = 0;
@@ -381,10 +387,9 @@ __global__ void __launch_bounds__(tc_threads(kCopy), 1)
           }
         }
       }
+      // no copy may still be writing shared memory when the CTA exits
+      ptx::cp_async_commit();
       ptx::cp_async_wait<0>();
-      ptx::fence_proxy_async_smem();
-      if (ok)
-        for (int j = pending; j >= 1; --j) ptx::mbar_arrive(ptx::smem_u32(&full_copy[(stage + STAGES - j) % STAGES]));
     }
   }
 
