@@ -185,8 +185,9 @@ def test_pair_planning(tg):
     assert p.cta_group == 1 and p.tile_m == 128
     st, p = plan(tg, 300, 520, 200, dtype=2, cta_group=2, tile_n=224)
     assert st == tg.OK and (p.tiles_m, p.tiles_n, p.ctas) == (2, 3, 12)
-    # pairs need bulk-tensor operands and a pair width
-    assert plan(tg, 1000, 1500, 4096, dtype=2, cta_group=2)[0] == tg.ERR_INVALID_VALUE
+    # pairs need bulk-tensor A rows and a pair width; B rows that are not
+    # 16-byte aligned go to the pair kernel that copies B per thread
+    assert plan(tg, 1000, 1500, 4096, dtype=2, cta_group=2, A=A0 + 8)[0] == tg.ERR_INVALID_VALUE
     assert plan(tg, 512, 512, 512, dtype=2, cta_group=2, tile_n=64)[0] == tg.ERR_INVALID_VALUE
     assert plan(tg, 512, 512, 512, dtype=2, cta_group=3)[0] == tg.ERR_INVALID_VALUE
     st, p = plan(tg, 1100, 1300, 330, lda=336, ldb=1304, dtype=3, cta_group=2, tile_n=256, max_ctas=6)
@@ -195,6 +196,30 @@ def test_pair_planning(tg):
     assert st == tg.OK and p.tile_k == 128 and p.stages == 3 and p.smem_bytes <= 232448
     assert plan(tg, 4096, 4096, 4096, dtype=3, cta_group=1, tile_k=128)[0] == tg.ERR_INVALID_VALUE
     assert plan(tg, 4096, 4096, 4096, dtype=3, tile_k=96)[0] == tg.ERR_INVALID_VALUE
+
+
+def test_copy_pair_planning(tg):
+    """B rows that rule out bulk-tensor copies (3000-byte pitch) with bulk-tensor
+    A rows: CTA pairs, each copying half of the tile's B columns per thread."""
+    st, p = plan(tg, 1000, 1500, 4096, dtype=2, sms=152)
+    assert st == tg.OK and p.kernel == tg.KERNEL_TC_COPY and p.cta_group == 2 and p.cluster_ctas == 2
+    assert (p.tile_m, p.tile_n, p.tiles_m, p.tiles_n, p.ctas) == (256, 128, 4, 12, 96)
+    assert (p.a_copy_bytes, p.b_copy_bytes, p.store_bytes, p.tile_k) == (0, 8, 8, 64)
+    assert p.smem_bytes <= 232448 and p.stages >= 3
+    # forced: the one-SM copy kernel stays reachable, the pair takes 128 or 256 only
+    st, p = plan(tg, 1000, 1500, 4096, dtype=2, cta_group=1)
+    assert st == tg.OK and p.cta_group == 1 and p.kernel == tg.KERNEL_TC_COPY
+    st, p = plan(tg, 1000, 1500, 4096, dtype=2, cta_group=2, tile_n=256)
+    assert st == tg.OK and (p.tile_n, p.tiles_n, p.ctas) == (256, 6, 48)
+    assert plan(tg, 1000, 1500, 4096, dtype=2, cta_group=2, tile_n=192)[0] == tg.ERR_INVALID_VALUE
+    assert plan(tg, 1000, 1500, 4096, dtype=2, cta_group=2, tile_k=128)[0] == tg.ERR_INVALID_VALUE
+    assert plan(tg, 1000, 1500, 4096, dtype=2, cta_group=2, store_mode=1)[0] == tg.ERR_INVALID_VALUE
+    # aligned operands forced through copies in pairs: A keeps bulk-tensor loads
+    st, p = plan(tg, 512, 512, 512, dtype=2, kernel=tg.KERNEL_TC_COPY, cta_group=2, tile_n=128)
+    assert st == tg.OK and p.cta_group == 2 and (p.a_copy_bytes, p.b_copy_bytes) == (0, 16) and p.store_bytes != 0
+    # a CTA cap bounds the pairs
+    st, p = plan(tg, 1000, 1500, 4096, dtype=2, cta_group=2, max_ctas=10)
+    assert st == tg.OK and p.ctas == 10
 
 
 def test_tuned_shape_table(tg):

@@ -40,6 +40,7 @@ PATHS = {
     "multicast_clusters": {"multicast": 2},
     "one_sm": {"cta_group": 1},
     "one_sm_copy_producers": {"kernel": 2},
+    "pairs_copy_producers": {"kernel": 2, "cta_group": 2},
 }
 
 
@@ -85,6 +86,13 @@ def test_epilogue_every_tensor_core_path(dtype, path, epi_name):
         assert res.plan.swap_ab == 1
     if path == "multicast_clusters":
         assert res.plan.cluster_ctas == 4
+
+
+@pytest.mark.parametrize("epi_name", list(EPILOGUES))
+def test_epilogue_copy_pairs_unaligned_rows(epi_name):
+    """B rows of 1048 bytes (8-byte granules): CTA pairs copying B per thread."""
+    res = run_case(300, 520, 200, wl.BF16, epi_name, {"cta_group": 2}, seed=81, ldb=524)
+    assert res.plan.cta_group == 2 and res.plan.kernel == 2 and res.plan.b_copy_bytes == 8
 
 
 @pytest.mark.parametrize("epi_name", list(EPILOGUES))

@@ -103,6 +103,46 @@ def test_copy_producer_on_aligned_rows(tile_n, dtype):
     H.check_full(res, A, B, M, N, K, dtype, f"copy tile_n {tile_n}")
 
 
+# ------------------------------------------- CTA pairs copying B per thread
+
+@pytest.mark.parametrize("ldb,b_off,granule", [(300, 0, 8), (302, 0, 4), (301, 0, 2), (304, 8, 8)],
+                         ids=["pitch600", "pitch604", "pitch602", "base_plus_8"])
+@pytest.mark.parametrize("tile_n", [128, 256])
+@pytest.mark.parametrize("dtype", [wl.BF16, wl.F16_F32OUT], ids=lambda d: wl.DTYPE_NAMES[d])
+def test_copy_pair_kernel(tile_n, dtype, ldb, b_off, granule):
+    """B rows off the 16-byte grid, A rows on it: CTA pairs whose CTAs copy
+    their halves of B per thread.  Ragged M (the third pair tile has 8 rows),
+    ragged N and a K tail, for each copy granule."""
+    M, N, K = 520, 300, 200
+    A, B, res = case(M, N, K, dtype, seed=26, lda=208, ldb=ldb, b_off=b_off,
+                     options={"cta_group": 2, "tile_n": tile_n})
+    p = res.plan
+    assert (p.kernel, p.cta_group, p.tile_n, p.a_copy_bytes, p.b_copy_bytes) == (2, 2, tile_n, 0, granule)
+    H.check_full(res, A, B, M, N, K, dtype, f"copy pair {tile_n} ldb {ldb}+{b_off}")
+
+
+@pytest.mark.parametrize("tile_n", [128, 256])
+def test_copy_pair_forced_on_aligned_rows(tile_n):
+    """kernel = copy with cta_group = 2 on aligned rows: 16-byte copies of B,
+    bulk-tensor loads of A, per-thread stores of C."""
+    M, N, K = 600, 392, 328
+    A, B, res = case(M, N, K, wl.BF16, seed=27, lda=336, ldb=392, ldc=400,
+                     options={"kernel": 2, "cta_group": 2, "tile_n": tile_n})
+    assert (res.plan.cta_group, res.plan.a_copy_bytes, res.plan.b_copy_bytes) == (2, 0, 16)
+    H.check_full(res, A, B, M, N, K, wl.BF16, f"copy pair aligned {tile_n}")
+
+
+@pytest.mark.parametrize("max_ctas,group_m", [(4, 1), (6, 3), (2, 2)])
+def test_copy_pair_persistent(max_ctas, group_m):
+    """Few pairs walking many tiles: every ring and accumulator phase turns
+    over many times (1100 x 700 in 256 x 128 tiles = 30 tiles)."""
+    M, N, K = 1100, 700, 264
+    A, B, res = case(M, N, K, wl.BF16, seed=28, lda=264, ldb=700, ldc=700,
+                     options={"cta_group": 2, "tile_n": 128, "max_ctas": max_ctas, "group_m": group_m})
+    assert res.plan.cta_group == 2 and res.plan.ctas == max_ctas and res.plan.b_copy_bytes == 8
+    H.check_full(res, A, B, M, N, K, wl.BF16, f"copy pair persistent {max_ctas}")
+
+
 @pytest.mark.parametrize("offsets", [(2, 0, 0), (4, 4, 4), (8, 8, 8), (0, 2, 2), (6, 10, 12)])
 @pytest.mark.parametrize("dtype", [wl.BF16, wl.F16], ids=lambda d: wl.DTYPE_NAMES[d])
 def test_misaligned_pointers(offsets, dtype):

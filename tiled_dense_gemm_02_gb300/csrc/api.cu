@@ -110,6 +110,7 @@ struct Plan {
   bool noop = false, zero = false;
   bool pair = false;
   bool swap = false;  // pair kernel with the MMA's operands exchanged (tile tm x 256)
+  bool copy_pair = false;  // pair kernel with B staged by per-thread copies (A by bulk-tensor copies)
   int tm = 0;         // tile height of the swapped kernel
   int cluster = 2;  // CTAs per cluster of the pair kernel: 2, or 4 (two pairs sharing B)
   int ksub = 1;  // 64-deep K sub-blocks per shared-memory stage (pair kernel)
@@ -267,6 +268,9 @@ int make_plan_core(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, 
 int make_plan(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb,
               const void* C, int64_t ldc, int dtype, const tgemm_options* o, int sms, int pair_cap, int quad_cap,
               int64_t workspace_bytes, Plan& p, int64_t batch = 1) {
+  // every plan starts from the defaults: a Plan filled by an earlier call (the
+  // device-free validation pass of run(), say) must not leak its choices
+  p = Plan();
   tgemm_options opt;
   std::memset(&opt, 0, sizeof opt);
   if (o) opt = *o;
@@ -380,6 +384,54 @@ int make_plan_core(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, 
     sms = std::min(sms, opt.max_ctas);
     pair_cap = std::min(pair_cap, std::max(1, opt.max_ctas / 2));
     quad_cap = std::min(quad_cap, opt.max_ctas / 4);
+  }
+  // B rows that rule out bulk-tensor copies (A's do not): CTA pairs that copy
+  // B per thread, each CTA its half of the tile's columns, move half the B
+  // bytes per SM and FLOP of the one-SM copy kernel, which per-thread copies
+  // bound.  Cost: rounds x the B columns one SM copies per tile.
+  const bool copy_pair_ok = p.kernel == TGEMM_KERNEL_TC_COPY && a_tma && pair_cap > 0 &&
+                            opt.cta_group != 1 && opt.stream_k != 2 && opt.multicast != 2 && opt.swap_ab != 2 &&
+                            opt.tile_k != 128 && opt.store_mode != 1 &&
+                            (opt.tile_n == 0 || opt.tile_n == 128 || opt.tile_n == 256) &&
+                            (opt.kernel == TGEMM_KERNEL_TC_COPY ? opt.cta_group == 2 : p.b_copy != 0);
+  if (copy_pair_ok) {
+    auto rounds = [&](int64_t tiles, int workers) { return static_cast<double>((tiles + workers - 1) / workers); };
+    int bnc = 0;
+    double cost_c = 1e300;
+    for (int bn : {256, 128}) {
+      if (opt.tile_n && bn != opt.tile_n) continue;
+      const double c = rounds(((M + 2 * kTileM - 1) / (2 * kTileM)) * ((N + bn - 1) / bn), pair_cap) * bn / 2;
+      if (c < cost_c * 0.999) {
+        cost_c = c;
+        bnc = bn;
+      }
+    }
+    double cost_1 = 1e300;
+    for (int bn : {256, 128, 64})
+      cost_1 = std::min(cost_1, rounds(((M + kTileM - 1) / kTileM) * ((N + bn - 1) / bn), sms) * bn);
+    if (opt.cta_group == 2 || cost_c < cost_1) {
+      p.pair = true;
+      p.copy_pair = true;
+      p.bn = bnc;
+      p.a_copy = 0;
+      p.b_copy = gb;
+      p.store = gc;  // the kernel stores C per thread
+      p.ksub = 1;
+      p.stages = copy_pair_stage_count(p.bn);
+      p.tiles_m = static_cast<int>((M + 2 * kTileM - 1) / (2 * kTileM));
+      p.tiles_n = static_cast<int>((N + p.bn - 1) / p.bn);
+      const int64_t tiles = int64_t(p.tiles_m) * p.tiles_n;
+      if (tiles >= (int64_t(1) << 31)) return TGEMM_ERR_TOO_LARGE;
+      const int64_t in_bytes = (M * K + K * N) * 2;
+      p.group_m = opt.group_m ? opt.group_m : (in_bytes <= (int64_t(64) << 20) ? 4 : 8);
+      p.group_m = std::max(1, std::min(p.group_m, p.tiles_m));
+      p.k_blocks = static_cast<int>((K + kTileK - 1) / kTileK);
+      p.dp_tiles = static_cast<int>(tiles);
+      p.ctas = static_cast<int>(2 * std::min<int64_t>(tiles, pair_cap));
+      p.smem = copy_pair_smem(p.bn);
+      if (batch > 1) p.batch_loop = true;
+      return TGEMM_OK;
+    }
   }
   // one SM per 128-row tile, or a CTA pair per 256-row tile (bulk-tensor
   // operands only)
@@ -780,7 +832,9 @@ int run(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void*
   const int to_us = (o && o->wait_timeout_us) ? o->wait_timeout_us : 2000000;
   a.timeout_ns = static_cast<unsigned long long>(to_us) * 1000ull;
   a.status = dev->status;
-  if (p.swap)
+  if (p.copy_pair)
+    e = launch_tc_pair_copy(p.bn, mA, a, p.ctas / 2, stream);
+  else if (p.swap)
     e = launch_tc_pair_swap(p.tm, p.ksub, mA, mB, mC, a, p.ctas / 2, stream);
   else if (p.pair)
     e = launch_tc_pair(p.bn, p.store == 0, p.ksub, p.cluster, mA, mB, mBt, mC, a, p.ctas / p.cluster, stream);

@@ -1,6 +1,7 @@
 // Device helpers shared by the tensor-core kernels: bounded mbarrier waits,
 // the tile scheduler's tile -> (m, n) map, shared-memory matrix descriptors of
-// tcgen05, the 128-byte swizzle, and epilogue conversion/store routines.
+// tcgen05, the 128-byte swizzle, the per-thread copy producers that write the
+// swizzled operand layout, and epilogue conversion/store routines.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -66,6 +67,117 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uin
 // 16-byte chunk index XOR (row mod 8).
 __device__ __forceinline__ uint32_t sw128_offset(int r, int cb) {
   return static_cast<uint32_t>(r * 128 + ((((cb >> 4) ^ (r & 7)) << 4) | (cb & 15)));
+}
+
+// ---------------------------------------------------------- copy producers
+// Every operand of these loops arrives as a value, so the pointers, leading
+// dimensions and extents stay in registers across the copy instructions
+// (read from the kernel's argument block inside the loop, they would be
+// fetched again after every copy).  A thread issues ITERS copies per stage;
+// where the number of granules per tile row divides the thread count, each
+// thread keeps one column granule and walks rows a fixed distance apart.
+
+// A tile: rows m0..m0+127, k0..k0+63 of row-major A -> K-major swizzled rows.
+template <int G>
+__device__ __forceinline__ void copy_a_tile(uint32_t sa, const uint16_t* __restrict__ A, int64_t lda, int M, int K,
+                                            int m0, int k0, int ct) {
+  constexpr int PER_ROW = 128 / G;  // granules per 64-element row
+  constexpr int STEP = kCopyWarps * 32;
+  constexpr int RS = STEP / PER_ROW;  // rows between a thread's copies
+  constexpr int ITERS = kTileM / RS;
+  static_assert(STEP % PER_ROW == 0, "copy layout");
+  const int cb = (ct % PER_ROW) * G, r0 = ct / PER_ROW;
+  const int gk = k0 + cb / 2;
+  const int vcol = max(0, min(G / 2, K - gk));
+  const uint16_t* src = A + static_cast<int64_t>(m0 + r0) * lda + gk;
+  const int64_t step = RS * lda;
+#pragma unroll 8
+  for (int j = 0; j < ITERS; ++j) {
+    const int r = r0 + j * RS;
+    const int valid = m0 + r < M ? vcol : 0;
+    const uint32_t off = sw128_offset(r, cb);
+    if constexpr (G >= 4) {
+      ptx::cp_async<G>(sa + off, valid ? src : A, static_cast<uint32_t>(valid * 2));
+    } else {
+      ptx::st_shared_u16(sa + off, valid ? *src : uint16_t(0));
+    }
+    src += step;
+  }
+}
+
+// B tile: rows k0..k0+63, columns n0..n0+BN-1 of row-major B -> N-major
+// swizzled atoms of 64 columns (8 KB each).
+template <int G, int BN>
+__device__ __forceinline__ void copy_b_tile(uint32_t sb, const uint16_t* __restrict__ B, int64_t ldb, int K, int N,
+                                            int k0, int n0, int ct) {
+  constexpr int PER_ROW = BN * 2 / G;  // granules per k-row of the tile
+  constexpr int STEP = kCopyWarps * 32;
+  constexpr int ITERS = kTileK * PER_ROW / STEP;
+  static_assert(kTileK * PER_ROW % STEP == 0, "copy layout");
+  if constexpr (STEP % PER_ROW == 0) {
+    constexpr int RS = STEP / PER_ROW;
+    const int cb = (ct % PER_ROW) * G, r0 = ct / PER_ROW;
+    const int gn = n0 + cb / 2;
+    const int vcol = max(0, min(G / 2, N - gn));
+    const uint32_t atom = sb + static_cast<uint32_t>((cb >> 7) * 8192);
+    const uint16_t* src = B + static_cast<int64_t>(k0 + r0) * ldb + gn;
+    const int64_t step = RS * ldb;
+#pragma unroll 8
+    for (int j = 0; j < ITERS; ++j) {
+      const int r = r0 + j * RS;
+      const int valid = k0 + r < K ? vcol : 0;
+      const uint32_t off = sw128_offset(r, cb & 127);
+      if constexpr (G >= 4) {
+        ptx::cp_async<G>(atom + off, valid ? src : B, static_cast<uint32_t>(valid * 2));
+      } else {
+        ptx::st_shared_u16(atom + off, valid ? *src : uint16_t(0));
+      }
+      src += step;
+    }
+  } else {
+#pragma unroll 4
+    for (int j = 0; j < ITERS; ++j) {
+      const int idx = ct + j * STEP;
+      const int r = idx / PER_ROW, cb = (idx % PER_ROW) * G;
+      const int gk = k0 + r, gn = n0 + cb / 2;
+      const int valid = gk < K ? max(0, min(G / 2, N - gn)) : 0;
+      const uint16_t* src = valid ? B + static_cast<int64_t>(gk) * ldb + gn : B;
+      const uint32_t off = static_cast<uint32_t>((cb >> 7) * 8192) + sw128_offset(r, cb & 127);
+      if constexpr (G >= 4) {
+        ptx::cp_async<G>(sb + off, src, static_cast<uint32_t>(valid * 2));
+      } else {
+        ptx::st_shared_u16(sb + off, valid ? *src : uint16_t(0));
+      }
+    }
+  }
+}
+
+// The copy side of one stage, with the operands already in registers.
+struct CopyOps {
+  const uint16_t* A;
+  const uint16_t* B;
+  int64_t lda, ldb;
+  int M, N, K;
+  int a_copy, b_copy;  // granule in bytes, 0 = not copied per thread
+};
+
+__device__ __forceinline__ void copy_a_dispatch(uint32_t sa, const CopyOps& o, int m0, int k0, int ct) {
+  switch (o.a_copy) {
+    case 16: copy_a_tile<16>(sa, o.A, o.lda, o.M, o.K, m0, k0, ct); break;
+    case 8: copy_a_tile<8>(sa, o.A, o.lda, o.M, o.K, m0, k0, ct); break;
+    case 4: copy_a_tile<4>(sa, o.A, o.lda, o.M, o.K, m0, k0, ct); break;
+    default: copy_a_tile<2>(sa, o.A, o.lda, o.M, o.K, m0, k0, ct); break;
+  }
+}
+
+template <int BN>
+__device__ __forceinline__ void copy_b_dispatch(uint32_t sb, const CopyOps& o, int k0, int n0, int ct) {
+  switch (o.b_copy) {
+    case 16: copy_b_tile<16, BN>(sb, o.B, o.ldb, o.K, o.N, k0, n0, ct); break;
+    case 8: copy_b_tile<8, BN>(sb, o.B, o.ldb, o.K, o.N, k0, n0, ct); break;
+    case 4: copy_b_tile<4, BN>(sb, o.B, o.ldb, o.K, o.N, k0, n0, ct); break;
+    default: copy_b_tile<2, BN>(sb, o.B, o.ldb, o.K, o.N, k0, n0, ct); break;
+  }
 }
 
 // ------------------------------------------------------------- epilogue

@@ -156,6 +156,11 @@ constexpr int tc2_smem_bytes(int bn, bool staged, int ksub = 1) {
   return 1024 + tc2_stages(bn, staged, ksub) * tc2_stage_bytes(bn, ksub) + tc2_epi_bytes(staged) + kBarrierBytes;
 }
 
+// CTA-pair kernel with B staged by per-thread copies (tile 256 x bn, bn 128
+// or 256): its ring depth and shared memory per CTA.
+int copy_pair_stage_count(int bn);
+int copy_pair_smem(int bn);
+
 // Launchers (return the cudaError_t of the launch).
 cudaError_t launch_tc(int bn, bool copy, const CUtensorMap& mapA, const CUtensorMap& mapB, const CUtensorMap& mapC,
                       const TcArgs& args, int ctas, cudaStream_t stream);
@@ -171,6 +176,7 @@ cudaError_t launch_tc_pair(int bn, bool staged, int ksub, int cluster, const CUt
 // M along C's columns, its N = tm along C's rows).  The maps are 3-D (matrix
 // index last, extent 1 for an operand whose batch stride is 0): mapA's box is
 // tm/2 rows of A, mapB's 64 columns x 64 k, mapC's an unswizzled 32 x 32 block.
+cudaError_t launch_tc_pair_copy(int bn, const CUtensorMap& mapA, const TcArgs& args, int pairs, cudaStream_t stream);
 cudaError_t launch_tc_pair_swap(int tm, int ksub, const CUtensorMap& mapA, const CUtensorMap& mapB,
                                 const CUtensorMap& mapC, const TcArgs& args, int pairs, cudaStream_t stream);
 // Number of clusters of `cluster` CTAs (2 or 4) of the pair kernel that can be
