@@ -357,6 +357,44 @@ TGEMM_API int tgemm_transpose(int64_t rows, int64_t cols,
                void* dst, int64_t ld_dst,
                int elem_bytes, void* stream);
 
+/*
+ * The product with A, B and C in host memory (the pages have no counterpart:
+ * this serves callers whose data lives on the host).  The library copies B
+ * and row panels of A into caller-owned device buffers, multiplies each panel
+ * as soon as its rows have arrived, and copies each panel of C back while the
+ * next one is computed, so host-to-device copies, kernels and
+ * device-to-host copies of different panels overlap.
+ *
+ *   C_host[i * ldc + j] = sum_k A_host[i * lda + k] * B_host[k * ldb + j]
+ *
+ * A_host, B_host, C_host: host memory, row-major with the given leading
+ *   dimensions (elements, as in tgemm_gemm).  Page-locked memory
+ *   (cudaHostAlloc / cudaHostRegister) lets the copies run asynchronously and
+ *   overlap; pageable memory gives the same result, but each copy then blocks
+ *   the calling thread.  Elements of C_host past N in each row are not written.
+ * dA, dB, dC: device buffers owned by the caller, at least M*K, K*N and M*N
+ *   elements, used densely (row pitches K, N and N).  Afterwards dC holds the
+ *   product; dA and dB hold the copied operands.  They must not overlap.
+ * panels: row panels of A and C (0 = chosen by the library; 1 = no overlap).
+ * stream: everything the call does follows the work already enqueued on
+ *   `stream`, and later work on `stream` follows all of it, including the
+ *   copy of C to the host.  The call returns once the work is enqueued:
+ *   synchronise `stream` before reading C_host.  The copies run on two
+ *   streams per device that the library creates on first use and keeps;
+ *   ordering with `stream` is by events, created and released per call.
+ * Errors: as tgemm_gemm for the product (M, N, K, dtype, leading dimensions);
+ *   TGEMM_ERR_INVALID_VALUE for a null buffer with a nonzero extent or
+ *   panels < 0, TGEMM_ERR_MISALIGNED for a pointer not aligned to its element
+ *   size, TGEMM_ERR_ALIAS for overlapping device buffers.  Argument errors are
+ *   returned before any CUDA call.
+ */
+TGEMM_API int tgemm_gemm_host(int64_t M, int64_t N, int64_t K,
+               const void* A_host, int64_t lda,
+               const void* B_host, int64_t ldb,
+               void* C_host, int64_t ldc,
+               int dtype, void* dA, void* dB, void* dC,
+               int panels, void* stream);
+
 /* Waits for `stream`, then returns and clears the device-side status word
  * that bounded in-kernel waits set when they give up (TGEMM_OK or
  * TGEMM_ERR_DEVICE_TIMEOUT).  A CUDA error while synchronising returns

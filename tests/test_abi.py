@@ -31,8 +31,8 @@ def test_header_declares_the_abi():
     names = declared_functions()
     assert names == sorted(["tgemm_gemm", "tgemm_gemm_ex", "tgemm_gemm_ws", "tgemm_workspace_size", "tgemm_plan",
                             "tgemm_gemm_noalloc", "tgemm_gemm_epilogue", "tgemm_gemm_batched",
-                            "tgemm_plan_batched", "tgemm_transpose", "tgemm_device_status", "tgemm_status_string",
-                            "tgemm_version"])
+                            "tgemm_plan_batched", "tgemm_transpose", "tgemm_gemm_host", "tgemm_device_status",
+                            "tgemm_status_string", "tgemm_version"])
 
 
 def test_library_exports_every_declared_symbol(tg):
@@ -306,6 +306,29 @@ def test_transpose_validation_returns_before_the_device(tg):
     assert tg.transpose(4, 4, 0, 4, D, 4, 4) == tg.ERR_INVALID_VALUE
     assert tg.transpose(0, 4, S, 4, D, 1, 4) == tg.OK
     assert tg.transpose(1 << 31, 4, S, 4, D, 1 << 31, 2) == tg.ERR_TOO_LARGE
+
+
+def test_gemm_host_validation_returns_before_the_device(tg):
+    """Argument errors of the host-buffer product come back before any CUDA
+    call (this machine has no GPU, so a call that reached CUDA would fail
+    with ERR_LAUNCH or ERR_UNSUPPORTED_DEVICE instead)."""
+    AH, BH, CH = 0x7000_0000, 0x7100_0000, 0x7200_0000
+    DA, DB, DC = 0x1000_0000, 0x2000_0000, 0x3000_0000
+    g = tg.gemm_host
+    assert g(-1, 4, 4, AH, 4, BH, 4, CH, 4, 2, DA, DB, DC) == tg.ERR_INVALID_VALUE
+    assert g(4, 4, 4, AH, 3, BH, 4, CH, 4, 2, DA, DB, DC) == tg.ERR_INVALID_VALUE       # lda < K
+    assert g(4, 4, 4, AH, 4, BH, 4, CH, 3, 2, DA, DB, DC) == tg.ERR_INVALID_VALUE       # ldc < N
+    assert g(4, 4, 4, AH, 4, BH, 4, CH, 4, 9, DA, DB, DC) == tg.ERR_UNSUPPORTED_DTYPE
+    assert g(4, 4, 4, AH, 4, BH, 4, CH, 4, 2, DA, DB, DC, panels=-1) == tg.ERR_INVALID_VALUE
+    assert g(4, 4, 4, 0, 4, BH, 4, CH, 4, 2, DA, DB, DC) == tg.ERR_INVALID_VALUE        # no A
+    assert g(4, 4, 4, AH, 4, BH, 4, CH, 4, 2, DA, 0, DC) == tg.ERR_INVALID_VALUE        # no device B
+    assert g(4, 4, 4, AH, 4, BH, 4, CH, 4, 2, DA, DB, 0) == tg.ERR_INVALID_VALUE        # no device C
+    assert g(4, 4, 4, AH + 1, 4, BH, 4, CH, 4, 2, DA, DB, DC) == tg.ERR_MISALIGNED
+    assert g(4, 4, 4, AH, 4, BH, 4, CH, 4, 0, DA, DB, DC + 2) == tg.ERR_MISALIGNED      # fp32 C
+    assert g(64, 64, 64, AH, 64, BH, 64, CH, 64, 2, DA, DA + 64 * 64, DC) == tg.ERR_ALIAS   # dB inside dA
+    assert g(64, 64, 64, AH, 64, BH, 64, CH, 64, 3, DA, DB, DB + 8) == tg.ERR_ALIAS         # dC over dB
+    assert g(0, 4, 4, AH, 4, BH, 4, CH, 4, 2, DA, DB, DC) == tg.OK                      # empty: nothing to do
+    assert g(1 << 31, 4, 4, AH, 4, BH, 4, CH, 4, 2, DA, DB, DC) == tg.ERR_TOO_LARGE
 
 
 def test_two_pair_cluster_planning(tg):

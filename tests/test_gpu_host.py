@@ -1,0 +1,95 @@
+"""GPU parity of tgemm_gemm_host: A, B and C in host memory (page-locked or
+pageable), copied in row panels through caller-owned device buffers, against
+the oracle.  Padding columns of C's host rows (ldc > N) must keep their
+canary, and a second call that reuses the device buffers must see its own
+inputs (the call's copies follow the work already on the stream).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as wl
+from tests import gpu_harness as H
+from tests import tolerance
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    H.tg()
+    torch.cuda.set_device(0)
+
+
+def host_buffer(bits: np.ndarray, pinned: bool):
+    """A host copy of `bits` (pinned torch tensor or plain numpy array) and its address."""
+    if pinned:
+        t = torch.from_numpy(np.ascontiguousarray(bits)).pin_memory()
+        return t, t.data_ptr()
+    a = np.ascontiguousarray(bits).copy()
+    return a, a.ctypes.data
+
+
+def run_host(M, N, K, dtype, seed, lda=None, ldb=None, ldc=None, panels=0, pinned=True, dev_bufs=None):
+    lib = H.tg()
+    dev = torch.device("cuda:0")
+    fin, fout = wl.IN_FORMAT[dtype], wl.OUT_FORMAT[dtype]
+    ldc = N if ldc is None else ldc
+    if K > 0:
+        A, B = wl.make_inputs(wl.Workload("host", M, N, K, dtype, "uniform", seed), lda=lda, ldb=ldb)
+    else:
+        A = np.zeros((M, 1), dtype=H.NP_BITS[fin])
+        B = np.zeros((1, N), dtype=H.NP_BITS[fin])
+    a_h, a_ptr = host_buffer(A, pinned)
+    b_h, b_ptr = host_buffer(B, pinned)
+    c_init = np.full((M, ldc), H.CANARY[fout], dtype=H.NP_BITS[fout])
+    c_h, c_ptr = host_buffer(c_init, pinned)
+    ei, eo = wl.FORMATS[fin][3], wl.FORMATS[fout][3]
+    if dev_bufs is None:
+        dev_bufs = [torch.empty(max(n, 1) * e, dtype=torch.uint8, device=dev)
+                    for n, e in ((M * K, ei), (K * N, ei), (M * N, eo))]
+    dA, dB, dC = dev_bufs
+    stream = torch.cuda.current_stream(dev).cuda_stream
+    st = lib.gemm_host(M, N, K, a_ptr, A.shape[1], b_ptr, B.shape[1], c_ptr, ldc, dtype,
+                       dA.data_ptr(), dB.data_ptr(), dC.data_ptr(), panels, stream)
+    assert st == lib.OK, lib.status_string(st)
+    torch.cuda.synchronize()
+    assert lib.device_status(stream) == lib.OK
+    raw = (c_h.numpy() if pinned else c_h).view(H.NP_BITS[fout]).reshape(M, ldc)
+    assert np.all(raw[:, N:] == H.CANARY[fout]), "a padding element of C's host rows was written"
+    got = wl.decode(np.ascontiguousarray(raw[:, :N]), fout)
+    if K > 0:
+        D, S = oracle.gemm(np.ascontiguousarray(A), np.ascontiguousarray(B), fin, M, N, K)
+    else:
+        D, S = np.zeros((M, N)), np.zeros((M, N))
+    ok, ratio, where = tolerance.check(got, D, S, fin, fout)
+    assert ok, f"{M}x{N}x{K} {wl.DTYPE_NAMES[dtype]} panels {panels}: error/bound {ratio:.3g} at {where}"
+    return dev_bufs
+
+
+@pytest.mark.parametrize("panels", [0, 1, 3])
+def test_ragged_product_from_host(panels):
+    """The ragged 1000 x 1500 x 4096 bf16 product (3000-byte rows) from pinned memory."""
+    run_host(1000, 1500, 4096, wl.BF16, seed=90, panels=panels)
+
+
+@pytest.mark.parametrize("dtype", [wl.F16, wl.BF16_F32OUT, wl.F32], ids=lambda d: wl.DTYPE_NAMES[d])
+def test_padded_host_rows(dtype):
+    """Leading dimensions above the extents on the host side; the device copies are dense."""
+    run_host(300, 520, 200, dtype, seed=91, lda=208, ldb=530, ldc=533, panels=3)
+
+
+def test_pageable_host_memory():
+    run_host(513, 300, 1000, wl.BF16, seed=92, pinned=False, panels=2)
+
+
+def test_k_zero_from_host():
+    run_host(130, 70, 0, wl.BF16, seed=93)
+
+
+def test_reused_device_buffers_see_each_calls_inputs():
+    bufs = run_host(700, 400, 300, wl.BF16, seed=94, panels=2)
+    run_host(700, 400, 300, wl.BF16, seed=95, panels=4, dev_bufs=bufs)

@@ -28,7 +28,7 @@ ACT_NONE, ACT_RELU = 0, 1
 
 EXPORTS = ("tgemm_gemm", "tgemm_gemm_ex", "tgemm_gemm_ws", "tgemm_workspace_size", "tgemm_plan",
            "tgemm_gemm_noalloc", "tgemm_gemm_epilogue", "tgemm_gemm_batched", "tgemm_plan_batched",
-           "tgemm_transpose", "tgemm_device_status", "tgemm_status_string", "tgemm_version")
+           "tgemm_transpose", "tgemm_gemm_host", "tgemm_device_status", "tgemm_status_string", "tgemm_version")
 # bytes of the scratch array built into the library (TGEMM_NOALLOC_SCRATCH_BYTES)
 NOALLOC_SCRATCH_BYTES = 20 * 1024 * 1024 + 4096
 
@@ -101,6 +101,8 @@ def _load():
     lib.tgemm_plan_batched.restype = ip
     lib.tgemm_transpose.argtypes = [i64, i64, vp, i64, vp, i64, ip, vp]
     lib.tgemm_transpose.restype = ip
+    lib.tgemm_gemm_host.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, ip, vp, vp, vp, ip, vp]
+    lib.tgemm_gemm_host.restype = ip
     lib.tgemm_device_status.argtypes = [vp]
     lib.tgemm_device_status.restype = ip
     lib.tgemm_status_string.argtypes = [ip]
@@ -191,6 +193,12 @@ def plan_batched(batch, M, N, K, A, lda, stride_a, B, ldb, stride_b, C, ldc, str
 def transpose(rows, cols, src, ld_src, dst, ld_dst, elem_bytes, stream=0) -> int:
     """tgemm_transpose: dst (cols x rows) = src (rows x cols) transposed."""
     return _lib.tgemm_transpose(rows, cols, src, ld_src, dst, ld_dst, elem_bytes, stream)
+
+
+def gemm_host(M, N, K, A_host, lda, B_host, ldb, C_host, ldc, dtype, dA, dB, dC, panels=0, stream=0) -> int:
+    """tgemm_gemm_host: A, B, C in host memory (pointers as ints), staged through
+    the caller's device buffers dA, dB, dC; returns the status."""
+    return _lib.tgemm_gemm_host(M, N, K, A_host, lda, B_host, ldb, C_host, ldc, dtype, dA, dB, dC, panels, stream)
 
 
 def workspace_size(M, N, K, A, lda, B, ldb, C, ldc, dtype, options=None):

@@ -13,6 +13,7 @@
 #include <cstring>
 #include <mutex>
 #include <string>
+#include <vector>
 
 #include "../../include/tgemm.h"
 #include "tgemm_internal.h"
@@ -88,6 +89,59 @@ int device_info(DeviceInfo** out) {
   *out = &d;
   return d.supported ? TGEMM_OK : TGEMM_ERR_UNSUPPORTED_DEVICE;
 }
+
+// Streams that carry tgemm_gemm_host's copies: one for host-to-device and one
+// for device-to-host per device, created on first use and kept for the life
+// of the process (guarded by g_mutex).  Non-blocking, so they never
+// synchronise implicitly with the legacy default stream; every ordering is an
+// event.
+struct CopyStreams {
+  cudaStream_t in = nullptr, out = nullptr;
+};
+CopyStreams g_copy_streams[64];
+
+int copy_streams(cudaStream_t* in, cudaStream_t* out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= 64) {
+    t_last_error = "device ordinal out of range";
+    return TGEMM_ERR_LAUNCH;
+  }
+  std::lock_guard<std::mutex> lock(g_mutex);
+  CopyStreams& c = g_copy_streams[dev];
+  for (cudaStream_t* sp : {&c.in, &c.out})
+    if (!*sp && (e = cudaStreamCreateWithFlags(sp, cudaStreamNonBlocking)) != cudaSuccess) {
+      *sp = nullptr;
+      return cuda_fail(e, "cudaStreamCreateWithFlags");
+    }
+  *in = c.in;
+  *out = c.out;
+  return TGEMM_OK;
+}
+
+// A block of `rows` rows of `width` bytes between host and device memory: one
+// linear copy when both sides are dense (the driver moves a pitched copy row
+// by row, which costs it half its rate on rows of a few KB), else pitched.
+cudaError_t copy_rows(void* dst, int64_t dpitch, const void* src, int64_t spitch, int64_t width, int64_t rows,
+                      cudaMemcpyKind kind, cudaStream_t s) {
+  if (dpitch == width && spitch == width) return cudaMemcpyAsync(dst, src, width * rows, kind, s);
+  return cudaMemcpy2DAsync(dst, dpitch, src, spitch, width, rows, kind, s);
+}
+
+// Events of one tgemm_gemm_host call, released when the call returns (a
+// recorded event that has not completed yet is released once it completes).
+struct CallEvents {
+  std::vector<cudaEvent_t> ev;
+  ~CallEvents() {
+    for (cudaEvent_t e : ev) cudaEventDestroy(e);
+  }
+  cudaError_t make(cudaEvent_t* out) {
+    const cudaError_t e = cudaEventCreateWithFlags(out, cudaEventDisableTiming);
+    if (e == cudaSuccess) ev.push_back(*out);
+    return e;
+  }
+};
 
 int in_bytes(int dtype) { return dtype == TGEMM_F32 ? 4 : 2; }
 int out_bytes(int dtype) {
@@ -978,6 +1032,97 @@ int tgemm_transpose(int64_t rows, int64_t cols, const void* src, int64_t ld_src,
   const cudaError_t e = tgemm::launch_transpose(src, ld_src, dst, ld_dst, static_cast<int>(rows), static_cast<int>(cols),
                                                 elem_bytes, vec, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? TGEMM_OK : tgemm::cuda_fail(e, "transpose launch");
+}
+
+int tgemm_gemm_host(int64_t M, int64_t N, int64_t K, const void* A_host, int64_t lda, const void* B_host, int64_t ldb,
+                    void* C_host, int64_t ldc, int dtype, void* dA, void* dB, void* dC, int panels, void* stream) {
+  using tgemm::ranges_overlap;
+  if (dtype < TGEMM_F32 || dtype > TGEMM_F16_F32OUT) return TGEMM_ERR_UNSUPPORTED_DTYPE;
+  if (M < 0 || N < 0 || K < 0 || panels < 0) return TGEMM_ERR_INVALID_VALUE;
+  if (M >= (int64_t(1) << 31) || N >= (int64_t(1) << 31) || K >= (int64_t(1) << 31)) return TGEMM_ERR_TOO_LARGE;
+  if (lda < std::max<int64_t>(1, K) || ldb < std::max<int64_t>(1, N) || ldc < std::max<int64_t>(1, N))
+    return TGEMM_ERR_INVALID_VALUE;
+  if (M == 0 || N == 0) return TGEMM_OK;
+  const int ei = tgemm::in_bytes(dtype), eo = tgemm::out_bytes(dtype);
+  if (!C_host || !dC || (K > 0 && (!A_host || !B_host || !dA || !dB))) return TGEMM_ERR_INVALID_VALUE;
+  auto misaligned = [](const void* q, int e) { return reinterpret_cast<uint64_t>(q) % e != 0; };
+  if (misaligned(C_host, eo) || misaligned(dC, eo)) return TGEMM_ERR_MISALIGNED;
+  if (K > 0 && (misaligned(A_host, ei) || misaligned(B_host, ei) || misaligned(dA, ei) || misaligned(dB, ei)))
+    return TGEMM_ERR_MISALIGNED;
+  const uint64_t c0 = reinterpret_cast<uint64_t>(dC), c1 = c0 + static_cast<uint64_t>(M * N * eo);
+  if (K > 0) {
+    const uint64_t a0 = reinterpret_cast<uint64_t>(dA), a1 = a0 + static_cast<uint64_t>(M * K * ei);
+    const uint64_t b0 = reinterpret_cast<uint64_t>(dB), b1 = b0 + static_cast<uint64_t>(K * N * ei);
+    if (ranges_overlap(a0, a1, b0, b1) || ranges_overlap(c0, c1, a0, a1) || ranges_overlap(c0, c1, b0, b1))
+      return TGEMM_ERR_ALIAS;
+  }
+  // Row panels, each a whole number of 128-row tiles, so that the copy of one
+  // panel of C back to the host overlaps the copies in and the products of the
+  // next.  What can overlap is C's copy: with C below 6 MB one panel measured
+  // as fast as several; above, about one panel per 12 MB of C (bf16 4096^3 ->
+  // fp32 on GB300: 772 us in one panel, 623-632 us in 4-6; the copy engines
+  // move about 200 GB/s each way and 335 GB/s in both directions at once).
+  const int64_t c_bytes = M * N * eo;
+  int64_t want = panels;
+  if (!want)
+    want = c_bytes < (int64_t(6) << 20) ? 1 : std::min<int64_t>(6, std::max<int64_t>(2, c_bytes / (int64_t(12) << 20)));
+  want = std::min<int64_t>(want, M);
+  int64_t rows_per = (M + want - 1) / want;
+  if (!panels) rows_per = (rows_per + 127) / 128 * 128;
+  const int64_t npanels = (M + rows_per - 1) / rows_per;
+
+  tgemm::DeviceInfo* dev = nullptr;
+  int st = tgemm::device_info(&dev);
+  if (st != TGEMM_OK) return st;
+  cudaStream_t in = nullptr, out = nullptr;
+  if ((st = tgemm::copy_streams(&in, &out)) != TGEMM_OK) return st;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  tgemm::CallEvents evs;
+  cudaEvent_t ev_start, ev_b, ev_done;
+  std::vector<cudaEvent_t> ev_a(npanels), ev_c(npanels);
+  cudaError_t e;
+  if ((e = evs.make(&ev_start)) != cudaSuccess || (e = evs.make(&ev_b)) != cudaSuccess ||
+      (e = evs.make(&ev_done)) != cudaSuccess)
+    return tgemm::cuda_fail(e, "cudaEventCreate");
+  for (int64_t p = 0; p < npanels; ++p)
+    if ((e = evs.make(&ev_a[p])) != cudaSuccess || (e = evs.make(&ev_c[p])) != cudaSuccess)
+      return tgemm::cuda_fail(e, "cudaEventCreate");
+  // both copy streams follow the work already on `stream` (it may still use
+  // the device buffers or the host memory of C)
+  if ((e = cudaEventRecord(ev_start, s)) != cudaSuccess || (e = cudaStreamWaitEvent(in, ev_start, 0)) != cudaSuccess ||
+      (e = cudaStreamWaitEvent(out, ev_start, 0)) != cudaSuccess)
+    return tgemm::cuda_fail(e, "stream ordering");
+  const char* ah = static_cast<const char*>(A_host);
+  char* ch = static_cast<char*>(C_host);
+  char* da = static_cast<char*>(dA);
+  char* dc = static_cast<char*>(dC);
+  if (K > 0) {
+    if ((e = tgemm::copy_rows(dB, N * ei, B_host, ldb * ei, N * ei, K, cudaMemcpyHostToDevice, in)) != cudaSuccess ||
+        (e = cudaEventRecord(ev_b, in)) != cudaSuccess || (e = cudaStreamWaitEvent(s, ev_b, 0)) != cudaSuccess)
+      return tgemm::cuda_fail(e, "copy of B");
+    for (int64_t p = 0; p < npanels; ++p) {
+      const int64_t r0 = p * rows_per, rows = std::min(rows_per, M - r0);
+      if ((e = tgemm::copy_rows(da + r0 * K * ei, K * ei, ah + r0 * lda * ei, lda * ei, K * ei, rows,
+                                cudaMemcpyHostToDevice, in)) != cudaSuccess ||
+          (e = cudaEventRecord(ev_a[p], in)) != cudaSuccess)
+        return tgemm::cuda_fail(e, "copy of A");
+    }
+  }
+  for (int64_t p = 0; p < npanels; ++p) {
+    const int64_t r0 = p * rows_per, rows = std::min(rows_per, M - r0);
+    if (K > 0 && (e = cudaStreamWaitEvent(s, ev_a[p], 0)) != cudaSuccess) return tgemm::cuda_fail(e, "stream ordering");
+    st = tgemm_gemm(rows, N, K, K > 0 ? da + r0 * K * ei : nullptr, K > 0 ? K : 1, dB, N, dc + r0 * N * eo, N, dtype,
+                    stream);
+    if (st != TGEMM_OK) return st;
+    if ((e = cudaEventRecord(ev_c[p], s)) != cudaSuccess || (e = cudaStreamWaitEvent(out, ev_c[p], 0)) != cudaSuccess ||
+        (e = tgemm::copy_rows(ch + r0 * ldc * eo, ldc * eo, dc + r0 * N * eo, N * eo, N * eo, rows,
+                              cudaMemcpyDeviceToHost, out)) != cudaSuccess)
+      return tgemm::cuda_fail(e, "copy of C");
+  }
+  // later work on `stream` follows the last copy of C
+  if ((e = cudaEventRecord(ev_done, out)) != cudaSuccess || (e = cudaStreamWaitEvent(s, ev_done, 0)) != cudaSuccess)
+    return tgemm::cuda_fail(e, "stream ordering");
+  return TGEMM_OK;
 }
 
 int tgemm_workspace_size(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb,
