@@ -236,7 +236,9 @@ __global__ void __launch_bounds__(tc_threads(kCopy), 1)
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
     }
-    if (lane == 0) ptx::bulk_wait_group<0>();
+    // the stores must have read shared memory before the CTA exits (their
+    // writes to C complete with the kernel)
+    if (lane == 0) ptx::bulk_wait_group_read<0>();
     __syncwarp();
   } else if constexpr (kCopy) {
     // -------------------------------------------------- copy producers

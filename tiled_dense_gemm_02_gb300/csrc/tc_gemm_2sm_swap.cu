@@ -416,7 +416,9 @@ __global__ void __launch_bounds__(32 * (2 + kEpiWarps), 1)
     // a prior-C load still in flight (a wait gave up) lands before shared memory is released
     for (int i = 0; i < 2; ++i)
       if (((pending >> i) & 1u) && lane == 0) wait_teardown(i ? pbar1 : pbar0, (pphase >> i) & 1u, ctl, SITE_TEARDOWN);
-    if (lane == 0) ptx::bulk_wait_group<0>();
+    // the stores must have read shared memory before the CTA exits (their
+    // writes to C complete with the kernel)
+    if (lane == 0) ptx::bulk_wait_group_read<0>();
     __syncwarp();
   }
 
