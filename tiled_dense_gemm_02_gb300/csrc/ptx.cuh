@@ -161,6 +161,23 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, int32_t x, 
                : "memory");
 }
 
+// L2 cache policy under which the lines an access touches are the first to be
+// evicted (for outputs nothing in the kernel reads again).
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// tma_store_3d with an L2 cache policy (l2_evict_first_policy, say).
+__device__ __forceinline__ void tma_store_3d_hint(const CUtensorMap* map, int32_t x, int32_t y, int32_t z,
+                                                  uint32_t src, uint64_t policy) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group.L2::cache_hint [%0, {%1, %2, %3}], [%4], %5;" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y), "r"(z), "r"(src), "l"(policy)
+               : "memory");
+}
+
 // Untiled bulk copy of `bytes` (multiple of 16; both addresses 16-byte aligned)
 // from global to this CTA's shared memory; completion as transaction bytes on `bar`.
 __device__ __forceinline__ void bulk_load_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
