@@ -248,8 +248,10 @@ def test_swapped_pair_planning(tg):
     assert (p.tiles_m, p.tiles_n, p.ctas, p.cta_group, p.cluster_ctas) == (19, 16, 152, 2, 2)
     st, p = plan(tg, 8192, 8192, 8192, dtype=2, sms=152)
     assert st == tg.OK and p.swap_ab == 1 and p.tile_m == 256 and p.group_m == 8
+    st, p = plan(tg, 3072, 4096, 4096, dtype=2, sms=152)
+    assert p.tuned == 0 and p.group_m == 4   # operands within half of L2
     st, p = plan(tg, 4096, 4096, 4096, dtype=2, sms=152)
-    assert p.group_m == 4   # operands within half of L2
+    assert p.tuned == 1 and p.group_m == 2    # the table's measured raster group
     for tm in (128, 192, 224, 256):
         st, p = plan(tg, 300, 520, 200, dtype=2, swap_ab=2, tile_m=tm)
         assert st == tg.OK and p.swap_ab == 1 and p.tile_m == tm and p.tile_n == 256
