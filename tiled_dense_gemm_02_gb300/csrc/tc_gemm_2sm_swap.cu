@@ -25,8 +25,7 @@
 // 32 x 32 box, or stores per thread, where a warp's 32 lanes write 32
 // consecutive columns of one row at a time.  Bulk stores mark C's lines first
 // to evict in L2, which keeps more of A and B resident when the three share
-// L2 (bf16 4096^3 -> fp32: 0.9 % faster, interleaved means of 195 calls;
-// neutral at 2048^3 and 8192^3).
+// L2 (bf16 4096^3 -> fp32: DRAM traffic per launch 121.9 -> 111.6 MB).
 #include <atomic>
 
 #include "tc_common.cuh"
