@@ -227,7 +227,7 @@ def test_tuned_shape_table(tg):
     the table's options; any tuned option set, another shape, or pointers the
     entry cannot serve keep the heuristics."""
     st, p = plan(tg, 1024, 1024, 1024, dtype=1, sms=152)
-    assert st == tg.OK and p.tuned == 1 and (p.cta_group, p.tile_n, p.group_m) == (1, 64, 4)
+    assert st == tg.OK and p.tuned == 1 and (p.cta_group, p.tile_n, p.group_m) == (1, 64, 8)
     st, p = plan(tg, 1024, 1024, 1024, dtype=1, sms=152, group_m=8)
     assert st == tg.OK and p.tuned == 0 and p.group_m == 8
     st, p = plan(tg, 1024, 1024, 1000, dtype=1, sms=152)

@@ -37,7 +37,7 @@ FIELDS = ("kernel", "cta_group", "tile_n", "tile_m", "swap_ab", "tile_k", "group
 def candidates():
     """Option sets tried for every shape (invalid ones for a shape are skipped)."""
     out = [{}]
-    for tm, tk, g in itertools.product((128, 192, 224, 256), (64, 128), (4, 8)):
+    for tm, tk, g in itertools.product((128, 192, 224, 256), (64, 128), (1, 2, 4, 8)):
         out.append({"swap_ab": 2, "tile_m": tm, "tile_n": 256, "tile_k": tk, "group_m": g})
     for bn, tk, g in itertools.product((128, 192, 224, 256), (64, 128), (4, 8)):
         out.append({"cta_group": 2, "swap_ab": 1, "tile_n": bn, "tile_k": tk, "group_m": g})
@@ -47,6 +47,12 @@ def candidates():
 
 
 def measure(shapes, reps):
+    """Time every valid candidate of each shape.  The candidates are timed
+    interleaved: each round calls all of them once, in an order rotated by one
+    from the previous round, each call after an L2 flush; the ranking is by the
+    mean over rounds.  (The median of back-to-back calls of one candidate moves
+    in the steps of the event clock, about 2 us on GB300, and the first call
+    of a round runs slower; rotating spreads that over all candidates.)"""
     import torch
     sys.path.insert(0, os.path.dirname(HERE))
     import tiled_dense_gemm_02_gb300 as tg
@@ -54,6 +60,7 @@ def measure(shapes, reps):
     torch.cuda.set_device(dev)
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.int32, device=dev)
     sp = torch.cuda.current_stream(dev).cuda_stream
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
     results = []
     for spec in shapes:
         dims, dname = spec.split(":")
@@ -62,18 +69,23 @@ def measure(shapes, reps):
         a = torch.randn(M, K, device=dev).to(torch.bfloat16 if dname.startswith("bf16") else torch.float16)
         b = torch.randn(K, N, device=dev).to(a.dtype)
         c = torch.empty(M, N, device=dev, dtype=torch.float32 if dname.endswith("f32") else a.dtype)
-        best = None
-        for opts in candidates():
-            st, _ = tg.plan(M, N, K, a.data_ptr(), K, b.data_ptr(), N, c.data_ptr(), N, dtype, opts or None,
-                            sm_count=torch.cuda.get_device_properties(dev).multi_processor_count)
+        # "auto": the heuristics alone (a CTA cap of one per SM changes nothing
+        # but keeps the compiled-in table out of the plan)
+        cands = [{"max_ctas": sms}] + candidates()[1:]
+        calls = []
+        for opts in cands:
+            st, _ = tg.plan(M, N, K, a.data_ptr(), K, b.data_ptr(), N, c.data_ptr(), N, dtype, opts, sm_count=sms)
             if st != tg.OK:
                 continue
-            call = lambda: tg.gemm_ex(M, N, K, a.data_ptr(), K, b.data_ptr(), N, c.data_ptr(), N, dtype,
-                                      opts or None, sp)
+            call = (lambda o: lambda: tg.gemm_ex(M, N, K, a.data_ptr(), K, b.data_ptr(), N, c.data_ptr(), N, dtype,
+                                                 o, sp))(opts)
             if call() != tg.OK:
                 continue
-            ts = []
-            for _ in range(reps):
+            calls.append((opts, call, []))
+        torch.cuda.synchronize()
+        for r in range(reps + 2):
+            for i in range(len(calls)):
+                opts, call, ts = calls[(i + r) % len(calls)]
                 flush.fill_(1)
                 s = torch.cuda.Event(enable_timing=True)
                 e = torch.cuda.Event(enable_timing=True)
@@ -81,16 +93,17 @@ def measure(shapes, reps):
                 call()
                 e.record()
                 torch.cuda.synchronize()
-                ts.append(s.elapsed_time(e) * 1000.0)
-            med = statistics.median(ts)
-            if best is None or med < best[0]:
-                best = (med, opts)
-            if not opts:
-                auto_us = med
+                if r >= 2:  # two warm-up rounds
+                    ts.append(s.elapsed_time(e) * 1000.0)
         assert tg.device_status(sp) == tg.OK
-        results.append({"shape": spec, "M": M, "N": N, "K": K, "dtype": dtype, "best_us": round(best[0], 2),
-                        "auto_us": round(auto_us, 2), "options": best[1],
-                        "tflops": round(2.0 * M * N * K / (best[0] * 1e-6) / 1e12, 1)})
+        means = [(statistics.mean(ts), opts) for opts, _, ts in calls]
+        best_us, best_opts = min(means, key=lambda x: x[0])
+        auto_us = means[0][0]
+        if "max_ctas" in best_opts:  # the heuristics won: the entry leaves every option at 0
+            best_opts = {}
+        results.append({"shape": spec, "M": M, "N": N, "K": K, "dtype": dtype, "best_us": round(best_us, 2),
+                        "auto_us": round(auto_us, 2), "options": best_opts,
+                        "tflops": round(2.0 * M * N * K / (best_us * 1e-6) / 1e12, 1)})
         print(json.dumps(results[-1]), flush=True)
     return results, torch.cuda.get_device_name(dev)
 
@@ -99,7 +112,8 @@ def write_table(results, device, path):
     lines = [
         "// Tuned launch options per shape, written by tiled_dense_gemm_02_gb300/tune.py",
         f"// on {device}, {datetime.date.today().isoformat()}: the fastest of the candidate option sets",
-        "// (median of timed calls after an L2 flush).  Entry: M, N, K, dtype, then the",
+        "// (mean over rounds of interleaved calls in rotating order, each after an L2",
+        "// flush; auto = the heuristics alone).  Entry: M, N, K, dtype, then the",
         "// tgemm_options fields " + ", ".join(FIELDS) + " (0 = auto).",
     ]
     for r in results:
@@ -115,7 +129,7 @@ def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("shapes", nargs="*", default=DEFAULT_SHAPES)
     ap.add_argument("--out", default=DEFAULT_OUT)
-    ap.add_argument("--reps", type=int, default=15)
+    ap.add_argument("--reps", type=int, default=30)
     args = ap.parse_args()
     results, device = measure(args.shapes, args.reps)
     write_table(results, device, args.out)
