@@ -96,7 +96,8 @@ enum tgemm_kernel {
   TGEMM_KERNEL_AUTO = 0,
   TGEMM_KERNEL_TC_TMA = 1,     /* tensor cores; A and B by bulk-tensor copies */
   TGEMM_KERNEL_TC_COPY = 2,    /* tensor cores; A and/or B by per-thread async
-                                  copies (any alignment) */
+                                  copies (any alignment); with cta_group = 2,
+                                  A by bulk-tensor copies and B per thread */
   TGEMM_KERNEL_SIMT = 3        /* fp32 CUDA cores (TGEMM_F32 only) */
 };
 
@@ -116,8 +117,11 @@ typedef struct tgemm_options {
                            pending; no copy is ever issued */
   int cta_group;        /* tensor-core tiles per CTA (0 auto): 1 = 128 x N
                            tiles on one SM, 2 = 256 x N tiles on a pair of
-                           SMs (a 2-CTA cluster; bulk-tensor operands only,
-                           tile_n 128, 192, 224 or 256) */
+                           SMs (a 2-CTA cluster): with bulk-tensor operands,
+                           tile_n 128, 192, 224 or 256; with A by bulk-tensor
+                           copies and B by per-thread copies (B's rows off the
+                           16-byte grid, or kernel = TC_COPY), tile_n 128 or
+                           256, 64-deep stages and per-thread stores of C */
   int tile_k;           /* K depth of one shared-memory stage (0 auto): 64, or
                            128 (two 64-deep sub-blocks per stage, one MMA
                            completion signal per stage; CTA-pair kernel only) */
