@@ -213,11 +213,12 @@ __global__ void __launch_bounds__(copy_pair_threads(), 1)
       wait_teardown(ptx::smem_u32(drain), 0, ctl, SITE_DRAIN);
     } else if (!leader && lane == 0) {
       // ---------------------------------------------------------- forwarder
-      // A release at cluster scope costs about as long as the copies still in
-      // flight in this SM take to land, so one release covers every stage
-      // that has landed by then: wait for the next stage, gather the stages
-      // after it that are already complete, fence once, then arrive on the
-      // leader's barriers of all of them.  A stage's next fill needs the
+      // A release at cluster scope measured about 1700 cycles here with copies
+      // in flight in this SM (a release per stage made the ragged bf16
+      // 1000 x 1500 x 4096 product 74 us instead of 44), so one release covers
+      // every stage that has landed by then: wait for the next stage, gather
+      // the stages after it that are already complete, fence once, then
+      // arrive on the leader's barriers of all of them.  A stage's next fill needs the
       // MMA's release of it, which needs this forward, so no stage can land
       // twice before it is forwarded.
       const int my_tiles = pair < args.num_tiles ? (args.num_tiles - pair + npairs - 1) / npairs : 0;
