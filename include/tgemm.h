@@ -146,7 +146,18 @@ typedef struct tgemm_options {
                            operands and no stream-K split or multicast */
   int tile_m;           /* tile height of swap_ab = 2 (0 auto): 128, 192, 224
                            or 256; other kernels take 0 */
-  int reserved[3];
+  int simt_split;       /* fp32 SIMT kernel (TGEMM_F32 only; other dtypes
+                           take 0).  When the last round of 128 x 128 tiles
+                           fills at most half of the resident CTA slots (two
+                           per SM), each of its tiles is computed as two K
+                           halves by two CTAs, whose results are added into C
+                           after the call zeroes those rows of C.  Two
+                           additions onto zero commute, so the result does
+                           not depend on which half lands first.  0 auto (on
+                           when K >= 256), 1 off, 2 on whenever the round
+                           fits and K spans two 16-deep stages.  A call with
+                           an epilogue computes every tile whole */
+  int reserved[2];
 } tgemm_options;
 
 /* tgemm_gemm with explicit options (opts may be NULL).  A forced kernel that
@@ -174,7 +185,9 @@ typedef struct tgemm_plan_info {
   int smem_bytes;    /* dynamic shared memory per CTA */
   int cta_group;     /* 1: one SM per tile; 2: a CTA pair per 256-row tile
                         (tile_m is then 256 and ctas counts CTAs, two per pair) */
-  int dp_tiles;      /* tiles computed whole (all of them without stream-K) */
+  int dp_tiles;      /* tiles computed whole (all of them without stream-K;
+                        SIMT kernel: the rest are split in two K halves, and
+                        ctas = dp_tiles + 2 x the split tiles) */
   int sk_iters;      /* k-stages of the remaining tiles split over the pairs */
   int workspace_bytes; /* workspace the call uses (0 without stream-K) */
   int cluster_ctas;  /* CTAs per cluster: 1 (one-SM tiles), 2 (a pair) or 4

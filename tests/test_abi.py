@@ -362,6 +362,32 @@ def test_two_pair_cluster_planning(tg):
     assert st == tg.OK and p.cluster_ctas == 1
 
 
+def test_simt_split_planning(tg):
+    """fp32: a last round of 128 x 128 tiles that fills at most half of the
+    2 x SMs resident CTA slots is split into K halves (two CTAs per tile)."""
+    # 4096^3 on 152 SMs: 1024 tiles, 3 full rounds of 304, 112 left -> 224 halves
+    st, p = plan(tg, 4096, 4096, 4096, dtype=0, sms=152)
+    assert st == tg.OK and p.kernel == tg.KERNEL_SIMT
+    assert (p.tiles_m, p.tiles_n, p.dp_tiles, p.ctas) == (32, 32, 912, 1136)
+    # 2048^3: 256 tiles in one round of 304 slots; halves would not fit in one round
+    st, p = plan(tg, 2048, 2048, 2048, dtype=0, sms=152)
+    assert (p.dp_tiles, p.ctas) == (256, 256)
+    # 1024^3: 64 tiles, all split
+    st, p = plan(tg, 1024, 1024, 1024, dtype=0, sms=152)
+    assert (p.dp_tiles, p.ctas) == (0, 128)
+    # auto needs K >= 256 (16 stages); simt_split = 2 needs two stages
+    assert plan(tg, 64, 64, 64, dtype=0, sms=152)[1].ctas == 1
+    assert plan(tg, 64, 64, 64, dtype=0, sms=152, simt_split=2)[1].ctas == 2
+    assert plan(tg, 64, 64, 16, dtype=0, sms=152, simt_split=2)[1].ctas == 1
+    assert plan(tg, 4096, 4096, 4096, dtype=0, sms=152, simt_split=1)[1].ctas == 1024
+    # a remainder above half of the slots stays whole: 3072^3 -> 576 = 304 + 272
+    st, p = plan(tg, 3072, 3072, 3072, dtype=0, sms=152, simt_split=2)
+    assert (p.dp_tiles, p.ctas) == (576, 576)
+    assert plan(tg, 64, 64, 64, dtype=0, simt_split=3)[0] == tg.ERR_INVALID_VALUE
+    assert plan(tg, 64, 64, 64, dtype=0, simt_split=-1)[0] == tg.ERR_INVALID_VALUE
+    assert plan(tg, 256, 256, 256, dtype=2, simt_split=2)[0] == tg.ERR_INVALID_VALUE
+
+
 def test_dispatch_options(tg):
     st, p = plan(tg, 1024, 1024, 1024, dtype=1, tile_n=64, max_ctas=5, group_m=3, store_mode=2)
     assert st == tg.OK

@@ -104,11 +104,14 @@ def test_epilogue_stream_k_finisher(epi_name):
     assert res.plan.sk_iters > 0
 
 
+@pytest.mark.parametrize("split", [0, 2], ids=["auto", "split_requested"])
 @pytest.mark.parametrize("epi_name", list(EPILOGUES))
 @pytest.mark.parametrize("shape", [(300, 520, 200), (129, 257, 33)], ids=lambda s: "x".join(map(str, s)))
-def test_epilogue_simt(shape, epi_name):
+def test_epilogue_simt(shape, epi_name, split):
+    """With an epilogue the SIMT kernel computes every tile whole, even where
+    the plan of the plain product splits tiles into K halves."""
     M, N, K = shape
-    run_case(M, N, K, wl.F32, epi_name, None, seed=82)
+    run_case(M, N, K, wl.F32, epi_name, {"simt_split": split} if split else None, seed=82)
 
 
 @pytest.mark.parametrize("epi_name", list(EPILOGUES))

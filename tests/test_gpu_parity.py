@@ -54,6 +54,57 @@ def test_workload_sampled(name):
     H.check_sampled(res, A, B, w.K, w.dtype, rows, cols, name)
 
 
+# ---------------------------------------------- fp32 tiles split into K halves
+
+def slots():
+    return 2 * torch.cuda.get_device_properties(0).multi_processor_count
+
+
+@pytest.mark.parametrize("shape,lds", [
+    ((300, 200, 1000), (None, None, None)),   # every tile split; 16-byte rows: vector adds
+    ((300, 200, 1000), (1003, 205, 211)),     # rows off the 16-byte grid: scalar loads and adds
+    ((130, 129, 40), (None, None, 133)),      # three 16-deep stages: halves of one and two stages
+], ids=["aligned", "unaligned", "short_k"])
+def test_simt_split_all_tiles(shape, lds):
+    """simt_split = 2 on a product whose tiles all fit in half of the CTA
+    slots: each tile is two CTAs, one per half of its k-stages, adding into
+    rows of C the call zeroes; ldc padding and guard bands keep their NaN
+    canaries (a missed zero would leave NaN in the sum)."""
+    (M, N, K), (lda, ldb, ldc) = shape, lds
+    A, B, res = case(M, N, K, wl.F32, seed=120, lda=lda, ldb=ldb, ldc=ldc, options={"simt_split": 2})
+    tiles = res.plan.tiles_m * res.plan.tiles_n
+    assert res.plan.dp_tiles == 0 and res.plan.ctas == 2 * tiles
+    H.check_full(res, A, B, M, N, K, wl.F32, "simt split")
+
+
+def test_simt_split_off_matches_oracle_too():
+    A, B, res = case(300, 200, 1000, wl.F32, seed=120, options={"simt_split": 1})
+    assert res.plan.ctas == res.plan.tiles_m * res.plan.tiles_n == res.plan.dp_tiles
+    H.check_full(res, A, B, 300, 200, 1000, wl.F32, "simt whole tiles")
+
+
+def test_simt_split_last_round_auto():
+    """20 x 17 tiles on 2 x SMs slots: the last round's tiles are split by
+    default (K >= 256), starting in the middle of a tile row whose first
+    tiles are computed whole after the zero fill."""
+    M, N, K = 20 * 128 - 37, 17 * 128 - 5, 300
+    A, B, res = case(M, N, K, wl.F32, seed=121, ldc=N + 3)
+    tiles = 20 * 17
+    tail = tiles % slots()
+    if 0 < tail <= slots() // 2:
+        assert res.plan.dp_tiles == tiles - tail and res.plan.ctas == tiles + tail
+        assert res.plan.dp_tiles % 17 != 0
+    H.check_full(res, A, B, M, N, K, wl.F32, "simt split tail")
+
+
+def test_simt_split_is_deterministic():
+    """Two additions onto zero commute: repeated calls give the same bits."""
+    A, B, r1 = case(300, 200, 1000, wl.F32, seed=122, options={"simt_split": 2})
+    for _ in range(3):
+        _, _, r2 = case(300, 200, 1000, wl.F32, seed=122, options={"simt_split": 2})
+        assert np.array_equal(r1.raw, r2.raw)
+
+
 @pytest.mark.parametrize("multicast", [1, 2], ids=["one_pair_clusters", "two_pair_clusters"])
 def test_headline_both_cluster_sizes(multicast):
     """The bf16 4096^3 -> fp32 product on CTA pairs in 2-CTA clusters and in

@@ -39,7 +39,8 @@ class Options(ctypes.Structure):
                 ("max_ctas", ctypes.c_int), ("store_mode", ctypes.c_int), ("wait_timeout_us", ctypes.c_int),
                 ("inject_fault", ctypes.c_int), ("cta_group", ctypes.c_int), ("tile_k", ctypes.c_int),
                 ("stream_k", ctypes.c_int), ("multicast", ctypes.c_int),
-                ("swap_ab", ctypes.c_int), ("tile_m", ctypes.c_int), ("reserved", ctypes.c_int * 3)]
+                ("swap_ab", ctypes.c_int), ("tile_m", ctypes.c_int), ("simt_split", ctypes.c_int),
+                ("reserved", ctypes.c_int * 2)]
 
 
 class Epilogue(ctypes.Structure):

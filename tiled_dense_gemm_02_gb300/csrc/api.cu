@@ -174,6 +174,7 @@ struct Plan {
   int k_blocks = 0;               // k-stages per tile
   int dp_tiles = 0, sk_iters = 0;  // stream-K split (sk_iters == 0: whole tiles only)
   int64_t workspace = 0;          // bytes of workspace the stream-K split uses
+  int split_stage = 0;            // SIMT kernel: k-stage dividing the halves of its split tiles (0: none)
   int64_t batch = 1;              // matrices computed by one launch (strided batch, swapped kernel)
   bool batch_loop = false;        // a batch the kernels cannot index: one launch per matrix
   bool tuned = false;             // options from the tuned-shape table
@@ -392,13 +393,31 @@ int make_plan_core(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, 
     p.zero = true;
     return TGEMM_OK;
   }
+  if (opt.simt_split < 0 || opt.simt_split > 2 || (opt.simt_split != 0 && dtype != TGEMM_F32))
+    return TGEMM_ERR_INVALID_VALUE;
   if (dtype == TGEMM_F32) {
     if (opt.kernel != TGEMM_KERNEL_AUTO && opt.kernel != TGEMM_KERNEL_SIMT) return TGEMM_ERR_INVALID_VALUE;
     p.kernel = TGEMM_KERNEL_SIMT;
     p.tiles_m = static_cast<int>((M + kSimtBM - 1) / kSimtBM);
     p.tiles_n = static_cast<int>((N + kSimtBN - 1) / kSimtBN);
     if (p.tiles_m > 65535) return TGEMM_ERR_TOO_LARGE;
-    p.ctas = p.tiles_m * p.tiles_n;
+    const int64_t tiles = static_cast<int64_t>(p.tiles_m) * p.tiles_n;
+    if (tiles > INT32_MAX / 2) return TGEMM_ERR_TOO_LARGE;
+    p.ctas = p.dp_tiles = static_cast<int>(tiles);
+    p.k_blocks = static_cast<int>((K + kSimtBK - 1) / kSimtBK);
+    {
+      // Two 256-thread CTAs are resident per SM.  Tiles run in rounds of
+      // 2 x SMs; a last round that fills at most half of the slots takes as
+      // long as a full one, and split into K halves it takes half as long.
+      const int64_t slots = 2 * static_cast<int64_t>(sms);
+      const int64_t tail = tiles % slots;
+      const bool fits = tail > 0 && 2 * tail <= slots && p.k_blocks >= 2;
+      if (fits && (opt.simt_split == 2 || (opt.simt_split == 0 && p.k_blocks >= 16))) {
+        p.dp_tiles = static_cast<int>(tiles - tail);
+        p.ctas = static_cast<int>(tiles + tail);
+        p.split_stage = p.k_blocks / 2;
+      }
+    }
     p.bn = kSimtBN;
     p.stages = 2;
     p.smem = 0;
@@ -792,7 +811,22 @@ int run(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void*
     a.ldc = ldc;
     a.vec = p.a_copy == 16 ? 1 : 0;
     a.epi = ep;
-    e = launch_simt(a, stream);
+    a.tiles_n = p.tiles_n;
+    a.full_tiles = p.dp_tiles;
+    a.split_stage = p.split_stage;
+    int64_t units = p.ctas;
+    if (ep.on || p.split_stage == 0) {
+      // an epilogue is applied once to the whole sum: every tile whole
+      a.full_tiles = p.tiles_m * p.tiles_n;
+      a.split_stage = 0;
+      units = a.full_tiles;
+    } else {
+      // the halves add into zeros: clear the rows of C the split tiles cover
+      const int64_t r0 = static_cast<int64_t>(p.dp_tiles / p.tiles_n) * kSimtBM;
+      e = launch_zero_fill(static_cast<float*>(C) + r0 * ldc, M - r0, N, ldc, 4, stream);
+      if (e != cudaSuccess) return cuda_fail(e, "zero-fill launch");
+    }
+    e = launch_simt(a, units, stream);
     return e == cudaSuccess ? TGEMM_OK : cuda_fail(e, "SIMT kernel launch");
   }
   const bool bf16 = (dtype == TGEMM_BF16 || dtype == TGEMM_BF16_F32OUT);

@@ -23,6 +23,14 @@
 // 4 (n, n+32), so each k step is 4 LDS.128 feeding 64 FMAs (32 paired FMA
 // instructions, each a pair of columns).  Edge tiles load
 // zeros outside the matrix and mask their stores ("CUDA tile", section 四.4).
+//
+// Work units: the grid is one-dimensional.  Tiles are numbered row by row;
+// tiles [0, full_tiles) are computed whole, and every later tile by two CTAs,
+// one per half of its k-stages ("矩阵乘法中的平铺", K-splitting taken across
+// CTAs).  The host plans that split only for a last round of tiles that fills
+// at most half of the resident CTA slots: split, it ends in half the time.
+// The halves add their sums into C, which the host has zeroed; two additions
+// onto zero give the same float whichever lands first.
 #include "tgemm_internal.h"
 
 namespace tgemm {
@@ -124,7 +132,17 @@ __global__ void __launch_bounds__(THREADS, 2) simt_sgemm_kernel(const SimtArgs p
   const int tm = lane >> 3, tn = lane & 7;       // 4 x 8 threads per warp
   const int m_in = wm * 32 + tm * 4;             // rows m_in..+3 and m_in+16..+19
   const int n_in = wn * 64 + tn * 4;             // cols n_in..+3 and n_in+32..+35
-  const int m0 = blockIdx.y * BM, n0 = blockIdx.x * BN;
+  int tile = blockIdx.x;
+  int s_begin = 0, s_end = (p.K + BK - 1) / BK;
+  bool half = false;
+  if (!EPI && tile >= p.full_tiles) {
+    const int h = tile - p.full_tiles;
+    tile = p.full_tiles + (h >> 1);
+    half = true;
+    if (h & 1) s_begin = p.split_stage;
+    else s_end = p.split_stage;
+  }
+  const int m0 = (tile / p.tiles_n) * BM, n0 = (tile % p.tiles_n) * BN;
 
   LoadPos q;
   {
@@ -144,18 +162,17 @@ __global__ void __launch_bounds__(THREADS, 2) simt_sgemm_kernel(const SimtArgs p
 #pragma unroll
     for (int j = 0; j < 4; ++j) acc[i][j] = make_float2(0.0f, 0.0f);
 
-  const int kstages = (p.K + BK - 1) / BK;
   Prefetch f;
-  if (kstages > 0) {
-    load_stage<VEC>(p, q, 0, f);
+  if (s_begin < s_end) {
+    load_stage<VEC>(p, q, s_begin * BK, f);
     store_stage(As[0], Bs[0], tid, f);
   }
   __syncthreads();
 
 #pragma unroll 1
-  for (int s = 0; s < kstages; ++s) {
-    const int buf = s & 1;
-    const bool more = s + 1 < kstages;
+  for (int s = s_begin; s < s_end; ++s) {
+    const int buf = (s - s_begin) & 1;
+    const bool more = s + 1 < s_end;
     if (more) load_stage<VEC>(p, q, (s + 1) * BK, f);
 #pragma unroll
     for (int k = 0; k < BK; ++k) {
@@ -182,7 +199,16 @@ __global__ void __launch_bounds__(THREADS, 2) simt_sgemm_kernel(const SimtArgs p
         for (int j = 0; j < 4; ++j)
           if (gn + j < p.N) v[j] = epi_apply(p.epi, v[j], gn + j, [&] { return crow[gn + j]; });
       }
-      if (VEC && gn + 3 < p.N) {
+      if (half) {
+        // one K half of the tile: add into C (zeroed by the host)
+        if (VEC && gn + 3 < p.N) {
+          atomicAdd(reinterpret_cast<float4*>(crow + gn), make_float4(v[0], v[1], v[2], v[3]));
+        } else {
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            if (gn + j < p.N) atomicAdd(crow + gn + j, v[j]);
+        }
+      } else if (VEC && gn + 3 < p.N) {
         *reinterpret_cast<float4*>(crow + gn) = make_float4(v[0], v[1], v[2], v[3]);
       } else {
 #pragma unroll
@@ -195,8 +221,8 @@ __global__ void __launch_bounds__(THREADS, 2) simt_sgemm_kernel(const SimtArgs p
 
 }  // namespace
 
-cudaError_t launch_simt(const SimtArgs& args, cudaStream_t stream) {
-  dim3 grid((args.N + BN - 1) / BN, (args.M + BM - 1) / BM);
+cudaError_t launch_simt(const SimtArgs& args, int64_t units, cudaStream_t stream) {
+  const dim3 grid(static_cast<unsigned>(units));
   const bool epi = args.epi.on != 0;
   if (args.vec)
     epi ? simt_sgemm_kernel<true, true><<<grid, THREADS, 0, stream>>>(args)

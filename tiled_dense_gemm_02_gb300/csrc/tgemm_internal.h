@@ -110,6 +110,9 @@ struct SimtArgs {
   float* C;
   int64_t ldc;
   int vec;              // 1 when A/B/C rows allow 16-byte vector accesses
+  int tiles_n;          // 128-column tiles per tile row (tiles are numbered row by row)
+  int full_tiles;       // tiles [0, full_tiles) are computed whole by one CTA each
+  int split_stage;      // k-stage dividing the two halves of each later tile
   Epilogue epi;
 };
 
@@ -182,7 +185,7 @@ cudaError_t launch_tc_pair_swap(int tm, int ksub, const CUtensorMap& mapA, const
 // Number of clusters of `cluster` CTAs (2 or 4) of the pair kernel that can be
 // resident at once.
 cudaError_t tc_pair_capacity(int cluster, int* clusters);
-cudaError_t launch_simt(const SimtArgs& args, cudaStream_t stream);
+cudaError_t launch_simt(const SimtArgs& args, int64_t units, cudaStream_t stream);
 cudaError_t launch_zero_fill(void* C, int64_t rows, int64_t cols, int64_t ldc, int elem_bytes, cudaStream_t stream);
 // out[j][i] = in[i][j], in rows x cols; elem_bytes 2 or 4; vec: every row of
 // in and out starts on a 16-byte boundary (16-byte accesses)
