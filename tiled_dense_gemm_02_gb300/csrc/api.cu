@@ -17,6 +17,7 @@
 
 #include "../../include/tgemm.h"
 #include "tgemm_internal.h"
+#include "simt_sgemm.h"
 
 namespace tgemm {
 

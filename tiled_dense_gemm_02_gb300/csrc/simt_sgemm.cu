@@ -21,7 +21,18 @@
 //   Bs[k][n]  B as in global memory.
 // A thread's 8 rows are two runs of 4 (m, m+16) and its 8 columns two runs of
 // 4 (n, n+32), so each k step is 4 LDS.128 feeding 64 FMAs (32 paired FMA
-// instructions, each a pair of columns).  Edge tiles load
+// instructions, each a pair of columns).
+//
+// Which lane takes which (tm, tn) sets the cost of those reads.  A 16-byte
+// shared load of a warp takes two wavefronts at best, one per half-warp.
+// Measured on GB300: a half-warp takes one wavefront when its lanes read
+// their chunks as adjacent runs (0,0,1,1,...) or at most two chunks per
+// quarter-warp, and two when its quarter-warps repeat a spread pattern
+// (0,1,..,7 in both).  With tn = lane % 8 the B reads were of the second
+// kind (4 wavefronts each; 3 per load with A's).  Taking tm from lane bits 0 and 3
+// and tn from bits 1, 2 and 4 makes every read 2 wavefronts (2.4 % faster at
+// fp32 4096^3, same bits).  A warp's store instruction still writes four
+// whole 128-byte row segments.  Edge tiles load
 // zeros outside the matrix and mask their stores ("CUDA tile", section 四.4).
 //
 // Work units: the grid is one-dimensional.  Tiles are numbered row by row;
@@ -31,7 +42,7 @@
 // at most half of the resident CTA slots: split, it ends in half the time.
 // The halves add their sums into C, which the host has zeroed; two additions
 // onto zero give the same float whichever lands first.
-#include "tgemm_internal.h"
+#include "simt_sgemm.h"
 
 namespace tgemm {
 namespace {
@@ -129,7 +140,8 @@ __global__ void __launch_bounds__(THREADS, 2) simt_sgemm_kernel(const SimtArgs p
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   const int wm = warp >> 1, wn = warp & 1;       // 4 x 2 warps
-  const int tm = lane >> 3, tn = lane & 7;       // 4 x 8 threads per warp
+  // 4 x 8 threads per warp: tm from lane bits 0 and 3, tn from bits 1, 2, 4
+  const int tm = (lane & 1) | ((lane >> 2) & 2), tn = ((lane >> 1) & 3) | ((lane >> 2) & 4);
   const int m_in = wm * 32 + tm * 4;             // rows m_in..+3 and m_in+16..+19
   const int n_in = wn * 64 + tn * 4;             // cols n_in..+3 and n_in+32..+35
   int tile = blockIdx.x;

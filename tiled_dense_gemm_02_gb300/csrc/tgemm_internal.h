@@ -101,21 +101,6 @@ inline int64_t sk_workspace_bytes(int workers, int bn) {
   return part + ((flags + 255) / 256) * 256;
 }
 
-struct SimtArgs {
-  int M, N, K;
-  const float* A;
-  int64_t lda;
-  const float* B;
-  int64_t ldb;
-  float* C;
-  int64_t ldc;
-  int vec;              // 1 when A/B/C rows allow 16-byte vector accesses
-  int tiles_n;          // 128-column tiles per tile row (tiles are numbered row by row)
-  int full_tiles;       // tiles [0, full_tiles) are computed whole by one CTA each
-  int split_stage;      // k-stage dividing the two halves of each later tile
-  Epilogue epi;
-};
-
 // Tile shapes of the tensor-core kernel: 128 x BN output tiles, K stages of
 // 64.  BN is one of 64, 128, 192, 224, 256; B is staged in 64-column atoms of
 // 8 KB (the last atom of BN = 224 is half used).
@@ -185,7 +170,6 @@ cudaError_t launch_tc_pair_swap(int tm, int ksub, const CUtensorMap& mapA, const
 // Number of clusters of `cluster` CTAs (2 or 4) of the pair kernel that can be
 // resident at once.
 cudaError_t tc_pair_capacity(int cluster, int* clusters);
-cudaError_t launch_simt(const SimtArgs& args, int64_t units, cudaStream_t stream);
 cudaError_t launch_zero_fill(void* C, int64_t rows, int64_t cols, int64_t ldc, int elem_bytes, cudaStream_t stream);
 // out[j][i] = in[i][j], in rows x cols; elem_bytes 2 or 4; vec: every row of
 // in and out starts on a 16-byte boundary (16-byte accesses)
@@ -194,10 +178,5 @@ cudaError_t launch_transpose(const void* in, int64_t ld_in, void* out, int64_t l
 // K = 0 with a fused epilogue (out_fmt: OutFmt)
 cudaError_t launch_epilogue_fill(void* C, int64_t rows, int64_t cols, int64_t ldc, int out_fmt, const Epilogue& e,
                                  cudaStream_t stream);
-
-// SIMT tile shape.
-constexpr int kSimtBM = 128;
-constexpr int kSimtBN = 128;
-constexpr int kSimtBK = 16;
 
 }  // namespace tgemm
