@@ -6,6 +6,7 @@ import ctypes
 import os
 import re
 
+import numpy as np
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
@@ -386,6 +387,25 @@ def test_simt_split_planning(tg):
     assert plan(tg, 64, 64, 64, dtype=0, simt_split=3)[0] == tg.ERR_INVALID_VALUE
     assert plan(tg, 64, 64, 64, dtype=0, simt_split=-1)[0] == tg.ERR_INVALID_VALUE
     assert plan(tg, 256, 256, 256, dtype=2, simt_split=2)[0] == tg.ERR_INVALID_VALUE
+
+
+def test_simt_split_rule_on_random_shapes(tg):
+    """For seeded random fp32 shapes and SM counts, the plan splits exactly the
+    tiles of a last round that fills at most half of the 2 x SMs slots (auto:
+    K >= 256), and the launch covers every tile once whole or twice as halves."""
+    rng = np.random.default_rng(7)
+    for _ in range(300):
+        M, N = (int(v) for v in rng.integers(1, 6000, size=2))
+        K = int(rng.integers(1, 1200))
+        sms = int(rng.choice([1, 8, 76, 132, 148, 152]))
+        st, p = plan(tg, M, N, K, dtype=0, sms=sms)
+        assert st == tg.OK
+        tiles = -(-M // 128) * -(-N // 128)
+        slots = 2 * sms
+        tail = tiles % slots
+        split = 0 < tail and 2 * tail <= slots and -(-K // 16) >= 16
+        assert (p.tiles_m * p.tiles_n, p.dp_tiles, p.ctas) == (
+            (tiles, tiles - tail, tiles + tail) if split else (tiles, tiles, tiles)), (M, N, K, sms)
 
 
 def test_dispatch_options(tg):
