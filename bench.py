@@ -87,7 +87,7 @@ def dist_env():
 def init_replicas(local: int, backend: str | None = None):
     """One process per GPU, each an independent replica: the process group
     carries only the start/stop barriers and the max-over-ranks timing (no data
-    exchange).  nccl on a GPU machine, gloo where there is none (tests)."""
+    exchange).  nccl where there are GPUs, gloo where there are none (tests)."""
     import torch
     import torch.distributed as dist
     if backend is None:
