@@ -247,6 +247,14 @@ def run_reference(args, w: wl.Workload):
     print(json.dumps(line), flush=True)
 
 
+def kernel_launches_per_call(tg, plan, epilogue: bool) -> int:
+    """Kernels one library call launches for `plan`: a plain fp32 product whose
+    last round of tiles is split into K halves first zeroes the rows of C those
+    halves add into (two launches); everything else is one launch."""
+    split = plan.kernel == tg.KERNEL_SIMT and plan.ctas != plan.tiles_m * plan.tiles_n
+    return 2 if split and not epilogue else 1
+
+
 def run_ours(args, w: wl.Workload):
     import torch
     world, rank, local = dist_env()
@@ -276,10 +284,7 @@ def run_ours(args, w: wl.Workload):
     assert st == tg.OK, tg.status_string(st)
 
     epi = EPILOGUES[args.epilogue]
-    # a plain fp32 product whose last round is split into K halves first zeroes
-    # the rows of C those halves add into: two launches per call
-    simt_split = plan.kernel == tg.KERNEL_SIMT and plan.ctas != plan.tiles_m * plan.tiles_n
-    launches_per_call = 2 if simt_split and epi is None else 1
+    launches_per_call = kernel_launches_per_call(tg, plan, epi is not None)
     bias = torch.linspace(-1.0, 1.0, w.N, dtype=torch.float32, device=dev) if epi and epi[2] else None
     epi_struct = None if epi is None else tg.Epilogue(alpha=epi[0], beta=epi[1],
                                                      bias=bias.data_ptr() if bias is not None else None,

@@ -57,3 +57,25 @@ def test_reference_arm_under_torchrun_prints_once_from_rank_0():
     assert len(lines) == 1, p.stdout
     line = json.loads(lines[0])
     assert line["impl"] == "reference" and line["n_gpus"] == 2 and line["value"] > 0
+
+
+def test_kernel_launch_count_per_call():
+    """gpu_launches counts the zero fill that precedes a split fp32 product;
+    plans come from the host planner (no GPU)."""
+    sys.path.insert(0, ROOT)
+    import bench
+    from tests.conftest import build_library
+    build_library()
+    import tiled_dense_gemm_02_gb300 as tg
+    a, b, c = 0x1000_0000, 0x2000_0000, 0x4000_0000
+
+    def count(M, N, K, dtype, epilogue=False):
+        st, p = tg.plan(M, N, K, a, K, b, N, c, N, dtype, None, sm_count=152)
+        assert st == tg.OK
+        return bench.kernel_launches_per_call(tg, p, epilogue)
+
+    assert count(4096, 4096, 4096, tg.F32) == 2                   # 112 tiles of the last round split
+    assert count(4096, 4096, 4096, tg.F32, epilogue=True) == 1    # an epilogue keeps whole tiles
+    assert count(2048, 2048, 2048, tg.F32) == 1                   # one round, halves would not fit
+    assert count(4096, 4096, 4096, tg.BF16_F32OUT) == 1
+    assert count(1000, 1500, 4096, tg.BF16) == 1
