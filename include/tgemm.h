@@ -76,8 +76,11 @@ enum tgemm_status {
  * take the bulk-tensor (TMA) loads and stores, others take per-thread copies.
  *
  * The call validates its arguments on the host, picks a kernel and a tile
- * shape for the current device, and enqueues one kernel on `stream`; it
- * returns before the product is computed.  It allocates no device memory.
+ * shape for the current device, and enqueues one kernel on `stream` (two for
+ * an fp32 product whose last round of tiles is split into K halves: a fill
+ * that zeroes the rows of C those halves add into, then the product; see
+ * tgemm_options.simt_split); it returns before the product is computed.  It
+ * allocates no device memory.
  * It keeps a small, mutex-guarded host cache of device attributes.  It is
  * safe to call from several host threads.
  *
