@@ -350,8 +350,10 @@ TGEMM_API int tgemm_gemm_batched(int64_t batch, int64_t M, int64_t N, int64_t K,
 
 /* The plan of tgemm_gemm_batched without touching the GPU (pair counts
  * modelled from sm_count as tgemm_plan does).  *launches: kernel launches the
- * call makes (1 for an in-kernel batch, batch for one launch per product, 0
- * when nothing is done).  out describes one launch. */
+ * call makes without an epilogue (1 for an in-kernel batch, batch for one
+ * launch per product, twice that for fp32 products split into K halves, each
+ * preceded by its zero fill; 0 when nothing is done).  out describes one
+ * product's launch. */
 TGEMM_API int tgemm_plan_batched(int64_t batch, int64_t M, int64_t N, int64_t K,
                const void* A, int64_t lda, int64_t stride_a,
                const void* B, int64_t ldb, int64_t stride_b,

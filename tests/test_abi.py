@@ -283,6 +283,9 @@ def test_batched_planning(tg):
     assert st == tg.OK and n == 8
     # fp32 runs the SIMT kernel once per product; batch 1 and 0
     assert tg.plan_batched(5, 64, 64, 64, A, 64, 4096, B, 64, 4096, C, 64, 4096, 0, sm_count=152)[2] == 5
+    # fp32 products whose tiles are split into K halves: a zero fill and the product each
+    assert tg.plan_batched(3, 1024, 1024, 1024, A, 1024, 1 << 20, B, 1024, 1 << 20, C, 1024, 1 << 20, 0,
+                           sm_count=152)[2] == 6
     assert tg.plan_batched(1, M, N, K, A, K, 0, B, N, 0, C, N, 0, 2, sm_count=152)[2] == 1
     assert tg.plan_batched(0, M, N, K, A, K, 0, B, N, 0, C, N, 0, 2, sm_count=152)[2] == 0
     # options that exclude the swapped kernel loop over the products

@@ -1022,7 +1022,10 @@ int tgemm_plan_batched(int64_t batch, int64_t M, int64_t N, int64_t K, const voi
   tgemm::Plan p;
   st = tgemm::make_plan(M, N, K, A, lda, B, ldb, C, ldc, dtype, opts, sms, sms / 2, sms / 4, 0, p, in_batch);
   if (st != TGEMM_OK) return st;
-  if (launches) *launches = p.noop ? 0 : (batch > 1 && p.batch == 1 ? static_cast<int>(batch) : 1);
+  // an fp32 product split into K halves is a zero fill plus the product
+  const int per_product = (p.kernel == TGEMM_KERNEL_SIMT && p.split_stage > 0) ? 2 : 1;
+  if (launches)
+    *launches = p.noop ? 0 : per_product * (batch > 1 && p.batch == 1 ? static_cast<int>(batch) : 1);
   if (out) {
     st = tgemm_plan(M, N, K, A, lda, B, ldb, C, ldc, dtype, opts, 0, sm_count, out);
     if (st == TGEMM_OK && p.batch > 1) {
