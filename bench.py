@@ -14,9 +14,11 @@ copies of A and B, the product, and the device -> host copy of C, all inside
 the event-timed region (with a fused epilogue: torch copies around
 tgemm_gemm_epilogue).
 
-`--impl reference` times the CPU oracle (the plain fp64 triple loop) on a
-bounded sample of rows of the same workload; it is a deliberately slow
-baseline, not a competitor.
+`cpu_baseline` times the CPU oracle (the plain fp64 triple loop, all host
+cores) on a bounded sample of rows of the workload, and `cpu_blocked` its
+cache-blocked fp64 variant on another; both are reported baselines, not
+targets.  `--impl reference` times the oracle alone the same way; it is a
+deliberately slow baseline, not a competitor.
 
 Multi-GPU: the product has no exchange step, so N ranks run N independent
 replicas of the workload (weak scaling) with no collective on the data path;
@@ -217,6 +219,29 @@ def cpu_oracle_sample(w: wl.Workload, A, B, target_seconds: float, rows: int | N
                       f"{dt:.2f} s, fp64 triple loop over the rounded inputs, rows split across threads)"}
 
 
+def cpu_blocked_sample(w: wl.Workload, A, B, target_seconds: float):
+    """Time the cache-blocked fp64 variant of the oracle (all host cores) on
+    the first rows of the product, about `target_seconds` of work."""
+    import oracle
+    fin = wl.IN_FORMAT[w.dtype]
+    threads = os.cpu_count() or 1
+    # two probes separate the per-call cost (decoding B into doubles) from the per-row cost
+    probes, times = (max(1, min(w.M, 2 * threads)), max(1, min(w.M, 6 * threads))), []
+    for n in probes:
+        t0 = time.perf_counter()
+        oracle.gemm_blocked(np.ascontiguousarray(A[:n]), B, fin, n, w.N, w.K, threads=threads)
+        times.append(time.perf_counter() - t0)
+    per_row = max((times[1] - times[0]) / max(probes[1] - probes[0], 1), times[1] / probes[1] / 8, 1e-9)
+    fixed = max(times[0] - per_row * probes[0], 0.0)
+    rows = int(max(probes[1], min(w.M, (target_seconds - fixed) / per_row)))
+    t0 = time.perf_counter()
+    oracle.gemm_blocked(np.ascontiguousarray(A[:rows]), B, fin, rows, w.N, w.K, threads=threads)
+    dt = time.perf_counter() - t0
+    return {"value": 2.0 * rows * w.N * w.K / dt / 1e12, "unit": "TFLOP/s", "cores": threads,
+            "kind": "cache-blocked fp64 variant of the oracle",
+            "sample": f"rows 0..{rows - 1} of the {w.M}x{w.N}x{w.K} product ({dt:.2f} s)"}
+
+
 def run_reference(args, w: wl.Workload):
     world, rank, _ = dist_env()
     if rank != 0:
@@ -387,9 +412,10 @@ def run_ours(args, w: wl.Workload):
                     "peak_source": f"{peak_src} bf16_tflops (burst; kernel timed alone)",
                     "algorithmic_flops_per_launch": w.flops,
                     "compulsory_bytes_per_launch": w.compulsory_bytes}
-    cpu = None
+    cpu = cpu_blocked = None
     if not args.no_cpu_baseline and world == 1:
         cpu = cpu_oracle_sample(w, A, B, args.cpu_seconds)
+        cpu_blocked = cpu_blocked_sample(w, A, B, args.cpu_seconds / 2)
     line = {
         "metric": "GEMM TFLOP/s", "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
@@ -400,6 +426,7 @@ def run_ours(args, w: wl.Workload):
                    "step_ms_median": statistics.median(step_ms), "wall_s": wall},
         "roofline": roofline,
         "cpu_baseline": cpu,
+        "cpu_blocked": cpu_blocked,
         "clocks": clocks,
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": int(A.nbytes + B.nbytes), "d2h_bytes_per_step": int(c.numel() * c.element_size())},

@@ -79,3 +79,17 @@ def test_kernel_launch_count_per_call():
     assert count(2048, 2048, 2048, tg.F32) == 1                   # one round, halves would not fit
     assert count(4096, 4096, 4096, tg.BF16_F32OUT) == 1
     assert count(1000, 1500, 4096, tg.BF16) == 1
+
+
+def test_cpu_baseline_samples_are_bounded():
+    """Both CPU baselines (the oracle and its cache-blocked variant) time a
+    bounded sample of rows and report the cores they used."""
+    sys.path.insert(0, ROOT)
+    import bench
+    import workloads as wl
+    w = wl.BY_NAME["bf16_1000x1500x4096_ragged"]
+    A, B = wl.make_inputs(w)
+    for fn, kind in ((bench.cpu_oracle_sample, "oracle"), (bench.cpu_blocked_sample, "cache-blocked")):
+        r = fn(w, A, B, 0.3)
+        assert r["value"] > 0 and r["unit"] == "TFLOP/s" and r["cores"] >= 1
+        assert kind in r["kind"] and "rows 0.." in r["sample"]
