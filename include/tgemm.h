@@ -133,20 +133,13 @@ typedef struct tgemm_options {
                            0 auto (currently off: on the measured shapes the
                            fix-up costs more than the idle tail), 1 off,
                            2 on whenever the tile count leaves a remainder */
-  int multicast;        /* clusters of two CTA pairs (CTA-pair kernel): 0 auto
-                           (currently off: measured no faster), 1 off, 2 on.
-                           The two pairs of a 4-CTA cluster take
-                           vertically adjacent 256-row tiles of the same
-                           columns and fetch each B tile once, multicast into
-                           both (loads read this GPU's memory only).  Needs
-                           the bulk-tensor store and no stream-K split;
-                           forcing it otherwise is TGEMM_ERR_INVALID_VALUE */
+  int reserved0;        /* must be 0 (TGEMM_ERR_INVALID_VALUE otherwise) */
   int swap_ab;          /* CTA pairs with the MMA's operands exchanged: 0 auto,
                            1 off, 2 on.  Each pair computes a tile_m x 256
                            tile of C as a tile of C^T = B^T A^T, so the tile
                            height can be any of 128, 192, 224, 256 with no
                            partly used shared-memory atoms.  Needs bulk-tensor
-                           operands and no stream-K split or multicast */
+                           operands and no stream-K split */
   int tile_m;           /* tile height of swap_ab = 2 (0 auto): 128, 192, 224
                            or 256; other kernels take 0 */
   int simt_split;       /* fp32 SIMT kernel (TGEMM_F32 only; other dtypes
@@ -193,9 +186,7 @@ typedef struct tgemm_plan_info {
                         ctas = dp_tiles + 2 x the split tiles) */
   int sk_iters;      /* k-stages of the remaining tiles split over the pairs */
   int workspace_bytes; /* workspace the call uses (0 without stream-K) */
-  int cluster_ctas;  /* CTAs per cluster: 1 (one-SM tiles), 2 (a pair) or 4
-                        (two pairs sharing B tiles; tiles_m still counts
-                        256-row tiles, scheduled two at a time) */
+  int cluster_ctas;  /* CTAs per cluster: 1 (one-SM tiles) or 2 (a pair) */
   int swap_ab;       /* 1: pairs with the MMA's operands exchanged (tile_m x
                         256 tiles of C computed as tiles of C^T) */
   int tuned;         /* 1: options from the library's table of measured
@@ -225,7 +216,8 @@ TGEMM_API int tgemm_plan(int64_t M, int64_t N, int64_t K,
  *
  * tgemm_gemm_ws: tgemm_gemm_ex with a workspace.  `workspace` is device memory
  * owned by the caller, 256-byte aligned, zero-initialised before its first use
- * (later calls need no clearing); `workspace_bytes` smaller than
+ * (later calls need no clearing, whatever their shapes: the flags always take
+ * the first 4 KiB and the partial sums follow); `workspace_bytes` smaller than
  * tgemm_workspace_size (including 0 with a NULL workspace) makes the call run
  * without stream-K.  Two calls that may run at the same time on the GPU must
  * not share a workspace.  Its contents after a call are unspecified.
@@ -271,8 +263,13 @@ TGEMM_API int tgemm_gemm_ws(int64_t M, int64_t N, int64_t K,
  *  - Every call shares the one array.  Calls that may run at the same time on
  *    the GPU (different streams, or several host threads) race on it and can
  *    produce wrong results; order them on one stream or use tgemm_gemm_ws.
- *  - Nothing in the array needs clearing between calls: a flag marks a partial
- *    sum with the value of the call that wrote it, and the array starts zeroed.
+ *  - Nothing in the array needs clearing between calls: the array starts
+ *    zeroed, its first 4 KiB hold only flags, and a flag marks a partial sum
+ *    with a value that differs from call to call, so whatever an earlier call
+ *    left behind is never taken for this call's data.
+ *  - The device address is looked up once per device and kept for the life of
+ *    the process: after cudaDeviceReset (or any tear-down of the device's
+ *    primary context) this entry point must not be called again.
  *  Other arguments, status codes and semantics: as tgemm_gemm_ex.
  */
 #define TGEMM_NOALLOC_SCRATCH_BYTES ((size_t)20 * 1024 * 1024 + 4096)

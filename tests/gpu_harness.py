@@ -121,9 +121,33 @@ def run_gpu(A_bits: np.ndarray, B_bits: np.ndarray, M: int, N: int, K: int, dtyp
     return res
 
 
-def check_full(res: Result, A_bits, B_bits, M, N, K, dtype, label=""):
+# full oracle products of named workloads, kept for the tests of one process
+# that compare several launches of the same workload (at most three: 4096^2
+# doubles are 128 MB per array)
+_WORKLOAD_REF: dict = {}
+
+
+def workload_reference(name: str):
+    """(A bits, B bits, C_ref, S) of a named workload: the oracle's full product,
+    computed once per process."""
+    if name not in _WORKLOAD_REF:
+        if len(_WORKLOAD_REF) >= 3:
+            _WORKLOAD_REF.pop(next(iter(_WORKLOAD_REF)))
+        w = wl.BY_NAME[name]
+        A, B = wl.make_inputs(w)
+        ref, S = oracle.gemm(np.ascontiguousarray(A), np.ascontiguousarray(B), wl.IN_FORMAT[w.dtype], w.M, w.N, w.K)
+        _WORKLOAD_REF[name] = (A, B, ref, S)
+    return _WORKLOAD_REF[name]
+
+
+def check_full(res: Result, A_bits, B_bits, M, N, K, dtype, label="", reference=None):
+    """Every element of C against the oracle; `reference` = (C_ref, S) when the
+    caller already holds the oracle's product of these inputs."""
     fin, fout = wl.IN_FORMAT[dtype], wl.OUT_FORMAT[dtype]
-    ref, S = oracle.gemm(np.ascontiguousarray(A_bits), np.ascontiguousarray(B_bits), fin, M, N, K)
+    if reference is None:
+        ref, S = oracle.gemm(np.ascontiguousarray(A_bits), np.ascontiguousarray(B_bits), fin, M, N, K)
+    else:
+        ref, S = reference
     ok, ratio, where = tolerance.check(res.got, ref, S, fin, fout)
     assert res.guard_ok, f"{label}: guard band around C overwritten"
     assert res.pad_ok, f"{label}: ldc padding of C overwritten"
@@ -138,6 +162,18 @@ def check_sampled(res: Result, A_bits, B_bits, K, dtype, rows, cols, label=""):
     ok, ratio, where = tolerance.check(res.got[rows, cols], ref, S, fin, fout)
     assert res.guard_ok and res.pad_ok, f"{label}: guard band or padding overwritten"
     assert ok, f"{label}: error/bound {ratio:.3g} at sample {where} (row {rows[where]}, col {cols[where]})"
+    return ratio
+
+
+def check_block(res: Result, A_bits, B_bits, K, dtype, r0, r1, c0, c1, label=""):
+    """Every element of the block C[r0:r1, c0:c1] against the oracle's product
+    of those rows of A and columns of B."""
+    fin, fout = wl.IN_FORMAT[dtype], wl.OUT_FORMAT[dtype]
+    ref, S = oracle.gemm(np.ascontiguousarray(A_bits[r0:r1]), np.ascontiguousarray(B_bits[:, c0:c1]), fin,
+                         r1 - r0, c1 - c0, K)
+    ok, ratio, where = tolerance.check(res.got[r0:r1, c0:c1], ref, S, fin, fout)
+    assert res.guard_ok and res.pad_ok, f"{label}: guard band or padding overwritten"
+    assert ok, f"{label}: error/bound {ratio:.3g} at block offset {where} of rows {r0}.. cols {c0}.."
     return ratio
 
 

@@ -44,6 +44,19 @@ def test_library_exports_every_declared_symbol(tg):
     assert tg.version() == 10000
 
 
+def test_noalloc_scratch_size_matches_header(tg):
+    """The binding's copy of TGEMM_NOALLOC_SCRATCH_BYTES is the header's value:
+    4 KiB of stream-K flags and 20 MiB of partial sums, enough for every pair
+    of 152 SMs at the widest tile."""
+    text = open(HEADER).read()
+    m = re.search(r"#define\s+TGEMM_NOALLOC_SCRATCH_BYTES\s+\(\(size_t\)(\d+)\s*\*\s*(\d+)\s*\*\s*(\d+)\s*\+\s*(\d+)\)",
+                  text)
+    assert m, "TGEMM_NOALLOC_SCRATCH_BYTES not found in the header"
+    a, b, c, d = (int(g) for g in m.groups())
+    assert a * b * c + d == tg.NOALLOC_SCRATCH_BYTES
+    assert 4096 + 76 * 2 * 4 * 32 * 256 * 4 <= tg.NOALLOC_SCRATCH_BYTES
+
+
 def header_struct_fields(name):
     """(field, element count) of `typedef struct name {...} name;` in the header,
     which declares int fields only."""
@@ -259,9 +272,8 @@ def test_swapped_pair_planning(tg):
     # off when asked, or when another option excludes it
     assert plan(tg, 4096, 4096, 4096, dtype=3, sms=152, swap_ab=1)[1].swap_ab == 0
     assert plan(tg, 4096, 4096, 4096, dtype=3, sms=152, tile_n=224)[1].swap_ab == 0
-    assert plan(tg, 4096, 4096, 4096, dtype=3, sms=152, multicast=2)[1].swap_ab == 0
     # refused combinations
-    for bad in ({"swap_ab": 2, "stream_k": 2}, {"swap_ab": 2, "multicast": 2}, {"swap_ab": 2, "cta_group": 1},
+    for bad in ({"swap_ab": 2, "stream_k": 2}, {"swap_ab": 2, "cta_group": 1},
                 {"swap_ab": 2, "tile_n": 224}, {"swap_ab": 2, "tile_m": 160}, {"tile_m": 224}, {"swap_ab": 3}):
         assert plan(tg, 4096, 4096, 4096, dtype=3, **bad)[0] == tg.ERR_INVALID_VALUE, bad
     assert plan(tg, 1000, 1500, 4096, dtype=2, swap_ab=2)[0] == tg.ERR_INVALID_VALUE  # per-thread copies
@@ -337,33 +349,19 @@ def test_gemm_host_validation_returns_before_the_device(tg):
     assert g(1 << 31, 4, 4, AH, 4, BH, 4, CH, 4, 2, DA, DB, DC) == tg.ERR_TOO_LARGE
 
 
-def test_two_pair_cluster_planning(tg):
-    """Clusters of two CTA pairs sharing B (multicast): only when asked for,
-    with bulk-tensor operands and store, without stream-K; 512-row super-tiles
-    are scheduled, four CTAs per cluster."""
+def test_cluster_planning(tg):
+    """Tensor-core pairs run in 2-CTA clusters, one-SM tiles and the SIMT
+    kernel in none; the reserved option field must stay 0."""
     st, p = plan(tg, 4096, 4096, 4096, dtype=3, sms=152)
-    assert st == tg.OK and p.cluster_ctas == 2          # auto: one pair per cluster
-    st, p = plan(tg, 4096, 4096, 4096, dtype=3, sms=152, multicast=2)
-    assert st == tg.OK and p.cluster_ctas == 4 and p.cta_group == 2 and p.tile_m == 256
-    assert p.ctas == 152 and p.tiles_m == 16 and p.dp_tiles == 8 * p.tiles_n
-    # an odd count of 256-row tiles: the last super-tile has one pair's rows below C
-    st, p = plan(tg, 600, 512, 256, dtype=2, sms=152, multicast=2, tile_n=256)
-    assert st == tg.OK and (p.tiles_m, p.tiles_n, p.dp_tiles, p.ctas) == (3, 2, 4, 16)
-    # a CTA cap counts whole clusters of four
-    st, p = plan(tg, 4096, 4096, 4096, dtype=3, sms=152, multicast=2, max_ctas=10)
-    assert st == tg.OK and p.ctas == 8
-    assert plan(tg, 4096, 4096, 4096, dtype=3, sms=152, multicast=2, max_ctas=3)[0] == tg.ERR_INVALID_VALUE
-    # refused combinations
-    assert plan(tg, 4096, 4096, 4096, dtype=3, multicast=2, cta_group=1)[0] == tg.ERR_INVALID_VALUE
-    assert plan(tg, 4096, 4096, 4096, dtype=3, multicast=2, stream_k=2)[0] == tg.ERR_INVALID_VALUE
-    assert plan(tg, 4096, 4096, 4096, dtype=3, multicast=2, store_mode=2)[0] == tg.ERR_INVALID_VALUE
-    assert plan(tg, 4096, 4096, 4096, dtype=3, multicast=3)[0] == tg.ERR_INVALID_VALUE
-    assert plan(tg, 1000, 1500, 4096, dtype=2, multicast=2)[0] == tg.ERR_INVALID_VALUE  # per-thread copies
-    assert plan(tg, 512, 260, 512, dtype=2, multicast=2)[0] == tg.ERR_INVALID_VALUE     # C rows not 16-byte units
-    st, p = plan(tg, 4096, 4096, 4096, dtype=3, sms=152, multicast=1, cta_group=2, swap_ab=1)
+    assert st == tg.OK and p.cluster_ctas == 2
+    st, p = plan(tg, 4096, 4096, 4096, dtype=3, sms=152, cta_group=2, swap_ab=1)
     assert st == tg.OK and p.cluster_ctas == 2 and p.swap_ab == 0
+    st, p = plan(tg, 4096, 4096, 4096, dtype=3, sms=152, cta_group=1)
+    assert st == tg.OK and p.cluster_ctas == 1
     st, p = plan(tg, 300, 300, 300, dtype=0)
     assert st == tg.OK and p.cluster_ctas == 1
+    for v in (1, 2, -1):
+        assert plan(tg, 4096, 4096, 4096, dtype=3, reserved0=v)[0] == tg.ERR_INVALID_VALUE
 
 
 def test_simt_split_planning(tg):
@@ -442,7 +440,7 @@ def test_stream_k_planning(tg):
     # 4096^3 on 152 SMs: 256 pair tiles on 76 pairs leave 28 tiles for the tail
     st, p = plan(tg, 4096, 4096, 4096, dtype=3, sms=152, cta_group=2, tile_n=256, stream_k=2)
     assert st == tg.OK and p.sk_iters == 0 and p.workspace_bytes == 0     # no workspace: whole tiles
-    need = 76 * 2 * 4 * 32 * 256 * 4 + 2560
+    need = 4096 + 76 * 2 * 4 * 32 * 256 * 4    # the flag region, then the partial sums
     st, p = plan(tg, 4096, 4096, 4096, dtype=3, sms=152, cta_group=2, tile_n=256, ws=need)
     assert p.sk_iters == 0                                                # auto: off
     st, p = plan(tg, 4096, 4096, 4096, dtype=3, sms=152, cta_group=2, tile_n=256, ws=need, stream_k=2)

@@ -25,10 +25,9 @@ def gpu():
     torch.cuda.set_device(0)
 
 
-@pytest.mark.parametrize("opts", [{"cta_group": 1}, {"cta_group": 2, "multicast": 1, "swap_ab": 1}, {"multicast": 2},
-                                  {"swap_ab": 2}, {"kernel": 2}, {"kernel": 2, "cta_group": 2}],
-                         ids=["one_sm", "cta_pair", "two_pairs_multicast", "pair_swapped", "copy_producer",
-                              "copy_pair"])
+@pytest.mark.parametrize("opts", [{"cta_group": 1}, {"cta_group": 2, "swap_ab": 1}, {"swap_ab": 2}, {"kernel": 2},
+                                  {"kernel": 2, "cta_group": 2}],
+                         ids=["one_sm", "cta_pair", "pair_swapped", "copy_producer", "copy_pair"])
 def test_bounded_wait_reports_timeout_and_context_survives(opts):
     lib = H.tg()
     M, N, K = 512, 512, 256

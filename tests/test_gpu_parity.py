@@ -42,16 +42,28 @@ def test_workload_full_product(name):
     H.check_full(res, A, B, w.M, w.N, w.K, w.dtype, name)
 
 
-@pytest.mark.parametrize("name", ["bf16_4096x4096x4096_f32out", "f32_4096x4096x4096", "f32_2048x2048x2048",
-                                  "f16_8192x8192x8192"])
-def test_workload_sampled(name):
+@pytest.mark.parametrize("name", ["bf16_4096x4096x4096_f32out", "f32_4096x4096x4096", "f32_2048x2048x2048"])
+def test_workload_full_size_every_element(name):
     """Full-size products in the launch configuration the benchmark times,
-    checked on every element of the border rows/columns and random samples."""
+    every element against the oracle's full product."""
     w = wl.BY_NAME[name]
+    A, B, ref, S = H.workload_reference(name)
+    res = H.run_gpu(A, B, w.M, w.N, w.K, w.dtype)
+    H.check_full(res, A, B, w.M, w.N, w.K, w.dtype, name, reference=(ref, S))
+
+
+def test_workload_f16_8192_bands():
+    """f16 8192^3 in the benchmark's launch configuration: every element of one
+    whole 256-row band of tiles and one whole 256-column band (about 4.2 M
+    outputs, every tile the band crosses), plus the border rows and columns
+    and random samples."""
+    w = wl.BY_NAME["f16_8192x8192x8192"]
     A, B = wl.make_inputs(w)
     res = H.run_gpu(A, B, w.M, w.N, w.K, w.dtype)
+    H.check_block(res, A, B, w.K, w.dtype, 17 * 256, 18 * 256, 0, w.N, "tile row 17")
+    H.check_block(res, A, B, w.K, w.dtype, 0, w.M, 23 * 256, 24 * 256, "tile column 23")
     rows, cols = H.sample_positions(w.M, w.N, 4096, seed=99)
-    H.check_sampled(res, A, B, w.K, w.dtype, rows, cols, name)
+    H.check_sampled(res, A, B, w.K, w.dtype, rows, cols, "f16 8192^3")
 
 
 # ---------------------------------------------- fp32 tiles split into K halves
@@ -105,16 +117,14 @@ def test_simt_split_is_deterministic():
         assert np.array_equal(r1.raw, r2.raw)
 
 
-@pytest.mark.parametrize("multicast", [1, 2], ids=["one_pair_clusters", "two_pair_clusters"])
-def test_headline_both_cluster_sizes(multicast):
-    """The bf16 4096^3 -> fp32 product on CTA pairs in 2-CTA clusters and in
-    4-CTA clusters sharing B tiles, sampled as above."""
+def test_headline_on_plain_pairs():
+    """The bf16 4096^3 -> fp32 product on CTA pairs without the operand
+    exchange (256 x BN tiles), every element."""
     w = wl.BY_NAME["bf16_4096x4096x4096_f32out"]
-    A, B = wl.make_inputs(w)
-    res = H.run_gpu(A, B, w.M, w.N, w.K, w.dtype, options={"cta_group": 2, "multicast": multicast, "swap_ab": 1})
-    assert res.plan.cluster_ctas == 2 * multicast
-    rows, cols = H.sample_positions(w.M, w.N, 4096, seed=98)
-    H.check_sampled(res, A, B, w.K, w.dtype, rows, cols, f"multicast {multicast}")
+    A, B, ref, S = H.workload_reference(w.name)
+    res = H.run_gpu(A, B, w.M, w.N, w.K, w.dtype, options={"cta_group": 2, "swap_ab": 1})
+    assert res.plan.cluster_ctas == 2 and res.plan.swap_ab == 0
+    H.check_full(res, A, B, w.M, w.N, w.K, w.dtype, "plain pairs", reference=(ref, S))
 
 
 # ------------------------------------------------------------ shape sweeps
@@ -226,7 +236,7 @@ def test_pair_kernel(tile_n, dtype, store_mode):
     and the unstaged variant with a deeper ring (store_mode 2)."""
     M, N, K = 300, 520, 200
     A, B, res = case(M, N, K, dtype, seed=34, options={"cta_group": 2, "tile_n": tile_n, "store_mode": store_mode,
-                                                             "multicast": 1, "swap_ab": 1})
+                                                             "swap_ab": 1})
     assert res.plan.cta_group == 2 and res.plan.tile_m == 256 and res.plan.tile_n == tile_n
     assert res.plan.cluster_ctas == 2
     H.check_full(res, A, B, M, N, K, dtype, f"pair tile_n {tile_n}")
@@ -241,7 +251,7 @@ def test_pair_kernel_persistent(store_mode, max_ctas, tile_k):
     M, N, K = 1100, 1300, 330
     A, B, res = case(M, N, K, wl.BF16_F32OUT, seed=35, lda=336, ldb=1304,
                      options={"cta_group": 2, "tile_n": 256, "max_ctas": max_ctas, "store_mode": store_mode,
-                              "tile_k": tile_k, "multicast": 1, "swap_ab": 1})
+                              "tile_k": tile_k, "swap_ab": 1})
     assert res.plan.cta_group == 2 and res.plan.cluster_ctas == 2
     if max_ctas:
         assert res.plan.ctas == max_ctas
@@ -256,53 +266,9 @@ def test_pair_kernel_k_depths(K, tile_k):
     M, N = 257, 260
     lda = (K + 7) // 8 * 8   # 16-byte rows for the bulk-tensor loads of the pair kernel
     A, B, res = case(M, N, K, wl.BF16, seed=36, lda=lda, ldb=264,
-                     options={"cta_group": 2, "tile_n": 128, "tile_k": tile_k, "multicast": 1, "swap_ab": 1})
+                     options={"cta_group": 2, "tile_n": 128, "tile_k": tile_k, "swap_ab": 1})
     assert res.plan.tile_k == tile_k and res.plan.cluster_ctas == 2
     H.check_full(res, A, B, M, N, K, wl.BF16, f"pair K {K}")
-
-
-# ---------------------------------- clusters of two CTA pairs sharing B tiles
-
-@pytest.mark.parametrize("M", [300, 600])
-@pytest.mark.parametrize("tile_n", [128, 192, 224, 256])
-@pytest.mark.parametrize("dtype", TC_DTYPES, ids=lambda d: wl.DTYPE_NAMES[d])
-def test_quad_kernel(tile_n, dtype, M):
-    """Two pairs stacked along M sharing each B tile (multicast loads): ragged
-    N and a K tail; M = 300 puts 44 rows in the second pair's tile, M = 600
-    gives three 256-row tiles, so the second super-tile's lower pair lies
-    entirely below C (computed, never stored)."""
-    N, K = 520, 200
-    A, B, res = case(M, N, K, dtype, seed=37, options={"cta_group": 2, "tile_n": tile_n, "multicast": 2})
-    assert res.plan.cluster_ctas == 4 and res.plan.tile_m == 256 and res.plan.tile_n == tile_n
-    H.check_full(res, A, B, M, N, K, dtype, f"quad tile_n {tile_n} M {M}")
-
-
-@pytest.mark.parametrize("tile_k", [64, 128])
-@pytest.mark.parametrize("max_ctas,group_m", [(4, 0), (8, 1), (12, 2), (0, 0)])
-def test_quad_kernel_persistent(max_ctas, group_m, tile_k):
-    """One to three clusters walking many 512 x 256 super-tiles (every ring
-    and accumulator phase), with several raster groups, and the full grid."""
-    M, N, K = 1100, 1300, 330
-    A, B, res = case(M, N, K, wl.BF16_F32OUT, seed=38, lda=336, ldb=1304,
-                     options={"tile_n": 256, "max_ctas": max_ctas, "group_m": group_m, "tile_k": tile_k,
-                              "multicast": 2})
-    assert res.plan.cluster_ctas == 4
-    if max_ctas:
-        assert res.plan.ctas == max_ctas
-    H.check_full(res, A, B, M, N, K, wl.BF16_F32OUT, f"quad ctas {max_ctas} group {group_m}")
-
-
-@pytest.mark.parametrize("tile_k", [64, 128])
-@pytest.mark.parametrize("K", [16, 32, 33, 64, 96, 129, 448])
-def test_quad_kernel_k_depths(K, tile_k):
-    """K around the 32-row halves each pair loads of a 64-deep B sub-block
-    and around the stage depth."""
-    M, N = 600, 264  # rows of C in whole 16-byte units: the bulk-tensor store
-    lda = (K + 7) // 8 * 8
-    A, B, res = case(M, N, K, wl.BF16, seed=39, lda=lda,
-                     options={"tile_n": 128, "tile_k": tile_k, "multicast": 2})
-    assert res.plan.tile_k == tile_k and res.plan.cluster_ctas == 4
-    H.check_full(res, A, B, M, N, K, wl.BF16, f"quad K {K}")
 
 
 # ------------------------------- pairs with the MMA's operands exchanged
@@ -349,13 +315,12 @@ def test_swap_kernel_k_depths(K, tile_k):
 
 @pytest.mark.parametrize("tile_m", [192, 224, 256])
 def test_swap_kernel_headline(tile_m):
-    """bf16 4096^3 -> fp32 in tile_m x 256 swapped tiles, sampled."""
+    """bf16 4096^3 -> fp32 in tile_m x 256 swapped tiles, every element."""
     w = wl.BY_NAME["bf16_4096x4096x4096_f32out"]
-    A, B = wl.make_inputs(w)
+    A, B, ref, S = H.workload_reference(w.name)
     res = H.run_gpu(A, B, w.M, w.N, w.K, w.dtype, options={"swap_ab": 2, "tile_m": tile_m})
     assert res.plan.swap_ab == 1 and res.plan.tile_m == tile_m
-    rows, cols = H.sample_positions(w.M, w.N, 4096, seed=97)
-    H.check_sampled(res, A, B, w.K, w.dtype, rows, cols, f"swap {tile_m}")
+    H.check_full(res, A, B, w.M, w.N, w.K, w.dtype, f"swap {tile_m}", reference=(ref, S))
 
 
 # ------------------------------------------------------- scheduler and edges

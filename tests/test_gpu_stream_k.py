@@ -85,14 +85,10 @@ def test_stream_k_deterministic_and_workspace_reuse():
 def test_stream_k_workloads(name):
     """Full-size workloads with the stream-K tail forced on (tile choice automatic)."""
     w = wl.BY_NAME[name]
-    A, B = wl.make_inputs(w)
+    A, B, ref, S = H.workload_reference(name)
     res = H.run_gpu(A, B, w.M, w.N, w.K, w.dtype, workspace=True, options={"stream_k": 2})
     assert res.plan.sk_iters > 0
-    if w.M * w.N <= 2048 * 2048:
-        H.check_full(res, A, B, w.M, w.N, w.K, w.dtype, name)
-    else:
-        rows, cols = H.sample_positions(w.M, w.N, 4096, seed=98)
-        H.check_sampled(res, A, B, w.K, w.dtype, rows, cols, name)
+    H.check_full(res, A, B, w.M, w.N, w.K, w.dtype, name, reference=(ref, S))
 
 
 def test_workspace_too_small_runs_whole_tiles():

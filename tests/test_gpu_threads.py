@@ -17,7 +17,7 @@ pytestmark = pytest.mark.gpu
 
 CASES = [(300, 520, 200, wl.BF16, None), (257, 264, 136, wl.F16, {"swap_ab": 2}),
          (129, 257, 33, wl.F32, None), (600, 264, 448, wl.BF16_F32OUT, {"cta_group": 2, "swap_ab": 1}),
-         (500, 300, 96, wl.F16, {"cta_group": 1}), (256, 256, 1024, wl.BF16, {"multicast": 2})]
+         (500, 300, 96, wl.F16, {"cta_group": 1}), (256, 256, 1024, wl.BF16, {"cta_group": 2, "tile_k": 128, "swap_ab": 1})]
 
 
 def test_concurrent_host_threads_on_separate_streams():

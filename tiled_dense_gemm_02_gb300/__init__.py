@@ -38,7 +38,7 @@ class Options(ctypes.Structure):
     _fields_ = [("kernel", ctypes.c_int), ("tile_n", ctypes.c_int), ("group_m", ctypes.c_int),
                 ("max_ctas", ctypes.c_int), ("store_mode", ctypes.c_int), ("wait_timeout_us", ctypes.c_int),
                 ("inject_fault", ctypes.c_int), ("cta_group", ctypes.c_int), ("tile_k", ctypes.c_int),
-                ("stream_k", ctypes.c_int), ("multicast", ctypes.c_int),
+                ("stream_k", ctypes.c_int), ("reserved0", ctypes.c_int),
                 ("swap_ab", ctypes.c_int), ("tile_m", ctypes.c_int), ("simt_split", ctypes.c_int),
                 ("reserved", ctypes.c_int * 2)]
 

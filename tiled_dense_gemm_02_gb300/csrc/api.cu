@@ -35,7 +35,6 @@ struct DeviceInfo {
   int sm_count = 0;
   unsigned int* status = nullptr;
   int pair_capacity = 0;  // resident CTA pairs of the pair kernel (0 = not queried)
-  int quad_capacity = 0;  // resident clusters of two CTA pairs (0 = not queried)
 };
 
 std::mutex g_mutex;
@@ -167,7 +166,6 @@ struct Plan {
   bool swap = false;  // pair kernel with the MMA's operands exchanged (tile tm x 256)
   bool copy_pair = false;  // pair kernel with B staged by per-thread copies (A by bulk-tensor copies)
   int tm = 0;         // tile height of the swapped kernel
-  int cluster = 2;  // CTAs per cluster of the pair kernel: 2, or 4 (two pairs sharing B)
   int ksub = 1;  // 64-deep K sub-blocks per shared-memory stage (pair kernel)
   int bn = 256, stages = 4, tiles_m = 0, tiles_n = 0, ctas = 0, group_m = 1;
   int a_copy = 0, b_copy = 0, store = 0;
@@ -246,24 +244,6 @@ int pick_pair_tile_n(int64_t M, int64_t N, int pairs, bool stream_k, double* cos
   return best;
 }
 
-// Tile width of clusters of two pairs: each round runs `quads` 512 x BN
-// super-tiles; rows beyond the last 256-row tile are computed and dropped.
-int pick_quad_tile_n(int64_t M, int64_t N, int quads, double* cost) {
-  int best = 256;
-  double best_t = 1e300;
-  const int64_t super_rows = ((M + 2 * kTileM - 1) / (2 * kTileM) + 1) / 2;
-  for (int bn : {256, 224, 192, 128}) {
-    const int64_t units = super_rows * ((N + bn - 1) / bn);
-    const double t = static_cast<double>((units + quads - 1) / quads) * bn / pair_rate(bn);
-    if (t < best_t * 0.999) {
-      best_t = t;
-      best = bn;
-    }
-  }
-  if (cost) *cost = best_t;
-  return best;
-}
-
 // Per-SM throughput per tile row of the swapped pair kernel (tile tm x 256),
 // in the units of width_rate, measured on GB300 with bf16 8192^3 (1915, 1806,
 // 1653 and 1397 TFLOP/s for tm = 256, 224, 192, 128).  It falls with tm
@@ -307,8 +287,8 @@ const TunedShape kTuned[] = {
 };
 
 const TunedShape* tuned_entry(int64_t M, int64_t N, int64_t K, int dtype, const tgemm_options& o) {
-  if (o.kernel || o.tile_n || o.group_m || o.max_ctas || o.cta_group || o.tile_k || o.stream_k || o.multicast ||
-      o.swap_ab || o.tile_m)
+  if (o.kernel || o.tile_n || o.group_m || o.max_ctas || o.cta_group || o.tile_k || o.stream_k || o.swap_ab ||
+      o.tile_m)
     return nullptr;
   for (const TunedShape& t : kTuned)
     if (t.dtype == dtype && t.M == M && t.N == N && t.K == K) return &t;
@@ -316,13 +296,13 @@ const TunedShape* tuned_entry(int64_t M, int64_t N, int64_t K, int dtype, const 
 }
 
 int make_plan_core(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb,
-                   const void* C, int64_t ldc, int dtype, const tgemm_options* o, int sms, int pair_cap, int quad_cap,
+                   const void* C, int64_t ldc, int dtype, const tgemm_options* o, int sms, int pair_cap,
                    int64_t workspace_bytes, Plan& p, int64_t batch);
 
 // The plan of a call: the tuned options of its shape when there is an entry
 // and they suit this call (pointers, alignment), else the heuristics.
 int make_plan(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb,
-              const void* C, int64_t ldc, int dtype, const tgemm_options* o, int sms, int pair_cap, int quad_cap,
+              const void* C, int64_t ldc, int dtype, const tgemm_options* o, int sms, int pair_cap,
               int64_t workspace_bytes, Plan& p, int64_t batch = 1) {
   // every plan starts from the defaults: a Plan filled by an earlier call (the
   // device-free validation pass of run(), say) must not leak its choices
@@ -341,19 +321,19 @@ int make_plan(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const
       tuned.tile_k = t->tile_k;
       tuned.group_m = t->group_m;
       Plan q;
-      if (make_plan_core(M, N, K, A, lda, B, ldb, C, ldc, dtype, &tuned, sms, pair_cap, quad_cap, workspace_bytes, q,
-                         batch) == TGEMM_OK) {
+      if (make_plan_core(M, N, K, A, lda, B, ldb, C, ldc, dtype, &tuned, sms, pair_cap, workspace_bytes, q, batch) ==
+          TGEMM_OK) {
         p = q;
         p.tuned = true;
         return TGEMM_OK;
       }
     }
   }
-  return make_plan_core(M, N, K, A, lda, B, ldb, C, ldc, dtype, o, sms, pair_cap, quad_cap, workspace_bytes, p, batch);
+  return make_plan_core(M, N, K, A, lda, B, ldb, C, ldc, dtype, o, sms, pair_cap, workspace_bytes, p, batch);
 }
 
 int make_plan_core(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb,
-                   const void* C, int64_t ldc, int dtype, const tgemm_options* o, int sms, int pair_cap, int quad_cap,
+                   const void* C, int64_t ldc, int dtype, const tgemm_options* o, int sms, int pair_cap,
                    int64_t workspace_bytes, Plan& p, int64_t batch) {
   if (dtype < TGEMM_F32 || dtype > TGEMM_F16_F32OUT) return TGEMM_ERR_UNSUPPORTED_DTYPE;
   if (M < 0 || N < 0 || K < 0) return TGEMM_ERR_INVALID_VALUE;
@@ -367,11 +347,8 @@ int make_plan_core(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, 
   if (opt.tile_n != 0 && !tc_valid_bn(opt.tile_n)) return TGEMM_ERR_INVALID_VALUE;
   if (opt.group_m < 0 || opt.max_ctas < 0 || opt.store_mode < 0 || opt.store_mode > 2 || opt.wait_timeout_us < 0 ||
       opt.cta_group < 0 || opt.cta_group > 2 || (opt.tile_k != 0 && opt.tile_k != 64 && opt.tile_k != 128) ||
-      opt.stream_k < 0 || opt.stream_k > 2 || opt.multicast < 0 || opt.multicast > 2 ||
-      (opt.multicast == 2 && (opt.stream_k == 2 || opt.cta_group == 1 || opt.store_mode == 2)) ||
-      opt.swap_ab < 0 || opt.swap_ab > 2 ||
-      (opt.swap_ab == 2 && (opt.stream_k == 2 || opt.cta_group == 1 || opt.multicast == 2 ||
-                            (opt.tile_n != 0 && opt.tile_n != 256))) ||
+      opt.stream_k < 0 || opt.stream_k > 2 || opt.reserved0 != 0 || opt.swap_ab < 0 || opt.swap_ab > 2 ||
+      (opt.swap_ab == 2 && (opt.stream_k == 2 || opt.cta_group == 1 || (opt.tile_n != 0 && opt.tile_n != 256))) ||
       (opt.tile_m != 0 && (opt.swap_ab != 2 || !tc2_valid_bn(opt.tile_m))))
     return TGEMM_ERR_INVALID_VALUE;
   if (M == 0 || N == 0) {
@@ -453,18 +430,17 @@ int make_plan_core(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, 
   }
   if (opt.store_mode == 1 && !c_tma) return TGEMM_ERR_INVALID_VALUE;
   p.store = (c_tma && opt.store_mode != 2) ? 0 : gc;
-  // a CTA cap limits every kind of worker (clusters of four need four CTAs)
+  // a CTA cap limits every kind of worker
   if (opt.max_ctas) {
     sms = std::min(sms, opt.max_ctas);
     pair_cap = std::min(pair_cap, std::max(1, opt.max_ctas / 2));
-    quad_cap = std::min(quad_cap, opt.max_ctas / 4);
   }
   // B rows that rule out bulk-tensor copies (A's do not): CTA pairs that copy
   // B per thread, each CTA its half of the tile's columns, move half the B
   // bytes per SM and FLOP of the one-SM copy kernel, which per-thread copies
   // bound.  Cost: rounds x the B columns one SM copies per tile.
   const bool copy_pair_ok = p.kernel == TGEMM_KERNEL_TC_COPY && a_tma && pair_cap > 0 &&
-                            opt.cta_group != 1 && opt.stream_k != 2 && opt.multicast != 2 && opt.swap_ab != 2 &&
+                            opt.cta_group != 1 && opt.stream_k != 2 && opt.swap_ab != 2 &&
                             opt.tile_k != 128 && opt.store_mode != 1 &&
                             (opt.tile_n == 0 || opt.tile_n == 128 || opt.tile_n == 256) &&
                             (opt.kernel == TGEMM_KERNEL_TC_COPY ? opt.cta_group == 2 : p.b_copy != 0);
@@ -512,23 +488,15 @@ int make_plan_core(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, 
   const bool pair_ok = p.kernel == TGEMM_KERNEL_TC_TMA && pair_cap > 0 &&
                        (opt.tile_n == 0 || tc2_valid_bn(opt.tile_n));
   if (opt.cta_group == 2 && !pair_ok) return TGEMM_ERR_INVALID_VALUE;
-  double cost1 = 0, cost2 = 1e300, cost4 = 1e300, cost_s = 1e300;
+  double cost1 = 0, cost2 = 1e300, cost_s = 1e300;
   const int bn1 = opt.tile_n ? opt.tile_n : pick_tile_n(M, N, sms, &cost1);
-  int bn2 = 0, bn4 = 0, tm_s = 0;
+  int bn2 = 0, tm_s = 0;
   if (pair_ok && opt.cta_group != 1) {
     // stream-K needs a workspace of at most sk_workspace_bytes(pairs, 256)
     const bool sk_possible = opt.stream_k == 2 && workspace_bytes >= sk_workspace_bytes(pair_cap, 256);
     bn2 = opt.tile_n ? opt.tile_n : pick_pair_tile_n(M, N, pair_cap, sk_possible, &cost2);
-    // Clusters of two pairs that share each B tile through multicast loads:
-    // bulk-tensor stores only, no stream-K split.  Auto leaves them off: on
-    // GB300 they halve the L2 reads of B but measured no faster (bf16 4096^3
-    // within 2 %, 8192^3 4 % slower), so the operand reads from L2 are not
-    // what bounds the pair kernel.
-    const bool quad_ok = quad_cap > 0 && p.store == 0 && opt.stream_k != 2 && opt.multicast == 2;
-    if (quad_ok) bn4 = opt.tile_n ? opt.tile_n : pick_quad_tile_n(M, N, quad_cap, &cost4);
-    // Pairs with the MMA's operands exchanged (tile tm x 256): no stream-K
-    // split, no multicast clusters.
-    const bool swap_ok = opt.stream_k != 2 && opt.multicast != 2 && opt.swap_ab != 1 &&
+    // Pairs with the MMA's operands exchanged (tile tm x 256): no stream-K split.
+    const bool swap_ok = opt.stream_k != 2 && opt.swap_ab != 1 &&
                          (opt.tile_n == 0 || opt.tile_n == 256);
     if (swap_ok) {
       tm_s = opt.tile_m ? opt.tile_m : pick_swap_tile_m(M, N, pair_cap, &cost_s);
@@ -542,34 +510,24 @@ int make_plan_core(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, 
       const int64_t t2 = ((M + 2 * kTileM - 1) / (2 * kTileM)) * ((N + bn2 - 1) / bn2);
       cost1 = static_cast<double>((t1 + sms - 1) / sms) * bn1 / width_rate(bn1);
       cost2 = static_cast<double>((t2 + pair_cap - 1) / pair_cap) * bn2 / pair_rate(bn2);
-      if (quad_ok) {
-        const int64_t t4 = (((M + 2 * kTileM - 1) / (2 * kTileM) + 1) / 2) * ((N + bn4 - 1) / bn4);
-        cost4 = static_cast<double>((t4 + quad_cap - 1) / quad_cap) * bn4 / pair_rate(bn4);
-      }
     }
   }
-  p.pair = bn2 != 0 && (opt.cta_group == 2 || opt.multicast == 2 || opt.swap_ab == 2 ||
-                        (opt.cta_group == 0 && std::min(std::min(cost2, cost4), cost_s) < cost1));
-  if (p.pair && tm_s != 0 && (opt.swap_ab == 2 || (cost_s < cost2 && cost_s < cost4))) {
+  p.pair = bn2 != 0 && (opt.cta_group == 2 || opt.swap_ab == 2 || (opt.cta_group == 0 && std::min(cost2, cost_s) < cost1));
+  if (p.pair && tm_s != 0 && (opt.swap_ab == 2 || cost_s < cost2)) {
     p.swap = true;
     p.tm = tm_s;
     bn2 = 256;
-  } else if (p.pair && bn4 != 0 && (opt.multicast == 2 || cost4 < cost2)) {
-    p.cluster = 4;
-    bn2 = bn4;
   }
-  if (opt.multicast == 2 && p.cluster != 4) return TGEMM_ERR_INVALID_VALUE;
   if (opt.swap_ab == 2 && !p.swap) return TGEMM_ERR_INVALID_VALUE;
   // A strided batch runs in one launch of the swapped kernel, whose tile list
   // spans all matrices; when that kernel cannot serve it, each matrix is
   // launched on its own with the plan of a single product.
   if (batch > 1) {
-    const bool in_kernel = pair_ok && opt.cta_group != 1 && opt.stream_k != 2 && opt.multicast != 2 &&
-                           opt.swap_ab != 1 && (opt.tile_n == 0 || opt.tile_n == 256);
+    const bool in_kernel = pair_ok && opt.cta_group != 1 && opt.stream_k != 2 && opt.swap_ab != 1 &&
+                           (opt.tile_n == 0 || opt.tile_n == 256);
     if (in_kernel) {
       p.pair = true;
       p.swap = true;
-      p.cluster = 2;
       p.tm = opt.tile_m ? opt.tile_m : pick_swap_tile_m(M, N, pair_cap, nullptr, batch);
       bn2 = 256;
       p.batch = batch;
@@ -590,8 +548,7 @@ int make_plan_core(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, 
   p.tiles_n = static_cast<int>((N + p.bn - 1) / p.bn);
   const int64_t tiles = int64_t(p.tiles_m) * p.tiles_n * p.batch;
   if (tiles >= (int64_t(1) << 31)) return TGEMM_ERR_TOO_LARGE;
-  // rows of scheduling units: 512-row super-tiles for clusters of two pairs
-  const int sched_rows = p.cluster == 4 ? (p.tiles_m + 1) / 2 : p.tiles_m;
+  const int sched_rows = p.tiles_m;
   // Raster group height.  8 keeps a round's A rows and B columns in L2 when
   // the operands do not fit there; when they do (A + B within half of L2),
   // 4 measured faster on GB300 (bf16 4096^3: +2.5 %; 8192^3 and
@@ -602,10 +559,7 @@ int make_plan_core(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, 
   p.k_blocks = static_cast<int>((K + kTileK * p.ksub - 1) / (kTileK * p.ksub));
   p.dp_tiles = static_cast<int>(int64_t(sched_rows) * p.tiles_n * p.batch);
   int64_t ctas;
-  if (p.pair && p.cluster == 4) {
-    int64_t cap = quad_cap;
-    ctas = 4 * std::min<int64_t>(p.dp_tiles, cap);
-  } else if (p.pair) {
+  if (p.pair) {
     int64_t cap = pair_cap;
     int64_t pairs = std::min<int64_t>(tiles, cap);
     // Stream-K tail: when the last round of tiles would leave pairs idle, the
@@ -618,7 +572,7 @@ int make_plan_core(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, 
     if (opt.stream_k == 2) {
       const int64_t rem = tiles % cap;
       const int64_t sk_iters = rem * p.k_blocks;
-      const bool worth = rem != 0 && sk_iters >= cap;
+      const bool worth = rem != 0 && sk_iters >= cap && cap <= kSkMaxWorkers;
       const int64_t need = sk_workspace_bytes(static_cast<int>(cap), p.bn);
       if (worth && workspace_bytes >= need && sk_iters < (int64_t(1) << 31)) {
         pairs = cap;
@@ -683,15 +637,14 @@ int encode_3d(CUtensorMap* map, CUtensorMapDataType type, const void* base, int6
   return TGEMM_OK;
 }
 
-// Resident clusters of the pair kernel on the current device, for clusters of
-// 2 CTAs (one pair) or 4 (two pairs), queried once.  0 when the query fails:
-// that cluster size is then not used.
-int cluster_capacity(DeviceInfo* d, int cluster) {
+// Resident CTA pairs of the pair kernel on the current device, queried once.
+// 0 when the query fails: pairs are then not used.
+int pair_capacity(DeviceInfo* d) {
   std::lock_guard<std::mutex> lock(g_mutex);
-  int& cap = cluster == 4 ? d->quad_capacity : d->pair_capacity;
+  int& cap = d->pair_capacity;
   if (cap == 0) {
     int n = 0;
-    if (tc_pair_capacity(cluster, &n) != cudaSuccess || n < 1) {
+    if (tc_pair_capacity(&n) != cudaSuccess || n < 1) {
       cudaGetLastError();
       n = -1;
     }
@@ -699,8 +652,6 @@ int cluster_capacity(DeviceInfo* d, int cluster) {
   }
   return cap > 0 ? cap : 0;
 }
-int pair_capacity(DeviceInfo* d) { return cluster_capacity(d, 2); }
-int quad_capacity(DeviceInfo* d) { return cluster_capacity(d, 4); }
 
 // Epoch of stream-K flags: a flag equal to the current call's epoch marks a
 // partial sum written by this call.  Starts at a per-process pseudo-random
@@ -770,7 +721,7 @@ int run(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void*
   if (workspace_bytes < 0 || (workspace_bytes > 0 && (!workspace || reinterpret_cast<uint64_t>(workspace) % 256)))
     return TGEMM_ERR_INVALID_VALUE;
   const int64_t in_batch = (bt.count > 1 && batch_tma_ok(bt, dtype)) ? bt.count : 1;
-  int st = make_plan(M, N, K, A, lda, B, ldb, C, ldc, dtype, o, 1, 1, 1, workspace_bytes, p, in_batch);
+  int st = make_plan(M, N, K, A, lda, B, ldb, C, ldc, dtype, o, 1, 1, workspace_bytes, p, in_batch);
   if (st != TGEMM_OK || p.noop) return st;
   Epilogue ep;
   st = make_epilogue(epi_in, M, N, C, ldc, dtype, ep);
@@ -779,8 +730,8 @@ int run(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void*
   DeviceInfo* dev = nullptr;
   st = device_info(&dev);
   if (st != TGEMM_OK) return st;
-  st = make_plan(M, N, K, A, lda, B, ldb, C, ldc, dtype, o, dev->sm_count, pair_capacity(dev), quad_capacity(dev),
-                 workspace_bytes, p, in_batch);
+  st = make_plan(M, N, K, A, lda, B, ldb, C, ldc, dtype, o, dev->sm_count, pair_capacity(dev), workspace_bytes, p,
+                 in_batch);
   if (st != TGEMM_OK) return st;
   if (bt.count > 1 && p.batch == 1) {
     // no kernel indexes this batch: one launch per matrix, each a single product
@@ -856,14 +807,12 @@ int run(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void*
   if (!p.swap && p.a_copy == 0 &&
       (st = encode_2d(&mA, tmap_type(2, bf16), A, K, M, lda * 2, kTileK, kTileM)) != TGEMM_OK)
     return st;
-  // clusters of two pairs load each 64-row B atom as two 32-row halves
-  const uint32_t b_rows = p.cluster == 4 ? kTileK / 2 : kTileK;
   if (!p.swap && p.b_copy == 0 &&
-      (st = encode_2d(&mB, tmap_type(2, bf16), B, N, K, ldb * 2, 64, b_rows)) != TGEMM_OK)
+      (st = encode_2d(&mB, tmap_type(2, bf16), B, N, K, ldb * 2, 64, kTileK)) != TGEMM_OK)
     return st;
   // the pair kernel's last, partial B atom (bn/2 = 96 or 112 columns per CTA)
   const uint32_t b_tail = (p.pair && !p.swap) ? static_cast<uint32_t>((p.bn / 2) % 64) : 0u;
-  if (b_tail && (st = encode_2d(&mBt, tmap_type(2, bf16), B, N, K, ldb * 2, b_tail, b_rows)) != TGEMM_OK) return st;
+  if (b_tail && (st = encode_2d(&mBt, tmap_type(2, bf16), B, N, K, ldb * 2, b_tail, kTileK)) != TGEMM_OK) return st;
   // C: 128-byte swizzled 32-row boxes; the swapped kernel writes unswizzled 32 x 32 blocks
   if (!p.swap && p.store == 0 &&
       (st = encode_2d(&mC, tmap_type(eo, dtype == TGEMM_BF16), C, N, M, ldc * eo, 128 / eo, 32)) != TGEMM_OK)
@@ -872,7 +821,7 @@ int run(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void*
   a.M = static_cast<int>(M);
   a.N = static_cast<int>(N);
   a.K = static_cast<int>(K);
-  a.tiles_m = p.cluster == 4 ? (p.tiles_m + 1) / 2 : p.tiles_m;  // scheduling rows
+  a.tiles_m = p.tiles_m;
   a.tiles_n = p.tiles_n;
   a.tiles_per = a.tiles_m * p.tiles_n;
   a.num_tiles = static_cast<int>(a.tiles_per * p.batch);
@@ -886,10 +835,8 @@ int run(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void*
   a.sk_flags = nullptr;
   a.sk_epoch = 0;
   if (p.sk_iters) {
-    const int workers = p.ctas / 2;
-    a.sk_partials = static_cast<float*>(workspace);
-    a.sk_flags = reinterpret_cast<unsigned int*>(static_cast<char*>(workspace) +
-                                                 int64_t(workers) * sk_partial_floats(p.bn) * 4);
+    a.sk_flags = static_cast<unsigned int*>(workspace);
+    a.sk_partials = reinterpret_cast<float*>(static_cast<char*>(workspace) + kSkFlagBytes);
     a.sk_epoch = next_epoch();
   }
   a.group_m = p.group_m;
@@ -926,7 +873,7 @@ int run(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void*
   else if (p.swap)
     e = launch_tc_pair_swap(p.tm, p.ksub, mA, mB, mC, a, p.ctas / 2, stream);
   else if (p.pair)
-    e = launch_tc_pair(p.bn, p.store == 0, p.ksub, p.cluster, mA, mB, mBt, mC, a, p.ctas / p.cluster, stream);
+    e = launch_tc_pair(p.bn, p.store == 0, p.ksub, mA, mB, mBt, mC, a, p.ctas / 2, stream);
   else
     e = launch_tc(p.bn, p.kernel == TGEMM_KERNEL_TC_COPY, mA, mB, mC, a, p.ctas, stream);
   return e == cudaSuccess ? TGEMM_OK : cuda_fail(e, "tensor-core kernel launch");
@@ -1020,7 +967,7 @@ int tgemm_plan_batched(int64_t batch, int64_t M, int64_t N, int64_t K, const voi
   const int64_t in_batch = (batch > 1 && tgemm::batch_tma_ok(bt, dtype)) ? batch : 1;
   const int sms = sm_count < 1 ? 1 : sm_count;
   tgemm::Plan p;
-  st = tgemm::make_plan(M, N, K, A, lda, B, ldb, C, ldc, dtype, opts, sms, sms / 2, sms / 4, 0, p, in_batch);
+  st = tgemm::make_plan(M, N, K, A, lda, B, ldb, C, ldc, dtype, opts, sms, sms / 2, 0, p, in_batch);
   if (st != TGEMM_OK) return st;
   // an fp32 product split into K halves is a zero fill plus the product
   const int per_product = (p.kernel == TGEMM_KERNEL_SIMT && p.split_stage > 0) ? 2 : 1;
@@ -1168,13 +1115,13 @@ int tgemm_workspace_size(int64_t M, int64_t N, int64_t K, const void* A, int64_t
   if (!bytes) return TGEMM_ERR_INVALID_VALUE;
   *bytes = 0;
   tgemm::Plan p;
-  int st = tgemm::make_plan(M, N, K, A, lda, B, ldb, C, ldc, dtype, opts, 1, 1, 1, 0, p);
+  int st = tgemm::make_plan(M, N, K, A, lda, B, ldb, C, ldc, dtype, opts, 1, 1, 0, p);
   if (st != TGEMM_OK || p.noop || p.zero) return st;
   tgemm::DeviceInfo* dev = nullptr;
   st = tgemm::device_info(&dev);
   if (st != TGEMM_OK) return st;
   st = tgemm::make_plan(M, N, K, A, lda, B, ldb, C, ldc, dtype, opts, dev->sm_count, tgemm::pair_capacity(dev),
-                        tgemm::quad_capacity(dev), INT64_MAX, p);
+                        INT64_MAX, p);
   if (st == TGEMM_OK) *bytes = static_cast<size_t>(p.workspace);
   return st;
 }
@@ -1185,7 +1132,7 @@ int tgemm_plan(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, cons
   tgemm::Plan p;
   const int sms = sm_count < 1 ? 1 : sm_count;
   const int64_t ws = workspace_bytes > static_cast<size_t>(INT64_MAX) ? INT64_MAX : static_cast<int64_t>(workspace_bytes);
-  const int st = tgemm::make_plan(M, N, K, A, lda, B, ldb, C, ldc, dtype, opts, sms, sms / 2, sms / 4, ws, p);
+  const int st = tgemm::make_plan(M, N, K, A, lda, B, ldb, C, ldc, dtype, opts, sms, sms / 2, ws, p);
   if (out) {
     std::memset(out, 0, sizeof *out);
     if (st == TGEMM_OK && !p.noop && !p.zero) {
@@ -1203,7 +1150,7 @@ int tgemm_plan(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, cons
       out->store_bytes = p.store;
       out->smem_bytes = p.smem;
       out->cta_group = p.pair ? 2 : 1;
-      out->cluster_ctas = p.pair ? p.cluster : 1;
+      out->cluster_ctas = p.pair ? 2 : 1;
       out->swap_ab = p.swap ? 1 : 0;
       out->tuned = p.tuned ? 1 : 0;
       out->dp_tiles = p.dp_tiles;
@@ -1262,7 +1209,8 @@ int tgemm_version(void) { return TGEMM_VERSION; }
 // static device array below instead of a caller workspace.  The array belongs
 // to the library image: every GPU that loads the library holds it until the
 // process exits.
-static constexpr size_t kNoAllocScratchBytes = TGEMM_NOALLOC_SCRATCH_BYTES;  // 20 MiB + 4 KiB
+static constexpr size_t kNoAllocScratchBytes = TGEMM_NOALLOC_SCRATCH_BYTES;  // 4 KiB of flags + 20 MiB
+static_assert(kNoAllocScratchBytes == size_t(tgemm::kSkFlagBytes) + (size_t(20) << 20), "scratch layout");
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
 namespace {
@@ -1300,14 +1248,14 @@ extern "C" int tgemm_gemm_noalloc(int64_t M, int64_t N, int64_t K, const void* A
   if (o.stream_k == 0) o.stream_k = 2;  // this entry point is the stream-K variant
   // validation first (no CUDA call on bad arguments)
   tgemm::Plan p;
-  int st = tgemm::make_plan(M, N, K, A, lda, B, ldb, C, ldc, dtype, &o, 1, 1, 1, 0, p);
+  int st = tgemm::make_plan(M, N, K, A, lda, B, ldb, C, ldc, dtype, &o, 1, 1, 0, p);
   if (st != TGEMM_OK || p.noop) return st;
   tgemm::DeviceInfo* dev = nullptr;
   st = tgemm::device_info(&dev);
   if (st != TGEMM_OK) return st;
   // scratch the call would use with no limit; beyond the static array: rejected
   st = tgemm::make_plan(M, N, K, A, lda, B, ldb, C, ldc, dtype, &o, dev->sm_count, tgemm::pair_capacity(dev),
-                        tgemm::quad_capacity(dev), INT64_MAX, p);
+                        INT64_MAX, p);
   if (st != TGEMM_OK) return st;
   if (static_cast<size_t>(p.workspace) > kNoAllocScratchBytes) return TGEMM_ERR_TOO_LARGE;
   void* scratch = nullptr;

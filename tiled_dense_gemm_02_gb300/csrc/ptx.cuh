@@ -334,20 +334,6 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
       : "memory");
 }
 
-// Tile load written at the same shared-memory offset into every CTA of
-// `cta_mask` (cluster multicast, this GPU's memory only).  The bytes landing in
-// each destination CTA are signalled on the mbarrier at the offset of
-// `bar_cluster` in the even CTA of that destination's pair, so `bar_cluster`
-// names an even CTA's barrier.
-__device__ __forceinline__ void tma_load_2d_pair_multicast(uint32_t dst, const CUtensorMap* map, int32_t x,
-                                                           int32_t y, uint32_t bar_cluster, uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-      ".cta_group::2 [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar_cluster), "h"(cta_mask)
-      : "memory");
-}
-
 // The same for a 3-D tensor (a strided batch of matrices; z = the matrix).
 __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap* map, int32_t x, int32_t y,
                                                  int32_t z, uint32_t bar_cluster) {

@@ -22,18 +22,6 @@
 // Every wait is bounded (see tc_common.cuh); CTAs of a cluster only meet at
 // the two cluster barriers (after set-up and before tensor memory is freed),
 // which all always reach.
-//
-// Clusters of four CTAs (CL = 4) hold two pairs stacked along M: pair 0 takes
-// rows [512 i, 512 i + 256) and pair 1 the next 256 rows of the same column
-// block, so both read the same B tile.  Each B tile is then fetched once per
-// cluster instead of once per pair: the CTAs of the same half of the two pairs
-// (ranks h and h + 2) each load 32 of the 64 rows of every B sub-block and
-// multicast them to both, which cuts the bytes each SM pulls from L2 per
-// stage by a quarter (by the same argument of "Tiling 策略与内存层次优化",
-// §约束一: a larger block of outputs shares each staged operand).  A stage of
-// a CTA is then written by three producers, so it is free only once both
-// pairs' MMAs have read it: each leader's stage commit is multicast to all
-// four CTAs and the empty barriers count two arrivals.
 #include <atomic>
 
 #include "tc_common.cuh"
@@ -41,7 +29,7 @@
 namespace tgemm {
 namespace {
 
-template <int BN, bool kStaged, int KSUB, int CL>
+template <int BN, bool kStaged, int KSUB>
 __global__ void __launch_bounds__(32 * (2 + kEpiWarps), 1)
     tc_gemm_2sm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
                        const __grid_constant__ CUtensorMap mapB_tail,
@@ -64,7 +52,6 @@ __global__ void __launch_bounds__(32 * (2 + kEpiWarps), 1)
   static_assert(tc2_valid_bn(BN), "pair tile width");
   static_assert(tc2_smem_bytes(BN, kStaged, KSUB) <= kSmemLimit, "shared memory per CTA");
   static_assert(STAGES >= 3, "ring depth");
-  static_assert(CL == 2 || CL == 4, "CTAs per cluster");
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -85,19 +72,18 @@ __global__ void __launch_bounds__(32 * (2 + kEpiWarps), 1)
   const int lane = threadIdx.x & 31;
   const uint32_t rank = ptx::cluster_ctarank();
   const uint32_t half = rank & 1u;         // which 128 rows of the pair's tile
-  const uint32_t sub = rank >> 1;          // which pair of the cluster (CL = 4)
   const bool leader = half == 0;           // issues the pair's MMAs
-  const uint32_t leader_rank = rank & ~1u;
-  const int worker = blockIdx.x / CL;      // persistent worker: one cluster
-  const int workers = gridDim.x / CL;
+  const uint32_t leader_rank = 0;
+  const int worker = blockIdx.x / 2;       // persistent worker: one pair
+  const int workers = gridDim.x / 2;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       ptx::mbar_init(ptx::smem_u32(&full[s]), 1);   // leader only: its producer's expect_tx
-      ptx::mbar_init(ptx::smem_u32(&empty[s]), CL / 2);  // multicast MMA commit of each pair
+      ptx::mbar_init(ptx::smem_u32(&empty[s]), 1);   // the pair's MMA commit, to both CTAs
     }
     for (int b = 0; b < 2; ++b) {
-      ptx::mbar_init(ptx::smem_u32(&acc_full[b]), 1);              // multicast MMA commit
+      ptx::mbar_init(ptx::smem_u32(&acc_full[b]), 1);              // the pair's MMA commit, to both CTAs
       ptx::mbar_init(ptx::smem_u32(&acc_empty[b]), 2 * kEpiWarps);  // leader only: both CTAs' epilogues
     }
     ptx::mbar_init(ptx::smem_u32(drain), 1);
@@ -115,7 +101,7 @@ __global__ void __launch_bounds__(32 * (2 + kEpiWarps), 1)
     ptx::tmem_alloc_pair(ptx::smem_u32(tmem_slot), TMEM_COLS);
     ptx::tmem_relinquish_pair();
   }
-  // barriers of all CTAs are initialised before any remote arrive or multicast
+  // both CTAs' barriers are initialised before any remote arrive
   ptx::tc_fence_before_sync();
   ptx::cluster_sync();
   ptx::tc_fence_after_sync();
@@ -130,13 +116,11 @@ __global__ void __launch_bounds__(32 * (2 + kEpiWarps), 1)
       int stage = 0;
       uint32_t phase = 0, filled = 0, last_parity = 0;
       bool ok = true;
-      // CL = 4: this CTA's B rows go to itself and to the same half of the other pair
-      const uint16_t b_mask = static_cast<uint16_t>((1u << half) | (1u << (half + 2)));
       Unit u;
       for (int ui = 0; ok && worker_unit(args, worker, workers, ui, u); ++ui) {
         int mb, nb;
         tile_coords(u.tile, args, mb, nb);
-        const int a_row = (mb * (CL / 2) + static_cast<int>(sub)) * 2 * kTileM + static_cast<int>(half) * kTileM;
+        const int a_row = mb * 2 * kTileM + static_cast<int>(half) * kTileM;
         for (int kb = u.lo; kb < u.hi; ++kb) {
           if (!wait_bounded(ptx::smem_u32(&empty[stage]), phase ^ 1u, ctl, SITE_PRODUCER_EMPTY)) {
             ok = false;
@@ -154,14 +138,7 @@ __global__ void __launch_bounds__(32 * (2 + kEpiWarps), 1)
               const uint32_t dst = ptx::smem_u32(sB + stage * B_BYTES + s * B_SUB + j * 8192);
               const int col = nb * BN + static_cast<int>(half) * BNH + j * 64;
               const CUtensorMap* map = j < B_FULL ? &mapB : &mapB_tail;
-              if constexpr (CL == 2) {
-                ptx::tma_load_2d_pair(dst, map, col, k0, fb);
-              } else {
-                // rows [32 sub, 32 sub + 32) of the 64-row atom (the swizzle
-                // pattern repeats every 8 rows, so the half lands in place)
-                ptx::tma_load_2d_pair_multicast(dst + sub * 4096u, map, col, k0 + static_cast<int>(sub) * 32, fb,
-                                                b_mask);
-              }
+              ptx::tma_load_2d_pair(dst, map, col, k0, fb);
             }
           }
           filled |= 1u << stage;
@@ -190,10 +167,6 @@ __global__ void __launch_bounds__(32 * (2 + kEpiWarps), 1)
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
-      // a stage is free once every pair of the cluster has read it; the
-      // accumulator belongs to this pair alone
-      constexpr uint16_t kStageMask = CL == 4 ? 0xF : 0x3;
-      const uint16_t acc_mask = static_cast<uint16_t>(0x3u << (2 * sub));
       Unit u;
       for (int ui = 0; ok && worker_unit(args, worker, workers, ui, u); ++ui) {
         if (!wait_bounded(ptx::smem_u32(&acc_empty[acc]), acc_phase ^ 1u, ctl, SITE_MMA_ACC_EMPTY)) break;
@@ -214,14 +187,14 @@ __global__ void __launch_bounds__(32 * (2 + kEpiWarps), 1)
               ptx::tc_mma_f16_pair(d_tmem, sw128_desc(a0 + s * A_SUB + k * 32, 16, 1024),
                                    sw128_desc(b0 + s * B_SUB + k * 2048, 8192, 1024), args.idesc,
                                    (kb != u.lo || s != 0 || k != 0) ? 1u : 0u);
-          ptx::tc_commit_pair_multicast(ptx::smem_u32(&empty[stage]), kStageMask);
+          ptx::tc_commit_pair_multicast(ptx::smem_u32(&empty[stage]), 0x3);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        ptx::tc_commit_pair_multicast(ptx::smem_u32(&acc_full[acc]), acc_mask);
+        ptx::tc_commit_pair_multicast(ptx::smem_u32(&acc_full[acc]), 0x3);
         acc ^= 1;
         if (acc == 0) acc_phase ^= 1u;
       }
@@ -248,7 +221,7 @@ __global__ void __launch_bounds__(32 * (2 + kEpiWarps), 1)
       if (!warp_wait(ptx::smem_u32(&acc_full[acc]), acc_phase, ctl, SITE_EPI_ACC_FULL)) break;
       ptx::tc_fence_after_sync();
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * ACC);
-      const int row0 = (mb * (CL / 2) + static_cast<int>(sub)) * 2 * kTileM + static_cast<int>(half) * kTileM + q * 32;
+      const int row0 = mb * 2 * kTileM + static_cast<int>(half) * kTileM + q * 32;
       if (u.role == UNIT_PARTIAL) {
         epilogue_partial<BN>(tbase, lane, args.sk_partials + worker * slot_floats + warp_off);
         __threadfence();
@@ -291,11 +264,11 @@ __global__ void __launch_bounds__(32 * (2 + kEpiWarps), 1)
   }
 }
 
-template <int BN, bool kStaged, int KSUB, int CL>
+template <int BN, bool kStaged, int KSUB>
 cudaError_t launch_pair(const CUtensorMap& mA, const CUtensorMap& mB, const CUtensorMap& mBt, const CUtensorMap& mC,
-                        const TcArgs& args, int clusters, cudaStream_t stream) {
+                        const TcArgs& args, int pairs, cudaStream_t stream) {
   constexpr int smem = tc2_smem_bytes(BN, kStaged, KSUB);
-  auto kernel = tc_gemm_2sm_kernel<BN, kStaged, KSUB, CL>;
+  auto kernel = tc_gemm_2sm_kernel<BN, kStaged, KSUB>;
   static std::atomic<uint64_t> done_mask{0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -307,13 +280,13 @@ cudaError_t launch_pair(const CUtensorMap& mA, const CUtensorMap& mB, const CUte
     done_mask.fetch_or(bit, std::memory_order_acq_rel);
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(CL * clusters, 1, 1);
+  cfg.gridDim = dim3(2 * pairs, 1, 1);
   cfg.blockDim = dim3(32 * (2 + kEpiWarps), 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = CL;
+  attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
@@ -321,41 +294,16 @@ cudaError_t launch_pair(const CUtensorMap& mA, const CUtensorMap& mB, const CUte
   return cudaLaunchKernelEx(&cfg, kernel, mA, mB, mBt, mC, args);
 }
 
-// Resident clusters of the 256-wide instantiation, which stands for all
-// widths (same threads, shared memory within a few KB of the limit).
-template <int CL>
-cudaError_t max_clusters(int* out) {
-  constexpr int smem = tc2_smem_bytes(256, true, 1);
-  auto kernel = tc_gemm_2sm_kernel<256, true, 1, CL>;
-  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e != cudaSuccess) return e;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(CL, 1, 1);
-  cfg.blockDim = dim3(32 * (2 + kEpiWarps), 1, 1);
-  cfg.dynamicSmemBytes = smem;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = CL;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaOccupancyMaxActiveClusters(out, kernel, &cfg);
-}
-
 }  // namespace
 
-cudaError_t launch_tc_pair(int bn, bool staged, int ksub, int cluster, const CUtensorMap& mA, const CUtensorMap& mB,
-                           const CUtensorMap& mBt, const CUtensorMap& mC, const TcArgs& args, int clusters,
+cudaError_t launch_tc_pair(int bn, bool staged, int ksub, const CUtensorMap& mA, const CUtensorMap& mB,
+                           const CUtensorMap& mBt, const CUtensorMap& mC, const TcArgs& args, int pairs,
                            cudaStream_t stream) {
-  // clusters of two pairs are built for the bulk-tensor store only
-  if (cluster == 4 && !staged) return cudaErrorInvalidValue;
-#define TGEMM_PAIR_LAUNCH(BNV, ST, KS, CLV) launch_pair<BNV, ST, KS, CLV>(mA, mB, mBt, mC, args, clusters, stream)
-#define TGEMM_PAIR_BN(BNV)                                                                        \
-  case BNV:                                                                                       \
-    if (cluster == 4) return ksub == 2 ? TGEMM_PAIR_LAUNCH(BNV, true, 2, 4) : TGEMM_PAIR_LAUNCH(BNV, true, 1, 4); \
-    if (ksub == 2) return staged ? TGEMM_PAIR_LAUNCH(BNV, true, 2, 2) : TGEMM_PAIR_LAUNCH(BNV, false, 2, 2);      \
-    return staged ? TGEMM_PAIR_LAUNCH(BNV, true, 1, 2) : TGEMM_PAIR_LAUNCH(BNV, false, 1, 2);
+#define TGEMM_PAIR_LAUNCH(BNV, ST, KS) launch_pair<BNV, ST, KS>(mA, mB, mBt, mC, args, pairs, stream)
+#define TGEMM_PAIR_BN(BNV)                                                                                   \
+  case BNV:                                                                                                  \
+    if (ksub == 2) return staged ? TGEMM_PAIR_LAUNCH(BNV, true, 2) : TGEMM_PAIR_LAUNCH(BNV, false, 2); \
+    return staged ? TGEMM_PAIR_LAUNCH(BNV, true, 1) : TGEMM_PAIR_LAUNCH(BNV, false, 1);
   switch (bn) {
     TGEMM_PAIR_BN(128)
     TGEMM_PAIR_BN(192)
@@ -367,12 +315,25 @@ cudaError_t launch_tc_pair(int bn, bool staged, int ksub, int cluster, const CUt
 #undef TGEMM_PAIR_LAUNCH
 }
 
-cudaError_t tc_pair_capacity(int cluster, int* clusters) {
-  switch (cluster) {
-    case 2: return max_clusters<2>(clusters);
-    case 4: return max_clusters<4>(clusters);
-    default: return cudaErrorInvalidValue;
-  }
+// Resident pairs of the 256-wide instantiation, which stands for all widths
+// (same threads, shared memory within a few KB of the limit).
+cudaError_t tc_pair_capacity(int* pairs) {
+  constexpr int smem = tc2_smem_bytes(256, true, 1);
+  auto kernel = tc_gemm_2sm_kernel<256, true, 1>;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2, 1, 1);
+  cfg.blockDim = dim3(32 * (2 + kEpiWarps), 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaOccupancyMaxActiveClusters(pairs, kernel, &cfg);
 }
 
 }  // namespace tgemm

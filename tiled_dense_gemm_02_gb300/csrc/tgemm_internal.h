@@ -95,10 +95,14 @@ struct TcArgs {
 
 // Workspace of the stream-K tail for `workers` CTA pairs and tile width bn.
 constexpr int64_t sk_partial_floats(int bn) { return int64_t(2) * 4 * 32 * bn; }
+// Workspace layout of a stream-K split: the flags (8 words per worker) always
+// take the first kSkFlagBytes, whatever the worker count and tile width, and
+// the partial sums follow.  So a flag word of one call can only ever land on a
+// flag word of an earlier call (whose epoch differs), never on partial sums.
+constexpr int64_t kSkFlagBytes = 4096;
+constexpr int kSkMaxWorkers = static_cast<int>(kSkFlagBytes / (8 * 4));
 inline int64_t sk_workspace_bytes(int workers, int bn) {
-  const int64_t part = int64_t(workers) * sk_partial_floats(bn) * 4;
-  const int64_t flags = int64_t(workers) * 8 * 4;
-  return part + ((flags + 255) / 256) * 256;
+  return kSkFlagBytes + int64_t(workers) * sk_partial_floats(bn) * 4;
 }
 
 // Tile shapes of the tensor-core kernel: 128 x BN output tiles, K stages of
@@ -152,14 +156,12 @@ int copy_pair_smem(int bn);
 // Launchers (return the cudaError_t of the launch).
 cudaError_t launch_tc(int bn, bool copy, const CUtensorMap& mapA, const CUtensorMap& mapB, const CUtensorMap& mapC,
                       const TcArgs& args, int ctas, cudaStream_t stream);
-// `cluster`: CTAs per cluster, 2 (one pair) or 4 (two pairs stacked along M
-// that share each B tile through multicast loads; the B boxes are then 32 rows
-// deep and args.tiles_m counts 512-row super-tiles).  `clusters` clusters.
-// mapB_tail: B with a box (bn/2) % 64 columns wide, for the last, partial
-// 64-column atom of a CTA's bn/2 columns (unused when bn/2 is a multiple of 64).
-cudaError_t launch_tc_pair(int bn, bool staged, int ksub, int cluster, const CUtensorMap& mapA,
-                           const CUtensorMap& mapB, const CUtensorMap& mapB_tail, const CUtensorMap& mapC,
-                           const TcArgs& args, int clusters, cudaStream_t stream);
+// `pairs` CTA pairs (2-CTA clusters).  mapB_tail: B with a box (bn/2) % 64
+// columns wide, for the last, partial 64-column atom of a CTA's bn/2 columns
+// (unused when bn/2 is a multiple of 64).
+cudaError_t launch_tc_pair(int bn, bool staged, int ksub, const CUtensorMap& mapA, const CUtensorMap& mapB,
+                           const CUtensorMap& mapB_tail, const CUtensorMap& mapC, const TcArgs& args, int pairs,
+                           cudaStream_t stream);
 // CTA pairs computing TM x 256 tiles of C as tiles of C^T = B^T A^T (the MMA's
 // M along C's columns, its N = tm along C's rows).  The maps are 3-D (matrix
 // index last, extent 1 for an operand whose batch stride is 0): mapA's box is
@@ -167,9 +169,9 @@ cudaError_t launch_tc_pair(int bn, bool staged, int ksub, int cluster, const CUt
 cudaError_t launch_tc_pair_copy(int bn, const CUtensorMap& mapA, const TcArgs& args, int pairs, cudaStream_t stream);
 cudaError_t launch_tc_pair_swap(int tm, int ksub, const CUtensorMap& mapA, const CUtensorMap& mapB,
                                 const CUtensorMap& mapC, const TcArgs& args, int pairs, cudaStream_t stream);
-// Number of clusters of `cluster` CTAs (2 or 4) of the pair kernel that can be
+// Number of CTA pairs (2-CTA clusters) of the pair kernel that can be
 // resident at once.
-cudaError_t tc_pair_capacity(int cluster, int* clusters);
+cudaError_t tc_pair_capacity(int* pairs);
 cudaError_t launch_zero_fill(void* C, int64_t rows, int64_t cols, int64_t ldc, int elem_bytes, cudaStream_t stream);
 // out[j][i] = in[i][j], in rows x cols; elem_bytes 2 or 4; vec: every row of
 // in and out starts on a 16-byte boundary (16-byte accesses)
