@@ -73,6 +73,8 @@ def parse_args():
     p.add_argument("--workload", default=wl.HEADLINE.name, choices=sorted(wl.BY_NAME) + sorted(wl.TRANSPOSE_BY_NAME))
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-configs", action="store_true",
+                   help="skip the other workloads, the FP32 probe and the host-dispatch measurement")
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU work of the oracle sample")
     p.add_argument("--epilogue", default="none", choices=sorted(EPILOGUES),
                    help="fused epilogue C = act(alpha A.B + beta C + bias) timed with the product")
@@ -272,6 +274,174 @@ def run_reference(args, w: wl.Workload):
     print(json.dumps(line), flush=True)
 
 
+def sampled_check(w: wl.Workload, A, B, got_bits: np.ndarray, n_random: int, seed: int):
+    """The oracle at every element of the first and last row and column plus
+    `n_random` random positions of the product's output (storage bits), under
+    the parity tolerance: (max error/bound, positions checked)."""
+    import oracle
+    from tests import tolerance
+    fin, fout = wl.IN_FORMAT[w.dtype], wl.OUT_FORMAT[w.dtype]
+    r = wl.splitmix64(seed, 2 * n_random)
+    rows = np.concatenate([np.zeros(w.N, np.int64), np.full(w.N, w.M - 1, np.int64), np.arange(w.M), np.arange(w.M),
+                           (r[:n_random] % np.uint64(w.M)).astype(np.int64)])
+    cols = np.concatenate([np.arange(w.N), np.arange(w.N), np.zeros(w.M, np.int64), np.full(w.M, w.N - 1, np.int64),
+                           (r[n_random:] % np.uint64(w.N)).astype(np.int64)])
+    ref, S = oracle.entries(np.ascontiguousarray(A), np.ascontiguousarray(B), fin, w.K, rows, cols)
+    got = wl.decode(np.ascontiguousarray(got_bits[rows, cols])[None, :], fout)[0]
+    ok, ratio, _ = tolerance.check(got, ref, S, fin, fout)
+    return float(ratio), int(rows.size)
+
+
+def full_check(w: wl.Workload, A, B, got_bits: np.ndarray):
+    """Every element against the oracle's full product: (max error/bound, elements)."""
+    import oracle
+    from tests import tolerance
+    fin, fout = wl.IN_FORMAT[w.dtype], wl.OUT_FORMAT[w.dtype]
+    ref, S = oracle.gemm(np.ascontiguousarray(A), np.ascontiguousarray(B), fin, w.M, w.N, w.K)
+    ok, ratio, _ = tolerance.check(wl.decode(np.ascontiguousarray(got_bits), fout), ref, S, fin, fout)
+    return float(ratio), int(w.M * w.N)
+
+
+def fp32_peak_probe(dev, sms: int):
+    """FP32 FMA throughput measured by the probe kernel (libtgemm_probe.so):
+    8 independent FMA chains per thread, 8 blocks of 256 threads per SM, best
+    of three launches of each of scalar fma.rn.f32 and paired fma.rn.f32x2,
+    timed with CUDA events.  None if the probe library is missing."""
+    import ctypes
+    import torch
+    path = os.path.join(ROOT, "tiled_dense_gemm_02_gb300", "libtgemm_probe.so")
+    if not os.path.exists(path):
+        return None
+    lib = ctypes.CDLL(path)
+    lib.tgemm_probe_ffma.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
+                                     ctypes.c_void_p]
+    lib.tgemm_probe_ffma.restype = ctypes.c_int
+    per_iter = lib.tgemm_probe_ffma_per_iter()
+    blocks, threads, iters = 8 * sms, 256, 4000
+    out = torch.empty(blocks * threads, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    best = {}
+    for paired in (0, 1):
+        flops = blocks * threads * iters * per_iter * 2 * (2 if paired else 1)
+        times = []
+        for _ in range(4):
+            s_, e_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s_.record(stream)
+            rc = lib.tgemm_probe_ffma(paired, blocks, threads, iters, out.data_ptr(), stream.cuda_stream)
+            e_.record(stream)
+            if rc != 0:
+                raise RuntimeError(f"FFMA probe launch failed: cudaError {rc}")
+            torch.cuda.synchronize(dev)
+            times.append(s_.elapsed_time(e_))
+        best["paired" if paired else "scalar"] = flops / (min(times[1:]) / 1e3) / 1e12
+    return {"tflops": max(best.values()), "scalar_tflops": best["scalar"], "paired_tflops": best["paired"],
+            "how": f"{blocks} blocks x {threads} threads x {iters} iterations x {per_iter} FMAs "
+                   "(8 independent chains), best of 3 after one warm-up, CUDA events"}
+
+
+def host_dispatch(tg, w: wl.Workload, dev, calls: int = 200):
+    """Host microseconds per tgemm_gemm call, measured with the GPU queue kept
+    busy (a long device sleep enqueued first), so launches never wait for the
+    GPU: the library's validation, planning, cached tensor maps and launch.
+    The same loop of calls with M = 0 (validation only, no CUDA call) gives the
+    cost of the ctypes call itself."""
+    import torch
+    fin, fout = wl.IN_FORMAT[w.dtype], wl.OUT_FORMAT[w.dtype]
+    tdt = {"f32": torch.int32, "f16": torch.int16, "bf16": torch.int16}
+    a = torch.zeros((w.M, w.K), dtype=tdt[fin], device=dev)
+    b = torch.zeros((w.K, w.N), dtype=tdt[fin], device=dev)
+    c = torch.empty((w.M, w.N), dtype=tdt[fout], device=dev)
+    sptr = torch.cuda.current_stream(dev).cuda_stream
+    args = (w.K, b.data_ptr(), w.N, c.data_ptr(), w.N, w.dtype, sptr)
+    for _ in range(5):
+        tg.gemm(w.M, w.N, w.K, a.data_ptr(), *args)
+    torch.cuda.synchronize(dev)
+    before = tg.host_counters()
+    torch.cuda._sleep(int(2e8))  # about 0.1 s of device time ahead of the calls
+    t0 = time.perf_counter_ns()
+    for _ in range(calls):
+        tg.gemm(w.M, w.N, w.K, a.data_ptr(), *args)
+    t1 = time.perf_counter_ns()
+    for _ in range(calls):
+        tg.gemm(0, w.N, w.K, a.data_ptr(), *args)
+    t2 = time.perf_counter_ns()
+    torch.cuda.synchronize(dev)
+    after = tg.host_counters()
+    return {"us_per_call": (t1 - t0) / calls / 1e3, "ctypes_us_per_call": (t2 - t1) / calls / 1e3,
+            "map_encodes": after["map_encodes"] - before["map_encodes"],
+            "map_hits": after["map_hits"] - before["map_hits"], "calls": calls, "workload": w.name}
+
+
+def time_workload(tg, w: wl.Workload, dev, flush, steps: int, peaks: dict, fp32_peak=None):
+    """One workload timed like the headline (L2 flushed before each step,
+    CUDA events around the call on its stream), checked against the oracle,
+    with its roofline: min(peak FLOP/s, compulsory AI x measured HBM GB/s)."""
+    import torch
+    fin, fout = wl.IN_FORMAT[w.dtype], wl.OUT_FORMAT[w.dtype]
+    A, B = wl.make_inputs(w)
+    np_view = {"f32": np.int32, "f16": np.int16, "bf16": np.int16}
+    tdt = {"f32": torch.int32, "f16": torch.int16, "bf16": torch.int16}
+    a = torch.from_numpy(A.view(np_view[fin])).to(dev)
+    b = torch.from_numpy(B.view(np_view[fin])).to(dev)
+    c = torch.empty((w.M, w.N), dtype=tdt[fout], device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sptr = stream.cuda_stream
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    st, plan = tg.plan(w.M, w.N, w.K, a.data_ptr(), w.K, b.data_ptr(), w.N, c.data_ptr(), w.N, w.dtype, None, sms)
+
+    def call():
+        s_ = tg.gemm(w.M, w.N, w.K, a.data_ptr(), w.K, b.data_ptr(), w.N, c.data_ptr(), w.N, w.dtype, sptr)
+        if s_ != tg.OK:
+            raise RuntimeError(tg.status_string(s_))
+
+    for _ in range(3):
+        flush.fill_(1)
+        call()
+    torch.cuda.synchronize(dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for i, (s_, e_) in enumerate(ev):
+        flush.fill_(i)
+        s_.record(stream)
+        call()
+        e_.record(stream)
+    torch.cuda.synchronize(dev)
+    if tg.device_status(sptr) != tg.OK:
+        raise RuntimeError(f"{w.name}: a kernel gave up a bounded wait")
+    step_ms = [s_.elapsed_time(e_) for s_, e_ in ev]
+    ms = sum(step_ms) / steps
+    achieved = w.flops / (ms / 1e3) / 1e12
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    ai = w.flops / w.compulsory_bytes
+    if w.dtype == wl.F32:
+        flop_peak = fp32_peak["tflops"] if fp32_peak else None
+        bound_unit = "fp32 pipe (measured FFMA probe)"
+    else:
+        flop_peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+        bound_unit = "tensor (measured bf16 burst)"
+    roof = min(flop_peak, ai * hbm / 1e3) if flop_peak else ai * hbm / 1e3
+    got = c.cpu().numpy().view(np.uint32 if fout == "f32" else np.uint16).copy()
+    entry = {"value": achieved, "unit": "TFLOP/s", "ms_per_step": ms, "step_ms_median": statistics.median(step_ms),
+            "step_ms_min": min(step_ms), "steps": steps,
+            "roofline": {"achieved": achieved, "peak": roof, "unit": "TFLOP/s", "frac": achieved / roof,
+                         "bound": bound_unit if flop_peak and roof == flop_peak else "hbm (measured copy)",
+                         "ai_flop_per_byte": ai, "dram_gbs_compulsory": w.compulsory_bytes / (ms / 1e3) / 1e9},
+            "kernel": {k: v for k, v in plan.as_dict().items()
+                       if k in ("kernel", "tile_m", "tile_n", "tile_k", "ctas", "cta_group", "swap_ab", "tuned")},
+            "launches_per_step": kernel_launches_per_call(tg, plan, False)}
+    return entry, (A, B, got)
+
+
+def check_output(w: wl.Workload, A, B, got) -> dict:
+    """The oracle leg of a timed workload, run on the host after all GPU work:
+    every element for products of up to 2^20 outputs, else the borders and
+    4096 random positions."""
+    if w.M * w.N <= 1 << 20:
+        ratio, checked = full_check(w, A, B, got)
+    else:
+        ratio, checked = sampled_check(w, A, B, got, 4096, seed=77)
+    return {"max_err_over_bound": ratio, "elements_checked": checked}
+
+
 def kernel_launches_per_call(tg, plan, epilogue: bool) -> int:
     """Kernels one library call launches for `plan`: a plain fp32 product whose
     last round of tiles is split into K halves first zeroes the rows of C those
@@ -354,6 +524,8 @@ def run_ours(args, w: wl.Workload):
     if world > 1:
         total_ms = max_over_ranks(total_ms, dev)
     assert tg.device_status(sptr) == tg.OK
+    # the output of the last timed step, against the oracle (after the timed region)
+    last_c = c.cpu().numpy().view(np.uint32 if fout == "f32" else np.uint16).copy()
     ms_per_step = total_ms / args.steps
     value = world * w.flops * args.steps / (total_ms / 1e3) / 1e12
 
@@ -392,15 +564,25 @@ def run_ours(args, w: wl.Workload):
 
     peaks, peak_src = load_peaks()
     peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    errors = {}
+    fp32_peak = None
+    if world == 1 and (w.dtype == wl.F32 or not args.no_configs):
+        try:
+            fp32_peak = fp32_peak_probe(dev, sms)
+        except Exception as exc:  # the headline line is printed whatever happens here
+            errors["fp32_peak_probe"] = repr(exc)
     if w.dtype == wl.F32:
-        # the SIMT kernel is bound by the FP32 pipe: SMs x 128 FMA/clk x 2 FLOP x
-        # the SM clock (the maximum nvidia-smi reports for this GPU)
+        # the SIMT kernel is bound by the FP32 pipe: the FFMA probe's measured
+        # rate, beside SMs x 128 FMA/clk x 2 FLOP x the SM clock
         achieved = w.flops / (ms_per_step / 1e3) / 1e12
         clk = clocks.get("sm_max_mhz") or 2070.0
-        fp32_peak = sms * 128 * 2 * clk * 1e6 / 1e12
-        roofline = {"bound": "alu", "achieved": achieved, "peak": fp32_peak, "unit": "TFLOP/s",
-                    "frac": achieved / fp32_peak, "traffic": None,
-                    "peak_source": f"derived: {sms} SMs x 128 fp32 FMA/clk x 2 x {clk:.0f} MHz",
+        derived = sms * 128 * 2 * clk * 1e6 / 1e12
+        fp32_peak_value = fp32_peak["tflops"] if fp32_peak else derived
+        roofline = {"bound": "alu", "achieved": achieved, "peak": fp32_peak_value, "unit": "TFLOP/s",
+                    "frac": achieved / fp32_peak_value, "traffic": None,
+                    "peak_source": ("measured: FFMA probe (libtgemm_probe.so), same run" if fp32_peak else
+                                    f"derived: {sms} SMs x 128 fp32 FMA/clk x 2 x {clk:.0f} MHz"),
+                    "peak_derived": derived, "frac_of_derived": achieved / derived,
                     "algorithmic_flops_per_launch": w.flops}
         if launches_per_call == 2:
             roofline["timed_span"] = "the zero fill of the split tiles' rows plus the SIMT kernel"
@@ -412,6 +594,38 @@ def run_ours(args, w: wl.Workload):
                     "peak_source": f"{peak_src} bf16_tflops (burst; kernel timed alone)",
                     "algorithmic_flops_per_launch": w.flops,
                     "compulsory_bytes_per_launch": w.compulsory_bytes}
+    # the other configurations, timed the same way (GPU work first, their
+    # oracle checks below with the CPU legs)
+    configs = dispatch = None
+    outputs = {}
+    if world == 1 and not args.no_configs and epi is None:
+        configs = {}
+        for name, steps in (("f32_64x64x64", 50), ("f16_1024x1024x1024", 50), ("bf16_2048x2048x2048", 50),
+                            ("bf16_1000x1500x4096_ragged", 50), ("f32_4096x4096x4096", 10)):
+            if name == w.name:
+                continue
+            try:
+                configs[name], outputs[name] = time_workload(tg, wl.BY_NAME[name], dev, flush, steps, peaks,
+                                                             fp32_peak)
+            except Exception as exc:
+                errors[name] = repr(exc)
+        if fp32_peak:
+            configs["fp32_peak_probe"] = fp32_peak
+        try:
+            dispatch = {n: host_dispatch(tg, wl.BY_NAME[n], dev)
+                        for n in ("f16_1024x1024x1024", "bf16_4096x4096x4096_f32out")}
+        except Exception as exc:
+            errors["host_dispatch"] = repr(exc)
+
+    # ---------------------------------------------- CPU legs (oracle), no GPU work
+    check = None
+    if epi is None:
+        ratio, checked = sampled_check(w, A, B, last_c, 4096, seed=78)
+        check = {"max_err_over_bound": ratio, "elements_checked": checked,
+                 "what": "the last timed step's C at every element of the first and last row and column and 4096 "
+                         "random positions, against the oracle under the parity tolerance"}
+    for name, (a_bits, b_bits, got) in outputs.items():
+        configs[name].update(check_output(wl.BY_NAME[name], a_bits, b_bits, got))
     cpu = cpu_blocked = None
     if not args.no_cpu_baseline and world == 1:
         cpu = cpu_oracle_sample(w, A, B, args.cpu_seconds)
@@ -423,10 +637,15 @@ def run_ours(args, w: wl.Workload):
         "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "in": fin, "out": fout, "accumulate": "f32",
                    "l2": "flushed before every timed step (256 MiB write)", "parallelism": f"replicas{world}",
                    "kernel": plan.as_dict(), "sms": sms, "epilogue": args.epilogue, "step_ms_min": min(step_ms),
-                   "step_ms_median": statistics.median(step_ms), "wall_s": wall},
+                   "step_ms_median": statistics.median(step_ms), "wall_s": wall,
+                   "host_dispatch_us": dispatch[w.name]["us_per_call"] if dispatch and w.name in dispatch else None},
         "roofline": roofline,
+        "check": check,
+        "configs": configs,
+        "host_dispatch": dispatch,
         "cpu_baseline": cpu,
         "cpu_blocked": cpu_blocked,
+        "errors": errors or None,
         "clocks": clocks,
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": int(A.nbytes + B.nbytes), "d2h_bytes_per_step": int(c.numel() * c.element_size())},

@@ -81,8 +81,9 @@ enum tgemm_status {
  * that zeroes the rows of C those halves add into, then the product; see
  * tgemm_options.simt_split); it returns before the product is computed.  It
  * allocates no device memory.
- * It keeps a small, mutex-guarded host cache of device attributes.  It is
- * safe to call from several host threads.
+ * It keeps small, mutex-guarded host caches of device attributes and of
+ * encoded tensor maps (see tgemm_host_counters).  It is safe to call from
+ * several host threads.
  *
  * Errors: see enum tgemm_status.  Validation errors are returned before any
  * CUDA call.  A launch failure returns TGEMM_ERR_LAUNCH with the CUDA error
@@ -426,6 +427,31 @@ TGEMM_API const char* tgemm_status_string(int status);
 
 /* TGEMM_VERSION of the loaded library. */
 TGEMM_API int tgemm_version(void);
+
+/*
+ * Host-side counters of the library, process-wide and cumulative ("GPU Kernel
+ * 的 Tile、Grid、Wave 与 Launch Overhead", section Launch Overhead: at small
+ * sizes the fixed cost of a launch dominates, so the host work per call is
+ * kept small and observable).
+ *
+ * Every bulk-tensor (TMA) descriptor a call needs is looked up in a cache of
+ * encoded tensor maps keyed on all of its encode arguments (device, base
+ * address, element type, dimensions, strides, box, swizzle); only a miss calls
+ * the driver's encoder.  Repeated calls on the same buffers and shapes then
+ * encode nothing.
+ *
+ *   tc_launches: tensor-core kernel launches enqueued by product calls
+ *   map_hits:    tensor maps taken from the cache
+ *   map_encodes: tensor maps encoded (cache misses)
+ * Returns TGEMM_ERR_INVALID_VALUE for a NULL `out`; needs no GPU.
+ */
+typedef struct tgemm_counters {
+  uint64_t tc_launches;
+  uint64_t map_hits;
+  uint64_t map_encodes;
+} tgemm_counters;
+
+TGEMM_API int tgemm_host_counters(tgemm_counters* out);
 
 #ifdef __cplusplus
 }

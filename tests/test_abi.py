@@ -33,7 +33,7 @@ def test_header_declares_the_abi():
     assert names == sorted(["tgemm_gemm", "tgemm_gemm_ex", "tgemm_gemm_ws", "tgemm_workspace_size", "tgemm_plan",
                             "tgemm_gemm_noalloc", "tgemm_gemm_epilogue", "tgemm_gemm_batched",
                             "tgemm_plan_batched", "tgemm_transpose", "tgemm_gemm_host", "tgemm_device_status",
-                            "tgemm_status_string", "tgemm_version"])
+                            "tgemm_status_string", "tgemm_version", "tgemm_host_counters"])
 
 
 def test_library_exports_every_declared_symbol(tg):
@@ -42,6 +42,17 @@ def test_library_exports_every_declared_symbol(tg):
         assert hasattr(lib, name), name
     assert set(declared_functions()) == set(tg.EXPORTS)
     assert tg.version() == 10000
+
+
+def test_host_counters_need_no_gpu(tg):
+    """The counters are readable without a device; validation-only calls move
+    none of them."""
+    c0 = tg.host_counters()
+    assert set(c0) == {"tc_launches", "map_hits", "map_encodes"}
+    assert tg.gemm(-1, 4, 4, 0, 4, 0, 4, 0, 4, tg.BF16) == tg.ERR_INVALID_VALUE
+    assert tg.gemm(0, 4, 4, 0, 4, 0, 4, 0, 4, tg.BF16) == tg.OK
+    assert tg.host_counters() == c0
+    assert tg.library().tgemm_host_counters(None) == tg.ERR_INVALID_VALUE
 
 
 def test_noalloc_scratch_size_matches_header(tg):

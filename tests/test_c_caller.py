@@ -11,7 +11,8 @@ import subprocess
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-STRUCTS = (("Options", "tgemm_options"), ("PlanInfo", "tgemm_plan_info"), ("Epilogue", "tgemm_epilogue"))
+STRUCTS = (("Options", "tgemm_options"), ("PlanInfo", "tgemm_plan_info"), ("Epilogue", "tgemm_epilogue"),
+           ("Counters", "tgemm_counters"))
 
 
 @pytest.fixture(scope="module")

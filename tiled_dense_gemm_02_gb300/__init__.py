@@ -28,7 +28,8 @@ ACT_NONE, ACT_RELU = 0, 1
 
 EXPORTS = ("tgemm_gemm", "tgemm_gemm_ex", "tgemm_gemm_ws", "tgemm_workspace_size", "tgemm_plan",
            "tgemm_gemm_noalloc", "tgemm_gemm_epilogue", "tgemm_gemm_batched", "tgemm_plan_batched",
-           "tgemm_transpose", "tgemm_gemm_host", "tgemm_device_status", "tgemm_status_string", "tgemm_version")
+           "tgemm_transpose", "tgemm_gemm_host", "tgemm_device_status", "tgemm_status_string", "tgemm_version",
+           "tgemm_host_counters")
 # bytes of the scratch array built into the library (TGEMM_NOALLOC_SCRATCH_BYTES)
 NOALLOC_SCRATCH_BYTES = 20 * 1024 * 1024 + 4096
 
@@ -61,6 +62,14 @@ class PlanInfo(ctypes.Structure):
 
     def as_dict(self) -> dict:
         return {name: getattr(self, name) for name, _ in self._fields_ if name != "reserved"}
+
+
+class Counters(ctypes.Structure):
+    """struct tgemm_counters"""
+    _fields_ = [("tc_launches", ctypes.c_uint64), ("map_hits", ctypes.c_uint64), ("map_encodes", ctypes.c_uint64)]
+
+    def as_dict(self) -> dict:
+        return {name: getattr(self, name) for name, _ in self._fields_}
 
 
 class TgemmError(RuntimeError):
@@ -110,6 +119,8 @@ def _load():
     lib.tgemm_status_string.restype = ctypes.c_char_p
     lib.tgemm_version.argtypes = []
     lib.tgemm_version.restype = ip
+    lib.tgemm_host_counters.argtypes = [ctypes.POINTER(Counters)]
+    lib.tgemm_host_counters.restype = ip
     return lib
 
 
@@ -228,6 +239,16 @@ def status_string(status: int) -> str:
 
 def version() -> int:
     return _lib.tgemm_version()
+
+
+def host_counters() -> dict:
+    """tgemm_host_counters: cumulative tensor-core launches, tensor-map cache
+    hits and tensor-map encodes of this process."""
+    c = Counters()
+    st = _lib.tgemm_host_counters(ctypes.byref(c))
+    if st != OK:
+        raise TgemmError(st, "tgemm_host_counters")
+    return c.as_dict()
 
 
 # ------------------------------------------------------------ torch helpers

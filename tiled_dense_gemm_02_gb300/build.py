@@ -18,6 +18,9 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 OBJ_DIR = os.path.join(HERE, "_build")
 LIBRARY = os.path.join(HERE, "libtgemm.so")
+# the FP32 FMA-throughput probe the benchmark uses for the SIMT roofline (not part of libtgemm.so)
+PROBE_SOURCE = os.path.join(CSRC, "probe", "fp32_peak.cu")
+PROBE_LIBRARY = os.path.join(HERE, "libtgemm_probe.so")
 HEADER = os.path.join(ROOT, "include", "tgemm.h")
 
 NVCC = os.environ.get("NVCC", "nvcc")
@@ -66,8 +69,24 @@ def _compile(src: str, extra: list[str]) -> str:
     return obj
 
 
+def build_probe(force: bool = False) -> str:
+    """Compile the FP32 FMA-throughput probe into its own shared library."""
+    if not force and os.path.exists(PROBE_LIBRARY) and \
+            os.path.getmtime(PROBE_LIBRARY) >= max(os.path.getmtime(PROBE_SOURCE), os.path.getmtime(__file__)):
+        return PROBE_LIBRARY
+    tmp = PROBE_LIBRARY + ".tmp"
+    cmd = [NVCC, *NVCC_FLAGS, "-shared", "-o", tmp, PROBE_SOURCE]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"nvcc failed for {PROBE_SOURCE}:\n{r.stdout}\n{r.stderr}")
+    os.replace(tmp, PROBE_LIBRARY)
+    return PROBE_LIBRARY
+
+
 def build(force: bool = False, extra: list[str] | None = None) -> str:
-    """Compile every CUDA source in parallel and link the shared library."""
+    """Compile every CUDA source in parallel and link the shared library (and
+    the FP32 probe beside it)."""
+    build_probe(force)
     if not force and not stale():
         return LIBRARY
     os.makedirs(OBJ_DIR, exist_ok=True)

@@ -28,6 +28,8 @@ __device__ unsigned int g_device_status = 0;
 namespace {
 
 thread_local std::string t_last_error;
+// Device the calling thread's current call runs on (set by device_info).
+thread_local int t_device = 0;
 
 struct DeviceInfo {
   bool ready = false;
@@ -59,6 +61,7 @@ int device_info(DeviceInfo** out) {
     t_last_error = "device ordinal out of range";
     return TGEMM_ERR_LAUNCH;
   }
+  t_device = dev;
   std::lock_guard<std::mutex> lock(g_mutex);
   DeviceInfo& d = g_devices[dev];
   if (!d.ready) {
@@ -597,6 +600,72 @@ CUtensorMapDataType tmap_type(int fmt_bytes, bool bf16) {
   return bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
 }
 
+// Cache of encoded tensor maps.  A map is a pure function of its encode
+// arguments (device, base address, element type, dimensions, strides, box,
+// swizzle), so a cached map is reused exactly when all of them match: the
+// same buffer called again with the same shape.  A buffer freed and
+// reallocated at the same address with the same shape gets the same map it
+// would be encoded to.  Least recently used entries are replaced; the cache is
+// guarded by its own mutex.
+struct MapKey {
+  uint64_t base;
+  uint64_t dims[3];
+  uint64_t strides[2];
+  uint32_t box[3];
+  int32_t device, rank, type, swizzle;
+};
+struct MapSlot {
+  MapKey key;
+  CUtensorMap map;
+  uint64_t stamp;  // 0: empty
+};
+constexpr int kMapSlots = 128;
+std::mutex g_map_mutex;
+MapSlot g_map_slots[kMapSlots];
+uint64_t g_map_clock = 0;
+std::atomic<uint64_t> g_map_hits{0}, g_map_encodes{0}, g_launch_calls{0};
+
+int encode_cached(CUtensorMap* map, CUtensorMapDataType type, int rank, const void* base, const cuuint64_t* dims,
+                  const cuuint64_t* strides, const cuuint32_t* box, CUtensorMapSwizzle swizzle) {
+  MapKey key;
+  std::memset(&key, 0, sizeof key);  // padding bytes take part in the comparison
+  key.base = reinterpret_cast<uint64_t>(base);
+  for (int i = 0; i < rank; ++i) {
+    key.dims[i] = dims[i];
+    key.box[i] = box[i];
+  }
+  for (int i = 0; i + 1 < rank; ++i) key.strides[i] = strides[i];
+  key.device = t_device;
+  key.rank = rank;
+  key.type = static_cast<int32_t>(type);
+  key.swizzle = static_cast<int32_t>(swizzle);
+  std::lock_guard<std::mutex> lock(g_map_mutex);
+  MapSlot* victim = &g_map_slots[0];
+  for (MapSlot& slot : g_map_slots) {
+    if (slot.stamp != 0 && slot.key.base == key.base && std::memcmp(&slot.key, &key, sizeof key) == 0) {
+      slot.stamp = ++g_map_clock;
+      *map = slot.map;
+      g_map_hits.fetch_add(1, std::memory_order_relaxed);
+      return TGEMM_OK;
+    }
+    if (slot.stamp < victim->stamp) victim = &slot;
+  }
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(map, type, static_cast<cuuint32_t>(rank), const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    t_last_error = "cuTensorMapEncodeTiled (" + std::to_string(rank) + "-D) failed with CUresult " +
+                   std::to_string(static_cast<int>(r));
+    return TGEMM_ERR_LAUNCH;
+  }
+  g_map_encodes.fetch_add(1, std::memory_order_relaxed);
+  victim->key = key;
+  victim->map = *map;
+  victim->stamp = ++g_map_clock;
+  return TGEMM_OK;
+}
+
 // 2-D row-major tensor (cols x rows, pitch in bytes), box of box_cols x box_rows,
 // 128-byte swizzle, zero fill outside the tensor.
 int encode_2d(CUtensorMap* map, CUtensorMapDataType type, const void* base, int64_t cols, int64_t rows,
@@ -605,15 +674,7 @@ int encode_2d(CUtensorMap* map, CUtensorMapDataType type, const void* base, int6
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(pitch_bytes)};
   const cuuint32_t box[2] = {box_cols, box_rows};
-  const cuuint32_t estr[2] = {1, 1};
-  CUresult r = g_encode(map, type, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) {
-    t_last_error = "cuTensorMapEncodeTiled failed with CUresult " + std::to_string(static_cast<int>(r));
-    return TGEMM_ERR_LAUNCH;
-  }
-  return TGEMM_OK;
+  return encode_cached(map, type, 2, base, dims, strides, box, swizzle);
 }
 
 // 3-D row-major tensor: `depth` matrices of cols x rows, `depth_bytes` apart
@@ -627,14 +688,7 @@ int encode_3d(CUtensorMap* map, CUtensorMapDataType type, const void* base, int6
                               static_cast<cuuint64_t>(depth < 1 ? 1 : depth)};
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(pitch_bytes), static_cast<cuuint64_t>(depth_bytes)};
   const cuuint32_t box[3] = {box_cols, box_rows, 1};
-  const cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = g_encode(map, type, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) {
-    t_last_error = "cuTensorMapEncodeTiled (3-D) failed with CUresult " + std::to_string(static_cast<int>(r));
-    return TGEMM_ERR_LAUNCH;
-  }
-  return TGEMM_OK;
+  return encode_cached(map, type, 3, base, dims, strides, box, swizzle);
 }
 
 // Resident CTA pairs of the pair kernel on the current device, queried once.
@@ -868,6 +922,7 @@ int run(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void*
   const int to_us = (o && o->wait_timeout_us) ? o->wait_timeout_us : 2000000;
   a.timeout_ns = static_cast<unsigned long long>(to_us) * 1000ull;
   a.status = dev->status;
+  g_launch_calls.fetch_add(1, std::memory_order_relaxed);
   if (p.copy_pair)
     e = launch_tc_pair_copy(p.bn, mA, a, p.ctas / 2, stream);
   else if (p.swap)
@@ -1194,6 +1249,14 @@ const char* tgemm_status_string(int status) {
 }
 
 int tgemm_version(void) { return TGEMM_VERSION; }
+
+int tgemm_host_counters(tgemm_counters* out) {
+  if (!out) return TGEMM_ERR_INVALID_VALUE;
+  out->tc_launches = tgemm::g_launch_calls.load(std::memory_order_relaxed);
+  out->map_hits = tgemm::g_map_hits.load(std::memory_order_relaxed);
+  out->map_encodes = tgemm::g_map_encodes.load(std::memory_order_relaxed);
+  return TGEMM_OK;
+}
 
 }  // extern "C"
 
