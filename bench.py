@@ -367,15 +367,20 @@ def host_dispatch(tg, w: wl.Workload, dev, calls: int = 200):
     t2 = time.perf_counter_ns()
     torch.cuda.synchronize(dev)
     after = tg.host_counters()
+    n = after["tc_launches"] - before["tc_launches"]
     return {"us_per_call": (t1 - t0) / calls / 1e3, "ctypes_us_per_call": (t2 - t1) / calls / 1e3,
+            "library_prepare_us": (after["ns_prepare"] - before["ns_prepare"]) / max(n, 1) / 1e3,
+            "library_launch_us": (after["ns_launch"] - before["ns_launch"]) / max(n, 1) / 1e3,
             "map_encodes": after["map_encodes"] - before["map_encodes"],
             "map_hits": after["map_hits"] - before["map_hits"], "calls": calls, "workload": w.name}
 
 
-def time_workload(tg, w: wl.Workload, dev, flush, steps: int, peaks: dict, fp32_peak=None):
+def time_workload(tg, w: wl.Workload, dev, flush, steps: int, peaks: dict, fp32_peak=None, options=None):
     """One workload timed like the headline (L2 flushed before each step,
     CUDA events around the call on its stream), checked against the oracle,
-    with its roofline: min(peak FLOP/s, compulsory AI x measured HBM GB/s)."""
+    with its roofline: min(peak FLOP/s, compulsory AI x measured HBM GB/s).
+    With `options` the call is tgemm_gemm_ws with those options and a
+    workspace of tgemm_workspace_size bytes (allocated before timing)."""
     import torch
     fin, fout = wl.IN_FORMAT[w.dtype], wl.OUT_FORMAT[w.dtype]
     A, B = wl.make_inputs(w)
@@ -387,10 +392,21 @@ def time_workload(tg, w: wl.Workload, dev, flush, steps: int, peaks: dict, fp32_
     stream = torch.cuda.current_stream(dev)
     sptr = stream.cuda_stream
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    st, plan = tg.plan(w.M, w.N, w.K, a.data_ptr(), w.K, b.data_ptr(), w.N, c.data_ptr(), w.N, w.dtype, None, sms)
+    ws_bytes = 0
+    ws = None
+    if options is not None:
+        st, ws_bytes = tg.workspace_size(w.M, w.N, w.K, a.data_ptr(), w.K, b.data_ptr(), w.N, c.data_ptr(), w.N,
+                                         w.dtype, options)
+        ws = torch.zeros(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
+    st, plan = tg.plan(w.M, w.N, w.K, a.data_ptr(), w.K, b.data_ptr(), w.N, c.data_ptr(), w.N, w.dtype, options, sms,
+                       workspace_bytes=ws_bytes)
 
     def call():
-        s_ = tg.gemm(w.M, w.N, w.K, a.data_ptr(), w.K, b.data_ptr(), w.N, c.data_ptr(), w.N, w.dtype, sptr)
+        if options is None:
+            s_ = tg.gemm(w.M, w.N, w.K, a.data_ptr(), w.K, b.data_ptr(), w.N, c.data_ptr(), w.N, w.dtype, sptr)
+        else:
+            s_ = tg.gemm_ws(w.M, w.N, w.K, a.data_ptr(), w.K, b.data_ptr(), w.N, c.data_ptr(), w.N, w.dtype, options,
+                            ws.data_ptr(), ws_bytes, sptr)
         if s_ != tg.OK:
             raise RuntimeError(tg.status_string(s_))
 
@@ -426,7 +442,9 @@ def time_workload(tg, w: wl.Workload, dev, flush, steps: int, peaks: dict, fp32_
                          "bound": bound_unit if flop_peak and roof == flop_peak else "hbm (measured copy)",
                          "ai_flop_per_byte": ai, "dram_gbs_compulsory": w.compulsory_bytes / (ms / 1e3) / 1e9},
             "kernel": {k: v for k, v in plan.as_dict().items()
-                       if k in ("kernel", "tile_m", "tile_n", "tile_k", "ctas", "cta_group", "swap_ab", "tuned")},
+                       if k in ("kernel", "tile_m", "tile_n", "tile_k", "ctas", "cta_group", "swap_ab", "tuned",
+                                "sk_iters", "workspace_bytes")},
+            "call": "tgemm_gemm" if options is None else f"tgemm_gemm_ws {dict(options)}",
             "launches_per_step": kernel_launches_per_call(tg, plan, False)}
     return entry, (A, B, got)
 
@@ -440,6 +458,29 @@ def check_output(w: wl.Workload, A, B, got) -> dict:
     else:
         ratio, checked = sampled_check(w, A, B, got, 4096, seed=77)
     return {"max_err_over_bound": ratio, "elements_checked": checked}
+
+
+def launch_floor(tg, dev, flush, steps: int = 50):
+    """The smallest launch of the library timed like every workload (L2 flush
+    first, CUDA events around the call): a 1 x 1 product with K = 0, which is
+    one zero-fill kernel writing one float.  What a workload's time has beyond
+    this is its own work."""
+    import torch
+    c = torch.empty(1, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sptr = stream.cuda_stream
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps + 3)]
+    for i, (s_, e_) in enumerate(ev):
+        flush.fill_(i)
+        s_.record(stream)
+        st = tg.gemm(1, 1, 0, 0, 1, 0, 1, c.data_ptr(), 1, tg.F32, sptr)
+        e_.record(stream)
+        if st != tg.OK:
+            raise RuntimeError(tg.status_string(st))
+    torch.cuda.synchronize(dev)
+    ms = [s_.elapsed_time(e_) for s_, e_ in ev[3:]]
+    return {"us_mean": 1e3 * sum(ms) / len(ms), "us_median": 1e3 * statistics.median(ms), "us_min": 1e3 * min(ms),
+            "what": "tgemm_gemm(1, 1, 0): one zero-fill kernel, after the same L2 flush, CUDA events"}
 
 
 def kernel_launches_per_call(tg, plan, epilogue: bool) -> int:
@@ -609,8 +650,19 @@ def run_ours(args, w: wl.Workload):
                                                              fp32_peak)
             except Exception as exc:
                 errors[name] = repr(exc)
+        # the ragged shape again with the stream-K split over every CTA pair (needs a workspace)
+        name = "bf16_1000x1500x4096_ragged"
+        try:
+            configs[name + "+stream_k"], outputs[name + "+stream_k"] = time_workload(
+                tg, wl.BY_NAME[name], dev, flush, 50, peaks, fp32_peak, options={"stream_k": 2})
+        except Exception as exc:
+            errors[name + "+stream_k"] = repr(exc)
         if fp32_peak:
             configs["fp32_peak_probe"] = fp32_peak
+        try:
+            configs["launch_floor"] = launch_floor(tg, dev, flush)
+        except Exception as exc:
+            errors["launch_floor"] = repr(exc)
         try:
             dispatch = {n: host_dispatch(tg, wl.BY_NAME[n], dev)
                         for n in ("f16_1024x1024x1024", "bf16_4096x4096x4096_f32out")}
@@ -625,7 +677,7 @@ def run_ours(args, w: wl.Workload):
                  "what": "the last timed step's C at every element of the first and last row and column and 4096 "
                          "random positions, against the oracle under the parity tolerance"}
     for name, (a_bits, b_bits, got) in outputs.items():
-        configs[name].update(check_output(wl.BY_NAME[name], a_bits, b_bits, got))
+        configs[name].update(check_output(wl.BY_NAME[name.split("+")[0]], a_bits, b_bits, got))
     cpu = cpu_blocked = None
     if not args.no_cpu_baseline and world == 1:
         cpu = cpu_oracle_sample(w, A, B, args.cpu_seconds)

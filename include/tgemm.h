@@ -443,12 +443,17 @@ TGEMM_API int tgemm_version(void);
  *   tc_launches: tensor-core kernel launches enqueued by product calls
  *   map_hits:    tensor maps taken from the cache
  *   map_encodes: tensor maps encoded (cache misses)
+ *   ns_prepare:  host nanoseconds those calls spent before their launch
+ *                (validation, planning, tensor maps)
+ *   ns_launch:   host nanoseconds spent inside their CUDA launch calls
  * Returns TGEMM_ERR_INVALID_VALUE for a NULL `out`; needs no GPU.
  */
 typedef struct tgemm_counters {
   uint64_t tc_launches;
   uint64_t map_hits;
   uint64_t map_encodes;
+  uint64_t ns_prepare;
+  uint64_t ns_launch;
 } tgemm_counters;
 
 TGEMM_API int tgemm_host_counters(tgemm_counters* out);

@@ -48,7 +48,7 @@ def test_host_counters_need_no_gpu(tg):
     """The counters are readable without a device; validation-only calls move
     none of them."""
     c0 = tg.host_counters()
-    assert set(c0) == {"tc_launches", "map_hits", "map_encodes"}
+    assert set(c0) == {"tc_launches", "map_hits", "map_encodes", "ns_prepare", "ns_launch"}
     assert tg.gemm(-1, 4, 4, 0, 4, 0, 4, 0, 4, tg.BF16) == tg.ERR_INVALID_VALUE
     assert tg.gemm(0, 4, 4, 0, 4, 0, 4, 0, 4, tg.BF16) == tg.OK
     assert tg.host_counters() == c0
@@ -247,6 +247,23 @@ def test_copy_pair_planning(tg):
     assert st == tg.OK and p.ctas == 10
 
 
+def test_copy_pair_stream_k_planning(tg):
+    """The ragged product's 48 pair tiles on 76 pairs: with stream_k = 2 and a
+    workspace, all 48 x 64 k-stages are spread over every pair; without a
+    workspace (or with stream_k 0 / 1) whole tiles on 48 pairs."""
+    need = 4096 + 76 * 2 * 4 * 32 * 128 * 4
+    st, p = plan(tg, 1000, 1500, 4096, dtype=2, sms=152, stream_k=2, ws=need)
+    assert st == tg.OK and p.kernel == tg.KERNEL_TC_COPY and p.cta_group == 2 and p.tile_n == 128
+    assert (p.dp_tiles, p.sk_iters, p.ctas, p.workspace_bytes) == (0, 48 * 64, 152, need)
+    for kw in ({"stream_k": 2, "ws": need - 1}, {"stream_k": 2}, {"stream_k": 1, "ws": need}, {"ws": need}):
+        st, p = plan(tg, 1000, 1500, 4096, dtype=2, sms=152, **kw)
+        assert st == tg.OK and (p.dp_tiles, p.sk_iters, p.ctas) == (48, 0, 96), kw
+    # more tiles than pairs: the whole rounds stay whole, the remainder is split
+    st, p = plan(tg, 4000, 3000, 4096, dtype=2, ldb=3004, sms=152, stream_k=2, cta_group=2, tile_n=128, ws=need)
+    tiles = 16 * 24
+    assert (p.dp_tiles, p.sk_iters, p.ctas) == (tiles - tiles % 76, (tiles % 76) * 64, 152)
+
+
 def test_tuned_shape_table(tg):
     """Calls that leave every tuned option at 0 and match a measured shape take
     the table's options; any tuned option set, another shape, or pointers the
@@ -399,6 +416,14 @@ def test_simt_split_planning(tg):
     assert plan(tg, 64, 64, 64, dtype=0, simt_split=3)[0] == tg.ERR_INVALID_VALUE
     assert plan(tg, 64, 64, 64, dtype=0, simt_split=-1)[0] == tg.ERR_INVALID_VALUE
     assert plan(tg, 256, 256, 256, dtype=2, simt_split=2)[0] == tg.ERR_INVALID_VALUE
+
+
+def test_simt_raster_group_planning(tg):
+    """The SIMT kernel walks tiles in groups of 16 tile rows by default, fewer
+    when the product has fewer rows; group_m overrides."""
+    assert plan(tg, 4096, 4096, 4096, dtype=0, sms=152)[1].group_m == 16
+    assert plan(tg, 300, 4096, 512, dtype=0, sms=152)[1].group_m == 3
+    assert plan(tg, 4096, 4096, 4096, dtype=0, sms=152, group_m=5)[1].group_m == 5
 
 
 def test_simt_split_rule_on_random_shapes(tg):

@@ -109,6 +109,19 @@ def test_simt_split_last_round_auto():
     H.check_full(res, A, B, M, N, K, wl.F32, "simt split tail")
 
 
+@pytest.mark.parametrize("group_m", [1, 3, 7, 16, 40])
+def test_simt_raster_groups_with_split_tail(group_m):
+    """Tiles in groups of group_m tile rows (column by column within a group),
+    with the last round split into K halves: the split tiles of grouped order
+    are not a suffix of rows, so the call zeroes their bounding box and any
+    whole tile inside it is stored over the zeros.  C starts as NaN canaries,
+    so a split tile outside the zeroed box would come back NaN."""
+    M, N, K = 20 * 128 - 37, 17 * 128 - 5, 300
+    A, B, res = case(M, N, K, wl.F32, seed=123, ldc=N + 3, options={"group_m": group_m, "simt_split": 2})
+    assert res.plan.group_m == min(group_m, 20)
+    H.check_full(res, A, B, M, N, K, wl.F32, f"simt group {group_m}")
+
+
 def test_simt_split_is_deterministic():
     """Two additions onto zero commute: repeated calls give the same bits."""
     A, B, r1 = case(300, 200, 1000, wl.F32, seed=122, options={"simt_split": 2})

@@ -98,3 +98,47 @@ def test_workspace_too_small_runs_whole_tiles():
     A, B, res = case(M, N, K, wl.BF16, opts, seed=74, workspace=ws)
     assert res.plan.sk_iters == 0
     H.check_full(res, A, B, M, N, K, wl.BF16, "small workspace")
+
+
+# ------------------------------- CTA pairs copying B per thread (unaligned B rows)
+
+@pytest.mark.parametrize("tile_n", [128, 256])
+@pytest.mark.parametrize("dtype", [wl.BF16, wl.BF16_F32OUT, wl.F16], ids=lambda d: wl.DTYPE_NAMES[d])
+@pytest.mark.parametrize("max_ctas,ldb_pad", [(16, 0), (14, 6), (0, 1)], ids=["8_pairs_8B", "7_pairs_4B", "all_2B"])
+def test_copy_pair_stream_k(dtype, tile_n, max_ctas, ldb_pad):
+    """B rows off the 16-byte grid (ldb = N + pad = 1300, 1306, 1301: pitches of
+    2600, 2612 and 2602 bytes, 8-, 4- and 2-byte granules) on CTA pairs that
+    copy B per thread, with the tiles past the last full round of pairs split
+    along K: ragged M, N and K, finishing pairs add one or more partial sums."""
+    M, N, K = 1100, 1300, 1000
+    opts = {"cta_group": 2, "tile_n": tile_n, "max_ctas": max_ctas, "stream_k": 2}
+    A, B, res = case(M, N, K, dtype, opts, seed=75, ldb=N + ldb_pad)
+    assert res.plan.kernel == 2 and res.plan.cta_group == 2 and res.plan.sk_iters > 0
+    assert res.plan.b_copy_bytes == {0: 8, 6: 4, 1: 2}[ldb_pad]
+    H.check_full(res, A, B, M, N, K, dtype, f"copy-pair stream-K tile_n {tile_n} ctas {max_ctas}")
+
+
+def test_copy_pair_stream_k_ragged_workload():
+    """The ragged bf16 1000 x 1500 x 4096 workload (3000-byte B rows): 48 pair
+    tiles spread over every pair, every element against the oracle, and a
+    second call through the same workspace gives the same bits."""
+    w = wl.BY_NAME["bf16_1000x1500x4096_ragged"]
+    A, B = wl.make_inputs(w)
+    r1 = H.run_gpu(A, B, w.M, w.N, w.K, w.dtype, workspace=True, options={"stream_k": 2})
+    assert r1.plan.kernel == 2 and r1.plan.cta_group == 2 and r1.plan.sk_iters == 48 * 64
+    assert r1.plan.dp_tiles == 0
+    H.check_full(r1, A, B, w.M, w.N, w.K, w.dtype, "ragged workload, stream-K")
+    r2 = H.run_gpu(A, B, w.M, w.N, w.K, w.dtype, workspace=r1.workspace, options={"stream_k": 2})
+    assert np.array_equal(r1.raw, r2.raw)
+
+
+@pytest.mark.parametrize("K", [200, 257, 448, 1000])
+def test_copy_pair_stream_k_short_k(K):
+    """Few k-stages per tile over every pair (24 pair tiles of 4 to 16 stages
+    on 76 pairs): ranges of one or two stages, tiles finished by pairs that
+    hold a single stage; B rows of 1804 bytes (4-byte granules)."""
+    M, N = 600, 900
+    opts = {"cta_group": 2, "tile_n": 128, "stream_k": 2}
+    A, B, res = case(M, N, K, wl.BF16, opts, seed=76, lda=(K + 7) // 8 * 8, ldb=N + 2)
+    assert res.plan.kernel == 2 and res.plan.sk_iters > 0 and res.plan.b_copy_bytes == 4
+    H.check_full(res, A, B, M, N, K, wl.BF16, f"copy-pair stream-K K {K}")

@@ -66,7 +66,8 @@ class PlanInfo(ctypes.Structure):
 
 class Counters(ctypes.Structure):
     """struct tgemm_counters"""
-    _fields_ = [("tc_launches", ctypes.c_uint64), ("map_hits", ctypes.c_uint64), ("map_encodes", ctypes.c_uint64)]
+    _fields_ = [("tc_launches", ctypes.c_uint64), ("map_hits", ctypes.c_uint64), ("map_encodes", ctypes.c_uint64),
+                ("ns_prepare", ctypes.c_uint64), ("ns_launch", ctypes.c_uint64)]
 
     def as_dict(self) -> dict:
         return {name: getattr(self, name) for name, _ in self._fields_}
@@ -243,7 +244,7 @@ def version() -> int:
 
 def host_counters() -> dict:
     """tgemm_host_counters: cumulative tensor-core launches, tensor-map cache
-    hits and tensor-map encodes of this process."""
+    hits and encodes, and host nanoseconds before and inside the launches."""
     c = Counters()
     st = _lib.tgemm_host_counters(ctypes.byref(c))
     if st != OK:

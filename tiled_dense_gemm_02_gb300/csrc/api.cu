@@ -395,10 +395,13 @@ int make_plan_core(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, 
       const bool fits = tail > 0 && 2 * tail <= slots && p.k_blocks >= 2;
       if (fits && (opt.simt_split == 2 || (opt.simt_split == 0 && p.k_blocks >= 16))) {
         p.dp_tiles = static_cast<int>(tiles - tail);
-        p.ctas = static_cast<int>(tiles + tail);
+        p.ctas = static_cast<int>(tiles - tail + kSimtSplitWays * tail);
         p.split_stage = p.k_blocks / 2;
       }
     }
+    // Raster group height: 16 tile rows keep a round of 2 x SMs resident
+    // CTAs on about 16 rows of A and 19 columns of B at 152 SMs.
+    p.group_m = std::max(1, std::min(opt.group_m ? opt.group_m : 16, p.tiles_m));
     p.bn = kSimtBN;
     p.stages = 2;
     p.smem = 0;
@@ -443,7 +446,7 @@ int make_plan_core(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, 
   // bytes per SM and FLOP of the one-SM copy kernel, which per-thread copies
   // bound.  Cost: rounds x the B columns one SM copies per tile.
   const bool copy_pair_ok = p.kernel == TGEMM_KERNEL_TC_COPY && a_tma && pair_cap > 0 &&
-                            opt.cta_group != 1 && opt.stream_k != 2 && opt.swap_ab != 2 &&
+                            opt.cta_group != 1 && opt.swap_ab != 2 &&
                             opt.tile_k != 128 && opt.store_mode != 1 &&
                             (opt.tile_n == 0 || opt.tile_n == 128 || opt.tile_n == 256) &&
                             (opt.kernel == TGEMM_KERNEL_TC_COPY ? opt.cta_group == 2 : p.b_copy != 0);
@@ -481,6 +484,21 @@ int make_plan_core(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, 
       p.k_blocks = static_cast<int>((K + kTileK - 1) / kTileK);
       p.dp_tiles = static_cast<int>(tiles);
       p.ctas = static_cast<int>(2 * std::min<int64_t>(tiles, pair_cap));
+      // Stream-K split of the tiles past the last full round of pairs, as in
+      // the bulk-tensor pair kernel below (needs the caller's workspace).
+      if (opt.stream_k == 2) {
+        const int64_t cap = pair_cap;
+        const int64_t rem = tiles % cap;
+        const int64_t sk_iters = rem * p.k_blocks;
+        const int64_t need = sk_workspace_bytes(static_cast<int>(cap), p.bn);
+        if (rem != 0 && sk_iters >= cap && cap <= kSkMaxWorkers && workspace_bytes >= need &&
+            sk_iters < (int64_t(1) << 31)) {
+          p.dp_tiles = static_cast<int>(tiles - rem);
+          p.sk_iters = static_cast<int>(sk_iters);
+          p.workspace = need;
+          p.ctas = static_cast<int>(2 * cap);
+        }
+      }
       p.smem = copy_pair_smem(p.bn);
       if (batch > 1) p.batch_loop = true;
       return TGEMM_OK;
@@ -624,6 +642,15 @@ std::mutex g_map_mutex;
 MapSlot g_map_slots[kMapSlots];
 uint64_t g_map_clock = 0;
 std::atomic<uint64_t> g_map_hits{0}, g_map_encodes{0}, g_launch_calls{0};
+// Host nanoseconds of tensor-core product calls: from entry to the launch
+// call (validation, planning, tensor maps) and inside the launch call.
+std::atomic<uint64_t> g_ns_prepare{0}, g_ns_launch{0};
+
+uint64_t now_ns() {
+  return static_cast<uint64_t>(
+      std::chrono::duration_cast<std::chrono::nanoseconds>(std::chrono::steady_clock::now().time_since_epoch())
+          .count());
+}
 
 int encode_cached(CUtensorMap* map, CUtensorMapDataType type, int rank, const void* base, const cuuint64_t* dims,
                   const cuuint64_t* strides, const cuuint32_t* box, CUtensorMapSwizzle swizzle) {
@@ -770,6 +797,7 @@ bool batch_tma_ok(const Batch& bt, int dtype) {
 int run(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb, void* C,
         int64_t ldc, int dtype, const tgemm_options* o, const tgemm_epilogue* epi_in, void* workspace,
         int64_t workspace_bytes, cudaStream_t stream, const Batch& bt = Batch()) {
+  const uint64_t t_entry = now_ns();
   // validation that needs no device first, so bad arguments never touch CUDA
   Plan p;
   if (workspace_bytes < 0 || (workspace_bytes > 0 && (!workspace || reinterpret_cast<uint64_t>(workspace) % 256)))
@@ -817,7 +845,9 @@ int run(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void*
     a.ldc = ldc;
     a.vec = p.a_copy == 16 ? 1 : 0;
     a.epi = ep;
+    a.tiles_m = p.tiles_m;
     a.tiles_n = p.tiles_n;
+    a.group_m = p.group_m;
     a.full_tiles = p.dp_tiles;
     a.split_stage = p.split_stage;
     int64_t units = p.ctas;
@@ -827,9 +857,20 @@ int run(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void*
       a.split_stage = 0;
       units = a.full_tiles;
     } else {
-      // the halves add into zeros: clear the rows of C the split tiles cover
-      const int64_t r0 = static_cast<int64_t>(p.dp_tiles / p.tiles_n) * kSimtBM;
-      e = launch_zero_fill(static_cast<float*>(C) + r0 * ldc, M - r0, N, ldc, 4, stream);
+      // the halves add into zeros: clear the bounding box of the split tiles
+      // (a whole tile inside it is stored over the zeros)
+      int r_lo = p.tiles_m, r_hi = -1, c_lo = p.tiles_n, c_hi = -1;
+      for (int t = p.dp_tiles; t < p.tiles_m * p.tiles_n; ++t) {
+        int r, c;
+        simt_tile_coords(t, p.tiles_m, p.tiles_n, p.group_m, r, c);
+        r_lo = std::min(r_lo, r);
+        r_hi = std::max(r_hi, r);
+        c_lo = std::min(c_lo, c);
+        c_hi = std::max(c_hi, c);
+      }
+      const int64_t r0 = int64_t(r_lo) * kSimtBM, r1 = std::min<int64_t>(M, int64_t(r_hi + 1) * kSimtBM);
+      const int64_t c0 = int64_t(c_lo) * kSimtBN, c1 = std::min<int64_t>(N, int64_t(c_hi + 1) * kSimtBN);
+      e = launch_zero_fill(static_cast<float*>(C) + r0 * ldc + c0, r1 - r0, c1 - c0, ldc, 4, stream);
       if (e != cudaSuccess) return cuda_fail(e, "zero-fill launch");
     }
     e = launch_simt(a, units, stream);
@@ -923,6 +964,7 @@ int run(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void*
   a.timeout_ns = static_cast<unsigned long long>(to_us) * 1000ull;
   a.status = dev->status;
   g_launch_calls.fetch_add(1, std::memory_order_relaxed);
+  const uint64_t t_launch = now_ns();
   if (p.copy_pair)
     e = launch_tc_pair_copy(p.bn, mA, a, p.ctas / 2, stream);
   else if (p.swap)
@@ -931,6 +973,9 @@ int run(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void*
     e = launch_tc_pair(p.bn, p.store == 0, p.ksub, mA, mB, mBt, mC, a, p.ctas / 2, stream);
   else
     e = launch_tc(p.bn, p.kernel == TGEMM_KERNEL_TC_COPY, mA, mB, mC, a, p.ctas, stream);
+  const uint64_t t_done = now_ns();
+  g_ns_prepare.fetch_add(t_launch - t_entry, std::memory_order_relaxed);
+  g_ns_launch.fetch_add(t_done - t_launch, std::memory_order_relaxed);
   return e == cudaSuccess ? TGEMM_OK : cuda_fail(e, "tensor-core kernel launch");
 }
 
@@ -1255,6 +1300,8 @@ int tgemm_host_counters(tgemm_counters* out) {
   out->tc_launches = tgemm::g_launch_calls.load(std::memory_order_relaxed);
   out->map_hits = tgemm::g_map_hits.load(std::memory_order_relaxed);
   out->map_encodes = tgemm::g_map_encodes.load(std::memory_order_relaxed);
+  out->ns_prepare = tgemm::g_ns_prepare.load(std::memory_order_relaxed);
+  out->ns_launch = tgemm::g_ns_launch.load(std::memory_order_relaxed);
   return TGEMM_OK;
 }
 

@@ -35,13 +35,15 @@
 // whole 128-byte row segments.  Edge tiles load
 // zeros outside the matrix and mask their stores ("CUDA tile", section 四.4).
 //
-// Work units: the grid is one-dimensional.  Tiles are numbered row by row;
-// tiles [0, full_tiles) are computed whole, and every later tile by two CTAs,
-// one per half of its k-stages ("矩阵乘法中的平铺", K-splitting taken across
-// CTAs).  The host plans that split only for a last round of tiles that fills
-// at most half of the resident CTA slots: split, it ends in half the time.
-// The halves add their sums into C, which the host has zeroed; two additions
-// onto zero give the same float whichever lands first.
+// Work units: the grid is one-dimensional.  Tiles are numbered in grouped
+// order (simt_tile_coords: groups of tile rows, column by column within a
+// group); tiles [0, full_tiles) are computed whole, and every later tile by
+// two CTAs, one per half of its k-stages ("矩阵乘法中的平铺", K-splitting taken
+// across CTAs).  The host plans that split only for a last round of tiles that
+// fills at most half of the resident CTA slots: split, it ends in half the
+// time.  The halves add their sums into C, which the host has zeroed; two
+// additions onto zero give the same float whichever lands first
+// (kSimtSplitWays).
 #include "simt_sgemm.h"
 
 namespace tgemm {
@@ -149,12 +151,14 @@ __global__ void __launch_bounds__(THREADS, 2) simt_sgemm_kernel(const SimtArgs p
   bool half = false;
   if (!EPI && tile >= p.full_tiles) {
     const int h = tile - p.full_tiles;
-    tile = p.full_tiles + (h >> 1);
+    tile = p.full_tiles + h / kSimtSplitWays;
     half = true;
-    if (h & 1) s_begin = p.split_stage;
+    if (h % kSimtSplitWays) s_begin = p.split_stage;
     else s_end = p.split_stage;
   }
-  const int m0 = (tile / p.tiles_n) * BM, n0 = (tile % p.tiles_n) * BN;
+  int tile_row, tile_col;
+  simt_tile_coords(tile, p.tiles_m, p.tiles_n, p.group_m, tile_row, tile_col);
+  const int m0 = tile_row * BM, n0 = tile_col * BN;
 
   LoadPos q;
   {

@@ -30,6 +30,16 @@
 // both CTAs wait on.
 // Every wait is bounded (tc_common.cuh); the CTAs meet only at the two cluster
 // barriers (after set-up and before tensor memory is freed).
+//
+// Stream-K split (with a caller workspace): every role walks the pair's list
+// of work units (worker_unit, tc_common.cuh), k-stages [lo, hi) of one tile.
+// When the tiles leave pairs idle, the k-stages of the remaining tiles are
+// spread evenly over all pairs ("矩阵乘法中的平铺": splitting K into stages
+// leaves the total unchanged, so the stages of one tile may run on several
+// pairs).  A pair holding the start of a tile writes its fp32 partial sums to
+// the workspace and releases a per-warp flag; the pair holding the tile's last
+// k-stage waits for the flags, adds the partial sums in pair order (so the
+// result does not depend on timing), applies the epilogue and stores C.
 #include <atomic>
 
 #include "tc_common.cuh"
@@ -80,7 +90,7 @@ __global__ void __launch_bounds__(copy_pair_threads(), 1)
   static_assert(BN == 128 || BN == 256, "pair tile width");
   static_assert(copy_pair_smem_bytes(BN) <= kSmemLimit, "shared memory per CTA");
   static_assert(STAGES >= 3, "ring depth");
-  static_assert((4 * STAGES + 5) * 8 + 8 <= kCopyPairBarBytes, "barrier area");
+  static_assert((4 * STAGES + 5 + kEpiWarps) * 8 + 8 <= kCopyPairBarBytes, "barrier area");
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -93,7 +103,8 @@ __global__ void __launch_bounds__(copy_pair_threads(), 1)
   uint64_t* acc_full = empty + STAGES;
   uint64_t* acc_empty = acc_full + 2;
   uint64_t* drain = acc_empty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* epi_bar = drain + 1;  // one per epilogue warp: bulk copies of partial sums
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(epi_bar + kEpiWarps);
   volatile uint32_t* abort_flag = tmem_slot + 1;
 
   const int warp = threadIdx.x >> 5;
@@ -115,6 +126,7 @@ __global__ void __launch_bounds__(copy_pair_threads(), 1)
       ptx::mbar_init(ptx::smem_u32(&acc_empty[b]), 2 * kEpiWarps);  // leader: both CTAs' epilogues
     }
     ptx::mbar_init(ptx::smem_u32(drain), 1);
+    for (int w = 0; w < kEpiWarps; ++w) ptx::mbar_init(ptx::smem_u32(&epi_bar[w]), 1);
     *abort_flag = 0u;
     ptx::fence_barrier_init();
   }
@@ -130,7 +142,6 @@ __global__ void __launch_bounds__(copy_pair_threads(), 1)
   const uint32_t tmem_base = *tmem_slot;
 
   const Ctl ctl{abort_flag, args.timeout_ns, args.status};
-  const int kbs = args.k_blocks;
 
   if (warp == 0) {
     // ------------------------------------------------ bulk-tensor producer (A)
@@ -139,11 +150,12 @@ __global__ void __launch_bounds__(copy_pair_threads(), 1)
       int stage = 0;
       uint32_t phase = 0, filled = 0, last_parity = 0;
       bool ok = true;
-      for (int t = pair; ok && t < args.num_tiles; t += npairs) {
+      Unit u;
+      for (int ui = 0; ok && worker_unit(args, pair, npairs, ui, u); ++ui) {
         int mb, nb;
-        tile_coords(t, args, mb, nb);
+        tile_coords(u.tile, args, mb, nb);
         const int a_row = mb * 2 * kTileM + static_cast<int>(rank) * kTileM;
-        for (int kb = 0; kb < kbs; ++kb) {
+        for (int kb = u.lo; kb < u.hi; ++kb) {
           if (!wait_bounded(ptx::smem_u32(&empty[stage]), phase ^ 1u, ctl, SITE_PRODUCER_EMPTY)) {
             ok = false;
             break;
@@ -175,11 +187,12 @@ __global__ void __launch_bounds__(copy_pair_threads(), 1)
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
-      for (int t = pair; ok && t < args.num_tiles; t += npairs) {
+      Unit u;
+      for (int ui = 0; ok && worker_unit(args, pair, npairs, ui, u); ++ui) {
         if (!wait_bounded(ptx::smem_u32(&acc_empty[acc]), acc_phase ^ 1u, ctl, SITE_MMA_ACC_EMPTY)) break;
         ptx::tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * ACC);
-        for (int kb = 0; kb < kbs; ++kb) {
+        for (int kb = u.lo; kb < u.hi; ++kb) {
           if (!wait_bounded(ptx::smem_u32(&full[stage]), phase, ctl, SITE_MMA_FULL) ||
               !wait_bounded(ptx::smem_u32(&copy_done[stage]), phase, ctl, SITE_MMA_FULL) ||
               !wait_bounded_cluster(ptx::smem_u32(&peer_ready[stage]), phase, ctl, SITE_MMA_FULL)) {
@@ -196,7 +209,7 @@ __global__ void __launch_bounds__(copy_pair_threads(), 1)
             // A: K-major, 16 elements = 32 bytes along each swizzled row;
             // B: N-major, 16 k-rows = two 1 KB groups, atoms 8 KB apart
             ptx::tc_mma_f16_pair(d_tmem, sw128_desc(a0 + k * 32, 16, 1024), sw128_desc(b0 + k * 2048, 8192, 1024),
-                                 args.idesc, (kb | k) != 0 ? 1u : 0u);
+                                 args.idesc, (kb != u.lo || k != 0) ? 1u : 0u);
           ptx::tc_commit_pair_multicast(ptx::smem_u32(&empty[stage]), 0x3);
           if (++stage == STAGES) {
             stage = 0;
@@ -221,8 +234,11 @@ __global__ void __launch_bounds__(copy_pair_threads(), 1)
       // arrive on the leader's barriers of all of them.  A stage's next fill needs the
       // MMA's release of it, which needs this forward, so no stage can land
       // twice before it is forwarded.
-      const int my_tiles = pair < args.num_tiles ? (args.num_tiles - pair + npairs - 1) / npairs : 0;
-      const int total = my_tiles * kbs;
+      int total = 0;  // k-stages this pair stages, over all its units
+      {
+        Unit u;
+        for (int ui = 0; worker_unit(args, pair, npairs, ui, u); ++ui) total += u.hi - u.lo;
+      }
       const uint32_t ready0 = ptx::mapa_shared(ptx::smem_u32(&peer_ready[0]), 0);
       int stage = 0;
       uint32_t phase = 0;
@@ -256,14 +272,40 @@ __global__ void __launch_bounds__(copy_pair_threads(), 1)
     const int q = warp & 3;
     int acc = 0, sbuf = 0;
     uint32_t acc_phase = 0;
-    for (int t = pair; t < args.num_tiles; t += npairs) {
+    // this warp's partial-sum slot and flag (stream-K), per pair, CTA and warp
+    const int64_t slot_floats = sk_partial_floats(BN);
+    const int64_t warp_off = (static_cast<int64_t>(rank) * 4 + q) * 32 * BN;
+    const int flag_off = static_cast<int>(rank) * 4 + q;
+    uint32_t epi_phase = 0;
+    Unit u;
+    for (int ui = 0; worker_unit(args, pair, npairs, ui, u); ++ui) {
       int mb, nb;
-      tile_coords(t, args, mb, nb);
+      tile_coords(u.tile, args, mb, nb);
       if (!warp_wait(ptx::smem_u32(&acc_full[acc]), acc_phase, ctl, SITE_EPI_ACC_FULL)) break;
       ptx::tc_fence_after_sync();
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * ACC);
       const int row0 = mb * 2 * kTileM + static_cast<int>(rank) * kTileM + q * 32;
-      if (row0 < args.M) epilogue_tile<BN, false>(tbase, row0, nb * BN, args, nullptr, nullptr, sbuf, lane);
+      if (u.role == UNIT_PARTIAL) {
+        epilogue_partial<BN>(tbase, lane, args.sk_partials + pair * slot_floats + warp_off);
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) st_release_gpu(args.sk_flags + pair * 8 + flag_off, args.sk_epoch);
+      } else if (u.role == UNIT_FINISH) {
+        // the last unit of this pair: the ring is idle, each warp borrows a share of it
+        const int first = sk_first_contributor(args, pair, npairs, u);
+        if (!warp_wait_flags(args.sk_flags + first * 8 + flag_off, 8, pair - first, args.sk_epoch, ctl,
+                             SITE_SK_FLAG))
+          break;
+        constexpr int RING_SHARE = (STAGES * (A_BYTES + B_BYTES) / kEpiWarps) / 4096 * 4096;
+        static_assert(RING_SHARE / 4096 >= 2, "a 16-bit output chunk needs two 4 KB slots");
+        if (!epilogue_finish<BN, false>(tbase, row0, nb * BN, args, nullptr, nullptr, sbuf, lane,
+                                        args.sk_partials + first * slot_floats + warp_off, slot_floats, pair - first,
+                                        sA + (warp - 2) * RING_SHARE, RING_SHARE / 4096,
+                                        ptx::smem_u32(&epi_bar[warp - 2]), epi_phase, ctl))
+          break;
+      } else if (row0 < args.M) {
+        epilogue_tile<BN, false>(tbase, row0, nb * BN, args, nullptr, nullptr, sbuf, lane);
+      }
       ptx::tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive_cluster(ptx::mapa_shared(ptx::smem_u32(&acc_empty[acc]), 0));
@@ -281,11 +323,12 @@ __global__ void __launch_bounds__(copy_pair_threads(), 1)
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (int t = pair; ok && t < args.num_tiles; t += npairs) {
+      Unit u;
+      for (int ui = 0; ok && worker_unit(args, pair, npairs, ui, u); ++ui) {
         int mb, nb;
-        tile_coords(t, args, mb, nb);
+        tile_coords(u.tile, args, mb, nb);
         const int n0 = nb * BN + static_cast<int>(rank) * BNH;
-        for (int kb = 0; kb < kbs; ++kb) {
+        for (int kb = u.lo; kb < u.hi; ++kb) {
           if (!warp_wait(ptx::smem_u32(&empty[stage]), phase ^ 1u, ctl, SITE_COPY_EMPTY)) {
             ok = false;
             break;
