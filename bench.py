@@ -443,7 +443,7 @@ def time_workload(tg, w: wl.Workload, dev, flush, steps: int, peaks: dict, fp32_
                          "ai_flop_per_byte": ai, "dram_gbs_compulsory": w.compulsory_bytes / (ms / 1e3) / 1e9},
             "kernel": {k: v for k, v in plan.as_dict().items()
                        if k in ("kernel", "tile_m", "tile_n", "tile_k", "ctas", "cta_group", "swap_ab", "tuned",
-                                "sk_iters", "workspace_bytes")},
+                                "sk_iters", "workspace_bytes", "packed")},
             "call": "tgemm_gemm" if options is None else f"tgemm_gemm_ws {dict(options)}",
             "launches_per_step": kernel_launches_per_call(tg, plan, False)}
     return entry, (A, B, got)
@@ -486,9 +486,10 @@ def launch_floor(tg, dev, flush, steps: int = 50):
 def kernel_launches_per_call(tg, plan, epilogue: bool) -> int:
     """Kernels one library call launches for `plan`: a plain fp32 product whose
     last round of tiles is split into K halves first zeroes the rows of C those
-    halves add into (two launches); everything else is one launch."""
+    halves add into (two launches); each operand repacked into the workspace
+    adds one launch; everything else is one launch."""
     split = plan.kernel == tg.KERNEL_SIMT and plan.ctas != plan.tiles_m * plan.tiles_n
-    return 2 if split and not epilogue else 1
+    return (2 if split and not epilogue else 1) + bin(plan.packed).count("1")
 
 
 def run_ours(args, w: wl.Workload):
@@ -650,13 +651,16 @@ def run_ours(args, w: wl.Workload):
                                                              fp32_peak)
             except Exception as exc:
                 errors[name] = repr(exc)
-        # the ragged shape again with the stream-K split over every CTA pair (needs a workspace)
+        # the ragged shape again through tgemm_gemm_ws: with a workspace the
+        # library repacks B (3000-byte rows) for the bulk-tensor kernels; and
+        # the per-thread copy pairs with the stream-K split over every pair
         name = "bf16_1000x1500x4096_ragged"
-        try:
-            configs[name + "+stream_k"], outputs[name + "+stream_k"] = time_workload(
-                tg, wl.BY_NAME[name], dev, flush, 50, peaks, fp32_peak, options={"stream_k": 2})
-        except Exception as exc:
-            errors[name + "+stream_k"] = repr(exc)
+        for tag, opts in (("+workspace", {}), ("+stream_k", {"stream_k": 2, "repack": 1})):
+            try:
+                configs[name + tag], outputs[name + tag] = time_workload(
+                    tg, wl.BY_NAME[name], dev, flush, 50, peaks, fp32_peak, options=opts)
+            except Exception as exc:
+                errors[name + tag] = repr(exc)
         if fp32_peak:
             configs["fp32_peak_probe"] = fp32_peak
         try:

@@ -154,7 +154,18 @@ typedef struct tgemm_options {
                            when K >= 256), 1 off, 2 on whenever the round
                            fits and K spans two 16-deep stages.  A call with
                            an epilogue computes every tile whole */
-  int reserved[2];
+  int repack;           /* tensor-core paths with a workspace (tgemm_gemm_ws,
+                           tgemm_gemm_epilogue): an operand whose rows are not
+                           16-byte aligned (base or pitch) is first copied into
+                           the workspace with its pitch rounded up to a
+                           multiple of 8 elements, and the bulk-tensor kernels
+                           read that copy (one extra launch per copied
+                           operand).  0 auto: copy B when M >= 512 and A when
+                           N >= 512 (the product reads them several times),
+                           whenever the workspace holds the copies; 1 never;
+                           2 any such operand.  tgemm_workspace_size counts
+                           the copies' bytes */
+  int reserved[1];      /* must be 0 */
 } tgemm_options;
 
 /* tgemm_gemm with explicit options (opts may be NULL).  A forced kernel that
@@ -186,13 +197,16 @@ typedef struct tgemm_plan_info {
                         SIMT kernel: the rest are split in two K halves, and
                         ctas = dp_tiles + 2 x the split tiles) */
   int sk_iters;      /* k-stages of the remaining tiles split over the pairs */
-  int workspace_bytes; /* workspace the call uses (0 without stream-K) */
+  int workspace_bytes; /* workspace the call uses (0 without stream-K or
+                          repacked operands) */
   int cluster_ctas;  /* CTAs per cluster: 1 (one-SM tiles) or 2 (a pair) */
   int swap_ab;       /* 1: pairs with the MMA's operands exchanged (tile_m x
                         256 tiles of C computed as tiles of C^T) */
   int tuned;         /* 1: options from the library's table of measured
                         shapes (the call left every tuned option at 0 and its
                         shape and dtype match an entry exactly) */
+  int packed;        /* operands copied into the workspace before the
+                        product (tgemm_options.repack): 1 = A, 2 = B, 3 = both */
 } tgemm_plan_info;
 
 TGEMM_API int tgemm_plan(int64_t M, int64_t N, int64_t K,
@@ -212,8 +226,12 @@ TGEMM_API int tgemm_plan(int64_t M, int64_t N, int64_t K,
  * depend on timing) and stores C.
  *
  * tgemm_workspace_size: bytes of workspace tgemm_gemm_ws would use for these
- * arguments on the current device (0 when it would use none).  Same
- * validation and status codes as tgemm_gemm_ex.
+ * arguments on the current device, for the stream-K split and for operands it
+ * repacks (tgemm_options.repack); 0 when it would use none.  Same validation
+ * and status codes as tgemm_gemm_ex.
+ *
+ * Workspace layout: the first 4 KiB hold stream-K flags only, the partial sums
+ * follow, then the repacked operands.
  *
  * tgemm_gemm_ws: tgemm_gemm_ex with a workspace.  `workspace` is device memory
  * owned by the caller, 256-byte aligned, zero-initialised before its first use
@@ -250,7 +268,8 @@ TGEMM_API int tgemm_gemm_ws(int64_t M, int64_t N, int64_t K,
  * pool, or a service whose memory budget is fixed after start-up, can neither
  * give this library a workspace nor let it call cudaMalloc.  For them,
  * tgemm_gemm_noalloc behaves as tgemm_gemm_ws with the stream-K split on
- * (opts->stream_k 0 is read as 2; 1 turns it off), but takes its partial sums
+ * (opts->stream_k 0 is read as 2; 1 turns it off; opts->repack 0 is read as
+ * 1, so operands are not copied unless asked), but takes its partial sums
  * and flags from a scratch array of TGEMM_NOALLOC_SCRATCH_BYTES built into the
  * library, in device memory that every GPU loading the library holds until
  * the process exits.  It allocates nothing and calls no allocating routine.

@@ -406,7 +406,7 @@ def test_simt_split_planning(tg):
     st, p = plan(tg, 1024, 1024, 1024, dtype=0, sms=152)
     assert (p.dp_tiles, p.ctas) == (0, 128)
     # auto needs K >= 256 (16 stages); simt_split = 2 needs two stages
-    assert plan(tg, 64, 64, 64, dtype=0, sms=152)[1].ctas == 1
+    assert plan(tg, 64, 64, 64, dtype=0, sms=2)[1].ctas == 1
     assert plan(tg, 64, 64, 64, dtype=0, sms=152, simt_split=2)[1].ctas == 2
     assert plan(tg, 64, 64, 16, dtype=0, sms=152, simt_split=2)[1].ctas == 1
     assert plan(tg, 4096, 4096, 4096, dtype=0, sms=152, simt_split=1)[1].ctas == 1024
@@ -416,6 +416,21 @@ def test_simt_split_planning(tg):
     assert plan(tg, 64, 64, 64, dtype=0, simt_split=3)[0] == tg.ERR_INVALID_VALUE
     assert plan(tg, 64, 64, 64, dtype=0, simt_split=-1)[0] == tg.ERR_INVALID_VALUE
     assert plan(tg, 256, 256, 256, dtype=2, simt_split=2)[0] == tg.ERR_INVALID_VALUE
+
+
+def test_simt_small_product_planning(tg):
+    """fp32 products whose 128 x 128 tiles would fill at most an eighth of the
+    SMs, with K <= 2048, take the small-product kernel: 32 x 32 tiles, 32-deep
+    stages in a 4-stage ring, one CTA per tile."""
+    st, p = plan(tg, 64, 64, 64, dtype=0, sms=152)
+    assert st == tg.OK and p.kernel == tg.KERNEL_SIMT
+    assert (p.tile_m, p.tile_n, p.tile_k, p.stages, p.ctas, p.dp_tiles) == (32, 32, 32, 4, 4, 4)
+    assert plan(tg, 512, 512, 512, dtype=0, sms=152)[1].ctas == 256            # 16 big tiles x 8 <= 152
+    assert plan(tg, 640, 640, 640, dtype=0, sms=152)[1].tile_m == 128          # 25 big tiles: throughput kernel
+    assert plan(tg, 256, 256, 4096, dtype=0, sms=152)[1].tile_m == 128         # long K: throughput kernel
+    assert plan(tg, 64, 64, 64, dtype=0, sms=152, simt_split=2)[1].tile_m == 128  # a forced split
+    assert plan(tg, 70, 90, 33, dtype=0, sms=152)[1].ctas == 3 * 3
+    assert plan(tg, 64, 64, 64, dtype=2, sms=152)[1].tile_m != 32              # tensor-core dtypes never
 
 
 def test_simt_raster_group_planning(tg):
@@ -438,6 +453,10 @@ def test_simt_split_rule_on_random_shapes(tg):
         st, p = plan(tg, M, N, K, dtype=0, sms=sms)
         assert st == tg.OK
         tiles = -(-M // 128) * -(-N // 128)
+        if tiles * 8 <= sms and K <= 2048:  # the small-product kernel: one CTA per 32 x 32 tile
+            small = -(-M // 32) * -(-N // 32)
+            assert (p.tile_m, p.tiles_m * p.tiles_n, p.dp_tiles, p.ctas) == (32, small, small, small), (M, N, K, sms)
+            continue
         slots = 2 * sms
         tail = tiles % slots
         split = 0 < tail and 2 * tail <= slots and -(-K // 16) >= 16
@@ -531,3 +550,42 @@ def test_stream_k_partition_covers_every_stage_once(tiles, kb, workers):
     for t in range(dp, tiles):
         owners = sorted({seen[(t, k)] for k in range(kb)})
         assert seen[(t, kb - 1)] == owners[-1]
+
+
+def test_repack_planning(tg):
+    """Operands whose rows rule out bulk-tensor copies are repacked into the
+    workspace (when it holds them) and the bulk-tensor kernels read the copy;
+    the first 4 KiB stay reserved for stream-K flags."""
+    M, N, K = 1000, 1500, 4096
+    b_bytes = K * 1504 * 2                      # pitch 1500 -> 1504 elements
+    need = 4096 + (b_bytes + 255) // 256 * 256
+    st, p = plan(tg, M, N, K, dtype=2, sms=152, ws=need)
+    assert st == tg.OK and p.packed == 2 and p.kernel == tg.KERNEL_TC_TMA and p.b_copy_bytes == 0
+    assert p.workspace_bytes == need
+    # too small a workspace, repack = 1, or no workspace: the per-thread copy pairs
+    for kw in ({"ws": need - 1}, {"ws": need, "repack": 1}, {}):
+        st, p = plan(tg, M, N, K, dtype=2, sms=152, **kw)
+        assert st == tg.OK and p.packed == 0 and p.kernel == tg.KERNEL_TC_COPY and p.b_copy_bytes == 8, kw
+    # auto leaves B alone when the product reads it about once (M < 512); repack = 2 copies it
+    st, p = plan(tg, 300, N, K, dtype=2, sms=152, ws=need)
+    assert st == tg.OK and p.packed == 0
+    st, p = plan(tg, 300, N, K, dtype=2, sms=152, ws=need, repack=2)
+    assert st == tg.OK and p.packed == 2 and p.kernel == tg.KERNEL_TC_TMA
+    # an unaligned A (K = 4100: 8200-byte rows) is repacked too, both in one workspace
+    a_bytes = 1000 * 4104 * 2
+    need2 = 4096 + (a_bytes + 255) // 256 * 256 + (4100 * 1504 * 2 + 255) // 256 * 256
+    st, p = plan(tg, M, N, 4100, dtype=2, sms=152, ws=need2)
+    assert st == tg.OK and p.packed == 3 and p.kernel == tg.KERNEL_TC_TMA and p.workspace_bytes == need2
+    # with a stream-K split: flags, partial sums, then the copy
+    st, p = plan(tg, M, N, K, dtype=2, sms=152, ws=64 << 20, stream_k=2, cta_group=2, swap_ab=1, tile_n=128)
+    assert st == tg.OK and p.packed == 2 and p.sk_iters > 0
+    assert p.workspace_bytes == 4096 + 76 * 2 * 4 * 32 * 128 * 4 + (b_bytes + 255) // 256 * 256
+    # forced per-thread copies never repack; forced bulk-tensor copies need the copy
+    st, p = plan(tg, M, N, K, dtype=2, sms=152, ws=need, kernel=tg.KERNEL_TC_COPY)
+    assert st == tg.OK and p.packed == 0
+    assert plan(tg, M, N, K, dtype=2, sms=152, ws=need, kernel=tg.KERNEL_TC_TMA)[1].packed == 2
+    assert plan(tg, M, N, K, dtype=2, sms=152, kernel=tg.KERNEL_TC_TMA)[0] == tg.ERR_INVALID_VALUE
+    for bad in ({"repack": 3}, {"repack": -1}):
+        assert plan(tg, M, N, K, dtype=2, ws=need, **bad)[0] == tg.ERR_INVALID_VALUE
+    # fp32 (SIMT) never repacks
+    assert plan(tg, M, N, K, dtype=0, ldb=1501, ws=64 << 20)[1].packed == 0

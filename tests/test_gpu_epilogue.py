@@ -105,7 +105,7 @@ def test_epilogue_stream_k_finisher(epi_name):
 def test_epilogue_copy_pairs_stream_k(epi_name):
     """Unaligned B rows on CTA pairs with the stream-K split: the pair that
     finishes a tile applies the epilogue once, to the sum of all partials."""
-    opts = {"cta_group": 2, "tile_n": 128, "max_ctas": 16, "stream_k": 2}
+    opts = {"cta_group": 2, "tile_n": 128, "max_ctas": 16, "stream_k": 2, "repack": 1}
     res = run_case(1100, 1300, 640, wl.BF16, epi_name, opts, seed=86, workspace=True, ldb=1302)
     assert res.plan.kernel == 2 and res.plan.sk_iters > 0
 

@@ -122,6 +122,21 @@ def test_simt_raster_groups_with_split_tail(group_m):
     H.check_full(res, A, B, M, N, K, wl.F32, f"simt group {group_m}")
 
 
+@pytest.mark.parametrize("K", [1, 31, 32, 33, 96, 97, 128, 129, 640, 2048])
+@pytest.mark.parametrize("vec", [True, False], ids=["vec", "scalar"])
+def test_simt_small_kernel(K, vec):
+    """The small-product kernel (32 x 32 tiles, 32-deep stages, 4-stage ring):
+    K around the stage and ring depths (every chunk in flight at once up to
+    K = 96), ragged M and N; 16-byte copies where every row is 16-byte aligned,
+    4-byte copies where none is (padding holds NaN, never read)."""
+    M, N = 70, 90
+    lda, ldb, ldc = ((K + 3) // 4 * 4, 92, 92) if vec else (K + 5, 93, 91)
+    A, B, res = case(M, N, K, wl.F32, seed=124, lda=lda, ldb=ldb, ldc=ldc)
+    assert res.plan.tile_m == 32 and res.plan.ctas == 3 * 3
+    assert res.plan.store_bytes == (16 if vec else 4)
+    H.check_full(res, A, B, M, N, K, wl.F32, f"simt small K {K}")
+
+
 def test_simt_split_is_deterministic():
     """Two additions onto zero commute: repeated calls give the same bits."""
     A, B, r1 = case(300, 200, 1000, wl.F32, seed=122, options={"simt_split": 2})

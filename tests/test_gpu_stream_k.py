@@ -111,7 +111,7 @@ def test_copy_pair_stream_k(dtype, tile_n, max_ctas, ldb_pad):
     copy B per thread, with the tiles past the last full round of pairs split
     along K: ragged M, N and K, finishing pairs add one or more partial sums."""
     M, N, K = 1100, 1300, 1000
-    opts = {"cta_group": 2, "tile_n": tile_n, "max_ctas": max_ctas, "stream_k": 2}
+    opts = {"cta_group": 2, "tile_n": tile_n, "max_ctas": max_ctas, "stream_k": 2, "repack": 1}
     A, B, res = case(M, N, K, dtype, opts, seed=75, ldb=N + ldb_pad)
     assert res.plan.kernel == 2 and res.plan.cta_group == 2 and res.plan.sk_iters > 0
     assert res.plan.b_copy_bytes == {0: 8, 6: 4, 1: 2}[ldb_pad]
@@ -124,11 +124,12 @@ def test_copy_pair_stream_k_ragged_workload():
     second call through the same workspace gives the same bits."""
     w = wl.BY_NAME["bf16_1000x1500x4096_ragged"]
     A, B = wl.make_inputs(w)
-    r1 = H.run_gpu(A, B, w.M, w.N, w.K, w.dtype, workspace=True, options={"stream_k": 2})
+    opts = {"stream_k": 2, "repack": 1}
+    r1 = H.run_gpu(A, B, w.M, w.N, w.K, w.dtype, workspace=True, options=opts)
     assert r1.plan.kernel == 2 and r1.plan.cta_group == 2 and r1.plan.sk_iters == 48 * 64
     assert r1.plan.dp_tiles == 0
     H.check_full(r1, A, B, w.M, w.N, w.K, w.dtype, "ragged workload, stream-K")
-    r2 = H.run_gpu(A, B, w.M, w.N, w.K, w.dtype, workspace=r1.workspace, options={"stream_k": 2})
+    r2 = H.run_gpu(A, B, w.M, w.N, w.K, w.dtype, workspace=r1.workspace, options=opts)
     assert np.array_equal(r1.raw, r2.raw)
 
 
@@ -138,7 +139,7 @@ def test_copy_pair_stream_k_short_k(K):
     on 76 pairs): ranges of one or two stages, tiles finished by pairs that
     hold a single stage; B rows of 1804 bytes (4-byte granules)."""
     M, N = 600, 900
-    opts = {"cta_group": 2, "tile_n": 128, "stream_k": 2}
+    opts = {"cta_group": 2, "tile_n": 128, "stream_k": 2, "repack": 1}
     A, B, res = case(M, N, K, wl.BF16, opts, seed=76, lda=(K + 7) // 8 * 8, ldb=N + 2)
     assert res.plan.kernel == 2 and res.plan.sk_iters > 0 and res.plan.b_copy_bytes == 4
     H.check_full(res, A, B, M, N, K, wl.BF16, f"copy-pair stream-K K {K}")

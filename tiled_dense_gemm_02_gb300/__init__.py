@@ -41,7 +41,7 @@ class Options(ctypes.Structure):
                 ("inject_fault", ctypes.c_int), ("cta_group", ctypes.c_int), ("tile_k", ctypes.c_int),
                 ("stream_k", ctypes.c_int), ("reserved0", ctypes.c_int),
                 ("swap_ab", ctypes.c_int), ("tile_m", ctypes.c_int), ("simt_split", ctypes.c_int),
-                ("reserved", ctypes.c_int * 2)]
+                ("repack", ctypes.c_int), ("reserved", ctypes.c_int * 1)]
 
 
 class Epilogue(ctypes.Structure):
@@ -58,7 +58,8 @@ class PlanInfo(ctypes.Structure):
                 ("a_copy_bytes", ctypes.c_int), ("b_copy_bytes", ctypes.c_int), ("store_bytes", ctypes.c_int),
                 ("smem_bytes", ctypes.c_int), ("cta_group", ctypes.c_int), ("dp_tiles", ctypes.c_int),
                 ("sk_iters", ctypes.c_int), ("workspace_bytes", ctypes.c_int),
-                ("cluster_ctas", ctypes.c_int), ("swap_ab", ctypes.c_int), ("tuned", ctypes.c_int)]
+                ("cluster_ctas", ctypes.c_int), ("swap_ab", ctypes.c_int), ("tuned", ctypes.c_int),
+                ("packed", ctypes.c_int)]
 
     def as_dict(self) -> dict:
         return {name: getattr(self, name) for name, _ in self._fields_ if name != "reserved"}

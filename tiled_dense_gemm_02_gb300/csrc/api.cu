@@ -177,7 +177,12 @@ struct Plan {
   int dp_tiles = 0, sk_iters = 0;  // stream-K split (sk_iters == 0: whole tiles only)
   int64_t workspace = 0;          // bytes of workspace the stream-K split uses
   int split_stage = 0;            // SIMT kernel: k-stage dividing the halves of its split tiles (0: none)
+  bool simt_small = false;        // fp32: the small-product kernel (32 x 32 tiles)
   int64_t batch = 1;              // matrices computed by one launch (strided batch, swapped kernel)
+  int packed = 0;                 // operands repacked into the workspace first: 1 = A, 2 = B
+  int64_t lda_p = 0, ldb_p = 0;   // their pitches there (elements, multiples of 8)
+  int64_t off_a = 0, off_b = 0;   // their byte offsets in the workspace
+  int granule_a = 0, granule_b = 0;  // the source rows' alignment (bytes)
   bool batch_loop = false;        // a batch the kernels cannot index: one launch per matrix
   bool tuned = false;             // options from the tuned-shape table
 };
@@ -289,6 +294,14 @@ const TunedShape kTuned[] = {
     {0, 0, 0, -1, 0, 0, 0, 0, 0, 0, 0}  // end
 };
 
+}  // namespace
+
+// Row repack of a 16-bit operand into a 16-byte-aligned pitch (repack.cu).
+cudaError_t launch_repack(const void* src, int64_t ld_src, void* dst, int64_t ld_dst, int rows, int cols,
+                          int src_granule, int sms, cudaStream_t stream);
+
+namespace {
+
 const TunedShape* tuned_entry(int64_t M, int64_t N, int64_t K, int dtype, const tgemm_options& o) {
   if (o.kernel || o.tile_n || o.group_m || o.max_ctas || o.cta_group || o.tile_k || o.stream_k || o.swap_ab ||
       o.tile_m)
@@ -351,6 +364,7 @@ int make_plan_core(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, 
   if (opt.group_m < 0 || opt.max_ctas < 0 || opt.store_mode < 0 || opt.store_mode > 2 || opt.wait_timeout_us < 0 ||
       opt.cta_group < 0 || opt.cta_group > 2 || (opt.tile_k != 0 && opt.tile_k != 64 && opt.tile_k != 128) ||
       opt.stream_k < 0 || opt.stream_k > 2 || opt.reserved0 != 0 || opt.swap_ab < 0 || opt.swap_ab > 2 ||
+      opt.repack < 0 || opt.repack > 2 || opt.reserved[0] != 0 ||
       (opt.swap_ab == 2 && (opt.stream_k == 2 || opt.cta_group == 1 || (opt.tile_n != 0 && opt.tile_n != 256))) ||
       (opt.tile_m != 0 && (opt.swap_ab != 2 || !tc2_valid_bn(opt.tile_m))))
     return TGEMM_ERR_INVALID_VALUE;
@@ -408,6 +422,22 @@ int make_plan_core(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, 
     const bool vec = reinterpret_cast<uint64_t>(A) % 16 == 0 && reinterpret_cast<uint64_t>(B) % 16 == 0 &&
                      reinterpret_cast<uint64_t>(C) % 16 == 0 && lda % 4 == 0 && ldb % 4 == 0 && ldc % 4 == 0;
     p.a_copy = p.b_copy = p.store = vec ? 16 : 4;
+    // Small products: when the 128 x 128 tiles would occupy at most an
+    // eighth of the SMs and K is short, 32 x 32 tiles with a deep copy ring
+    // finish sooner (fixed costs dominate; more CTAs, fewer waits on DRAM).
+    // Not with a forced split; the fused epilogue is supported.
+    if (opt.simt_split != 2 && tiles * 8 <= sms && K <= 2048) {
+      p.simt_small = true;
+      p.split_stage = 0;
+      p.tiles_m = static_cast<int>((M + kSimtSmallTile - 1) / kSimtSmallTile);
+      p.tiles_n = static_cast<int>((N + kSimtSmallTile - 1) / kSimtSmallTile);
+      if (p.tiles_m > 65535) return TGEMM_ERR_TOO_LARGE;
+      p.ctas = p.dp_tiles = p.tiles_m * p.tiles_n;
+      p.bn = kSimtSmallTile;
+      p.stages = kSimtSmallStages;
+      p.k_blocks = static_cast<int>((K + kSimtSmallK - 1) / kSimtSmallK);
+      p.group_m = 1;
+    }
     return TGEMM_OK;
   }
   if (opt.kernel == TGEMM_KERNEL_SIMT) return TGEMM_ERR_INVALID_VALUE;
@@ -419,9 +449,48 @@ int make_plan_core(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, 
   // is used only when the row's byte extent is a multiple of 16 (otherwise it
   // would overwrite the ldc padding, or the bytes past the last row).
   const bool c_tma = gc == 16 && (N * eo) % 16 == 0 && ldc * eo < (int64_t(1) << 40);
+  // Repack through the caller's workspace: an operand whose rows rule out
+  // bulk-tensor copies is first copied into the workspace with a pitch of a
+  // multiple of 8 elements (16 bytes), and the bulk-tensor kernels read that
+  // copy.  Auto repacks an operand the product reads several times over (B
+  // when M >= 512, A when N >= 512); 2 repacks any such operand, 1 never.
+  // The workspace keeps its first kSkFlagBytes for stream-K flags, then the
+  // partial sums (if any), then the copies.
+  bool a_ok = a_tma, b_ok = b_tma;
+  int64_t pack_a = 0, pack_b = 0;
+  if (opt.repack != 1 && opt.kernel != TGEMM_KERNEL_TC_COPY && workspace_bytes > 0) {
+    const int64_t lda_p = (K + 7) / 8 * 8, ldb_p = (N + 7) / 8 * 8;
+    const bool want_a = !a_tma && (opt.repack == 2 || N >= 512) && lda_p * 2 < (int64_t(1) << 40);
+    const bool want_b = !b_tma && (opt.repack == 2 || M >= 512) && ldb_p * 2 < (int64_t(1) << 40);
+    const int64_t bytes_a = want_a ? (M * lda_p * 2 + 255) / 256 * 256 : 0;
+    const int64_t bytes_b = want_b ? (K * ldb_p * 2 + 255) / 256 * 256 : 0;
+    if ((want_a || want_b) && kSkFlagBytes + bytes_a + bytes_b <= workspace_bytes) {
+      pack_a = bytes_a;
+      pack_b = bytes_b;
+      p.packed = (want_a ? 1 : 0) | (want_b ? 2 : 0);
+      p.lda_p = lda_p;
+      p.ldb_p = ldb_p;
+      p.granule_a = ga;
+      p.granule_b = gb;
+      a_ok = a_ok || want_a;
+      b_ok = b_ok || want_b;
+      // what is left of the workspace for a stream-K split (its own flag
+      // region is the one already reserved)
+      workspace_bytes -= bytes_a + bytes_b;
+    }
+  }
+  // byte offsets of the copies, after the stream-K region (or after the
+  // reserved flag region when there is no split)
+  auto place_copies = [&]() {
+    if (!p.packed) return;
+    const int64_t base = p.workspace > 0 ? p.workspace : kSkFlagBytes;
+    p.off_a = base;
+    p.off_b = base + pack_a;
+    p.workspace = base + pack_a + pack_b;
+  };
+  if (opt.kernel == TGEMM_KERNEL_TC_TMA && (!a_ok || !b_ok)) return TGEMM_ERR_INVALID_VALUE;
   switch (opt.kernel) {
     case TGEMM_KERNEL_TC_TMA:
-      if (!a_tma || !b_tma) return TGEMM_ERR_INVALID_VALUE;
       p.kernel = TGEMM_KERNEL_TC_TMA;
       break;
     case TGEMM_KERNEL_TC_COPY:
@@ -430,9 +499,9 @@ int make_plan_core(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, 
       p.b_copy = gb;
       break;
     default:
-      p.kernel = (a_tma && b_tma) ? TGEMM_KERNEL_TC_TMA : TGEMM_KERNEL_TC_COPY;
-      p.a_copy = a_tma ? 0 : ga;
-      p.b_copy = b_tma ? 0 : gb;
+      p.kernel = (a_ok && b_ok) ? TGEMM_KERNEL_TC_TMA : TGEMM_KERNEL_TC_COPY;
+      p.a_copy = a_ok ? 0 : ga;
+      p.b_copy = b_ok ? 0 : gb;
   }
   if (opt.store_mode == 1 && !c_tma) return TGEMM_ERR_INVALID_VALUE;
   p.store = (c_tma && opt.store_mode != 2) ? 0 : gc;
@@ -445,7 +514,7 @@ int make_plan_core(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, 
   // B per thread, each CTA its half of the tile's columns, move half the B
   // bytes per SM and FLOP of the one-SM copy kernel, which per-thread copies
   // bound.  Cost: rounds x the B columns one SM copies per tile.
-  const bool copy_pair_ok = p.kernel == TGEMM_KERNEL_TC_COPY && a_tma && pair_cap > 0 &&
+  const bool copy_pair_ok = p.kernel == TGEMM_KERNEL_TC_COPY && a_ok && pair_cap > 0 &&
                             opt.cta_group != 1 && opt.swap_ab != 2 &&
                             opt.tile_k != 128 && opt.store_mode != 1 &&
                             (opt.tile_n == 0 || opt.tile_n == 128 || opt.tile_n == 256) &&
@@ -501,6 +570,7 @@ int make_plan_core(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, 
       }
       p.smem = copy_pair_smem(p.bn);
       if (batch > 1) p.batch_loop = true;
+      place_copies();
       return TGEMM_OK;
     }
   }
@@ -610,6 +680,7 @@ int make_plan_core(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, 
   p.ctas = static_cast<int>(ctas);
   p.smem = p.swap ? tc2_smem_bytes(p.tm, true, p.ksub)
                   : (p.pair ? tc2_smem_bytes(p.bn, p.store == 0, p.ksub) : tc_smem_bytes(p.bn));
+  place_copies();
   return TGEMM_OK;
 }
 
@@ -845,6 +916,10 @@ int run(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void*
     a.ldc = ldc;
     a.vec = p.a_copy == 16 ? 1 : 0;
     a.epi = ep;
+    if (p.simt_small) {
+      e = launch_simt_small(a, stream);
+      return e == cudaSuccess ? TGEMM_OK : cuda_fail(e, "SIMT kernel launch");
+    }
     a.tiles_m = p.tiles_m;
     a.tiles_n = p.tiles_n;
     a.group_m = p.group_m;
@@ -878,6 +953,23 @@ int run(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void*
   }
   const bool bf16 = (dtype == TGEMM_BF16 || dtype == TGEMM_BF16_F32OUT);
   const int eo = out_bytes(dtype);
+  // operands repacked into the workspace: copy them, then read the copies
+  if (p.packed & 1) {
+    void* dst = static_cast<char*>(workspace) + p.off_a;
+    e = launch_repack(A, lda, dst, p.lda_p, static_cast<int>(M), static_cast<int>(K), p.granule_a, dev->sm_count,
+                      stream);
+    if (e != cudaSuccess) return cuda_fail(e, "repack launch");
+    A = dst;
+    lda = p.lda_p;
+  }
+  if (p.packed & 2) {
+    void* dst = static_cast<char*>(workspace) + p.off_b;
+    e = launch_repack(B, ldb, dst, p.ldb_p, static_cast<int>(K), static_cast<int>(N), p.granule_b, dev->sm_count,
+                      stream);
+    if (e != cudaSuccess) return cuda_fail(e, "repack launch");
+    B = dst;
+    ldb = p.ldb_p;
+  }
   CUtensorMap mA, mB, mBt, mC;
   std::memset(&mA, 0, sizeof mA);
   std::memset(&mB, 0, sizeof mB);
@@ -963,6 +1055,7 @@ int run(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void*
   const int to_us = (o && o->wait_timeout_us) ? o->wait_timeout_us : 2000000;
   a.timeout_ns = static_cast<unsigned long long>(to_us) * 1000ull;
   a.status = dev->status;
+  a.pdl = p.packed ? 1 : 0;  // the product follows its operands' repack on the stream
   g_launch_calls.fetch_add(1, std::memory_order_relaxed);
   const uint64_t t_launch = now_ns();
   if (p.copy_pair)
@@ -1215,7 +1308,9 @@ int tgemm_workspace_size(int64_t M, int64_t N, int64_t K, const void* A, int64_t
   if (!bytes) return TGEMM_ERR_INVALID_VALUE;
   *bytes = 0;
   tgemm::Plan p;
-  int st = tgemm::make_plan(M, N, K, A, lda, B, ldb, C, ldc, dtype, opts, 1, 1, 0, p);
+  // validated as the call would be with an unbounded workspace (a forced
+  // bulk-tensor option may be possible only with a repacked operand)
+  int st = tgemm::make_plan(M, N, K, A, lda, B, ldb, C, ldc, dtype, opts, 1, 1, INT64_MAX, p);
   if (st != TGEMM_OK || p.noop || p.zero) return st;
   tgemm::DeviceInfo* dev = nullptr;
   st = tgemm::device_info(&dev);
@@ -1237,9 +1332,11 @@ int tgemm_plan(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, cons
     std::memset(out, 0, sizeof *out);
     if (st == TGEMM_OK && !p.noop && !p.zero) {
       out->kernel = p.kernel;
-      out->tile_m = p.kernel == TGEMM_KERNEL_SIMT ? tgemm::kSimtBM : (p.swap ? p.tm : (p.pair ? 2 : 1) * tgemm::kTileM);
+      out->tile_m = p.kernel == TGEMM_KERNEL_SIMT ? (p.simt_small ? tgemm::kSimtSmallTile : tgemm::kSimtBM)
+                                                  : (p.swap ? p.tm : (p.pair ? 2 : 1) * tgemm::kTileM);
       out->tile_n = p.bn;
-      out->tile_k = p.kernel == TGEMM_KERNEL_SIMT ? tgemm::kSimtBK : tgemm::kTileK * p.ksub;
+      out->tile_k = p.kernel == TGEMM_KERNEL_SIMT ? (p.simt_small ? tgemm::kSimtSmallK : tgemm::kSimtBK)
+                                                  : tgemm::kTileK * p.ksub;
       out->stages = p.stages;
       out->tiles_m = p.tiles_m;
       out->tiles_n = p.tiles_n;
@@ -1256,6 +1353,7 @@ int tgemm_plan(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, cons
       out->dp_tiles = p.dp_tiles;
       out->sk_iters = p.sk_iters;
       out->workspace_bytes = p.workspace;
+      out->packed = p.packed;
     }
   }
   return st;
@@ -1356,9 +1454,10 @@ extern "C" int tgemm_gemm_noalloc(int64_t M, int64_t N, int64_t K, const void* A
   std::memset(&o, 0, sizeof o);
   if (opts) o = *opts;
   if (o.stream_k == 0) o.stream_k = 2;  // this entry point is the stream-K variant
+  if (o.repack == 0) o.repack = 1;      // and does not repack operands unless asked
   // validation first (no CUDA call on bad arguments)
   tgemm::Plan p;
-  int st = tgemm::make_plan(M, N, K, A, lda, B, ldb, C, ldc, dtype, &o, 1, 1, 0, p);
+  int st = tgemm::make_plan(M, N, K, A, lda, B, ldb, C, ldc, dtype, &o, 1, 1, INT64_MAX, p);
   if (st != TGEMM_OK || p.noop) return st;
   tgemm::DeviceInfo* dev = nullptr;
   st = tgemm::device_info(&dev);

@@ -231,6 +231,13 @@ __device__ __forceinline__ void st_shared_u16(uint32_t addr, uint16_t v) {
 
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 
+// Programmatic dependent launch.  griddep_wait: wait until the grids this one
+// depends on have completed and their memory is visible (returns at once for
+// a grid launched without the dependency).  griddep_launch_dependents: let
+// the grid that depends on this one be scheduled now.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" :::); }
+
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
@@ -297,6 +304,7 @@ __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)
 }
 
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
 
 
 // ------------------------------------------------------- CTA pairs (clusters of 2)

@@ -53,4 +53,12 @@ __host__ __device__ inline void simt_tile_coords(int t, int tiles_m, int tiles_n
 // Launches `units` CTAs: tiles [0, full_tiles) whole, then two per later tile.
 cudaError_t launch_simt(const SimtArgs& args, int64_t units, cudaStream_t stream);
 
+// The small-product kernel (simt_small.cu): 32 x 32 tiles, 32-deep K stages
+// through a 4-stage ring of asynchronous copies, one CTA per tile.  Uses
+// M, N, K, the operands, vec and epi of `args`.
+constexpr int kSimtSmallTile = 32;
+constexpr int kSimtSmallK = 32;
+constexpr int kSimtSmallStages = 4;
+cudaError_t launch_simt_small(const SimtArgs& args, cudaStream_t stream);
+
 }  // namespace tgemm

@@ -109,6 +109,7 @@ __global__ void __launch_bounds__(tc_threads(kCopy), 1)
   if (warp == 0) {
     // ------------------------------------------------ bulk-tensor producer
     if (lane == 0 && has_tma && !args.inject_fault) {
+      ptx::griddep_wait();  // operands written by the kernel before (repack) are visible
       const bool a_tma = args.a_copy == 0, b_tma = args.b_copy == 0;
       const uint32_t tx = (a_tma ? A_BYTES : 0) + (b_tma ? B_BYTES : 0);
       int stage = 0;
@@ -247,6 +248,7 @@ __global__ void __launch_bounds__(tc_threads(kCopy), 1)
                       args.M, args.N, args.K, args.a_copy, args.b_copy};
     const uint32_t sA_u = ptx::smem_u32(sA), sB_u = ptx::smem_u32(sB);
     if (has_copy && !args.inject_fault) {
+      ptx::griddep_wait();
       const bool sync_arrive = ops.a_copy == 2 || ops.b_copy == 2;
       int stage = 0;
       uint32_t phase = 0;
@@ -337,8 +339,15 @@ cudaError_t launch_one(const CUtensorMap& mA, const CUtensorMap& mB, const CUten
     if (e != cudaSuccess) return e;
     done_mask.fetch_or(bit, std::memory_order_acq_rel);
   }
-  kernel<<<ctas, tc_threads(kCopy), smem, stream>>>(mA, mB, mC, args);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(ctas), 1, 1);
+  cfg.blockDim = dim3(tc_threads(kCopy), 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  cfg.attrs = attr;
+  cfg.numAttrs = static_cast<unsigned>(tc_launch_attrs(attr, 1, args));
+  return cudaLaunchKernelEx(&cfg, kernel, mA, mB, mC, args);
 }
 
 }  // namespace

@@ -112,6 +112,7 @@ __global__ void __launch_bounds__(32 * (2 + kEpiWarps), 1)
   if (warp == 0) {
     // ------------------------------------------------ bulk-tensor producer
     if (lane == 0 && !args.inject_fault) {
+      ptx::griddep_wait();  // operands written by the kernel before (repack) are visible
       const uint32_t tx_pair = 2u * (A_BYTES + B_LOAD);
       int stage = 0;
       uint32_t phase = 0, filled = 0, last_parity = 0;
@@ -284,13 +285,9 @@ cudaError_t launch_pair(const CUtensorMap& mA, const CUtensorMap& mB, const CUte
   cfg.blockDim = dim3(32 * (2 + kEpiWarps), 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
+  cudaLaunchAttribute attr[2];
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = static_cast<unsigned>(tc_launch_attrs(attr, 2, args));
   return cudaLaunchKernelEx(&cfg, kernel, mA, mB, mBt, mC, args);
 }
 

@@ -146,6 +146,7 @@ __global__ void __launch_bounds__(copy_pair_threads(), 1)
   if (warp == 0) {
     // ------------------------------------------------ bulk-tensor producer (A)
     if (lane == 0 && !args.inject_fault) {
+      ptx::griddep_wait();  // operands written by the kernel before (repack) are visible
       const uint32_t tx_pair = 2u * A_BYTES;
       int stage = 0;
       uint32_t phase = 0, filled = 0, last_parity = 0;
@@ -319,6 +320,7 @@ __global__ void __launch_bounds__(copy_pair_threads(), 1)
                       args.M, args.N, args.K, 0, args.b_copy};
     const uint32_t sB_u = ptx::smem_u32(sB);
     if (!args.inject_fault) {
+      ptx::griddep_wait();
       const bool sync_arrive = ops.b_copy == 2;
       int stage = 0;
       uint32_t phase = 0;
@@ -383,13 +385,9 @@ cudaError_t launch_copy_pair(const CUtensorMap& mA, const TcArgs& args, int pair
   cfg.blockDim = dim3(copy_pair_threads(), 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
+  cudaLaunchAttribute attr[2];
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = static_cast<unsigned>(tc_launch_attrs(attr, 2, args));
   return cudaLaunchKernelEx(&cfg, kernel, mA, args);
 }
 

@@ -91,7 +91,30 @@ struct TcArgs {
   // product is a batch of one.
   int tiles_per;
   int64_t stride_a, stride_b, stride_c;
+  // 1: launched as a programmatic dependent of the kernel before it on the
+  // stream (the repack of an operand): the producers wait for that kernel
+  // (griddep_wait) before their first load, while set-up overlaps its end.
+  int pdl;
 };
+
+// Launch attributes of a tensor-core launch: the 2-CTA cluster (pairs) and, when
+// args.pdl, programmatic stream serialisation.  Returns the number used.
+inline int tc_launch_attrs(cudaLaunchAttribute (&attr)[2], int cluster, const TcArgs& args) {
+  int n = 0;
+  if (cluster > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = cluster;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  if (args.pdl) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  return n;
+}
 
 // Workspace of the stream-K tail for `workers` CTA pairs and tile width bn.
 constexpr int64_t sk_partial_floats(int bn) { return int64_t(2) * 4 * 32 * bn; }
