@@ -414,7 +414,9 @@ TGEMM_API int tgemm_transpose(int64_t rows, int64_t cols,
  * dA, dB, dC: device buffers owned by the caller, at least M*K, K*N and M*N
  *   elements, used densely (row pitches K, N and N).  Afterwards dC holds the
  *   product; dA and dB hold the copied operands.  They must not overlap.
- * panels: row panels of A and C (0 = chosen by the library; 1 = no overlap).
+ * panels: row panels of A and C (0 = chosen by the library: one when C is
+ *   below 6 MB, else graduated whole numbers of 128-row tiles, small first so
+ *   that C's copy back starts early; n > 0 = n even panels; 1 = no overlap).
  * stream: everything the call does follows the work already enqueued on
  *   `stream`, and later work on `stream` follows all of it, including the
  *   copy of C to the host.  The call returns once the work is enqueued:

@@ -1234,20 +1234,33 @@ int tgemm_gemm_host(int64_t M, int64_t N, int64_t K, const void* A_host, int64_t
     if (ranges_overlap(a0, a1, b0, b1) || ranges_overlap(c0, c1, a0, a1) || ranges_overlap(c0, c1, b0, b1))
       return TGEMM_ERR_ALIAS;
   }
-  // Row panels, each a whole number of 128-row tiles, so that the copy of one
-  // panel of C back to the host overlaps the copies in and the products of the
-  // next.  What can overlap is C's copy: with C below 6 MB one panel measured
-  // as fast as several; above, about one panel per 12 MB of C (bf16 4096^3 ->
-  // fp32 on GB300: 772 us in one panel, 623-632 us in 4-6; the copy engines
-  // move about 200 GB/s each way and 335 GB/s in both directions at once).
+  // Row panels, so that the copy of one panel of C back to the host overlaps
+  // the copies in and the products of the next.  What can overlap is C's copy,
+  // and it can start only once all of B, the first panel of A and that
+  // panel's product are done.  Auto: one panel when C is below 6 MB (nothing
+  // to overlap); above, graduated whole numbers of 128-row tiles, u, u, 2u,
+  // then 4u, with u about M/16, so C's copy starts early and the later
+  // products stay large (bf16 4096^3 -> fp32 on GB300: 772 us in one panel,
+  // 625 us in six even panels, 605-610 us in 256, 256, 512, 1024, 1024, 1024
+  // rows; the copy engines move about 200 GB/s each way, 335 GB/s both ways).
+  // An explicit panel count gives even panels.
   const int64_t c_bytes = M * N * eo;
-  int64_t want = panels;
-  if (!want)
-    want = c_bytes < (int64_t(6) << 20) ? 1 : std::min<int64_t>(6, std::max<int64_t>(2, c_bytes / (int64_t(12) << 20)));
-  want = std::min<int64_t>(want, M);
-  int64_t rows_per = (M + want - 1) / want;
-  if (!panels) rows_per = (rows_per + 127) / 128 * 128;
-  const int64_t npanels = (M + rows_per - 1) / rows_per;
+  std::vector<int64_t> panel_rows;
+  if (panels) {
+    const int64_t want = std::min<int64_t>(panels, M), per = (M + want - 1) / want;
+    for (int64_t r0 = 0; r0 < M; r0 += per) panel_rows.push_back(std::min(per, M - r0));
+  } else if (c_bytes < (int64_t(6) << 20)) {
+    panel_rows.push_back(M);
+  } else {
+    const int64_t u = std::max<int64_t>(128, M / 16 / 128 * 128);
+    int64_t r0 = 0;
+    for (int i = 0; r0 < M; ++i) {
+      const int64_t r = std::min(M - r0, i < 2 ? u : (i == 2 ? 2 * u : 4 * u));
+      panel_rows.push_back(r);
+      r0 += r;
+    }
+  }
+  const int64_t npanels = static_cast<int64_t>(panel_rows.size());
 
   tgemm::DeviceInfo* dev = nullptr;
   int st = tgemm::device_info(&dev);
@@ -1278,16 +1291,16 @@ int tgemm_gemm_host(int64_t M, int64_t N, int64_t K, const void* A_host, int64_t
     if ((e = tgemm::copy_rows(dB, N * ei, B_host, ldb * ei, N * ei, K, cudaMemcpyHostToDevice, in)) != cudaSuccess ||
         (e = cudaEventRecord(ev_b, in)) != cudaSuccess || (e = cudaStreamWaitEvent(s, ev_b, 0)) != cudaSuccess)
       return tgemm::cuda_fail(e, "copy of B");
-    for (int64_t p = 0; p < npanels; ++p) {
-      const int64_t r0 = p * rows_per, rows = std::min(rows_per, M - r0);
+    for (int64_t p = 0, r0 = 0; p < npanels; r0 += panel_rows[p], ++p) {
+      const int64_t rows = panel_rows[p];
       if ((e = tgemm::copy_rows(da + r0 * K * ei, K * ei, ah + r0 * lda * ei, lda * ei, K * ei, rows,
                                 cudaMemcpyHostToDevice, in)) != cudaSuccess ||
           (e = cudaEventRecord(ev_a[p], in)) != cudaSuccess)
         return tgemm::cuda_fail(e, "copy of A");
     }
   }
-  for (int64_t p = 0; p < npanels; ++p) {
-    const int64_t r0 = p * rows_per, rows = std::min(rows_per, M - r0);
+  for (int64_t p = 0, r0 = 0; p < npanels; r0 += panel_rows[p], ++p) {
+    const int64_t rows = panel_rows[p];
     if (K > 0 && (e = cudaStreamWaitEvent(s, ev_a[p], 0)) != cudaSuccess) return tgemm::cuda_fail(e, "stream ordering");
     st = tgemm_gemm(rows, N, K, K > 0 ? da + r0 * K * ei : nullptr, K > 0 ? K : 1, dB, N, dc + r0 * N * eo, N, dtype,
                     stream);
