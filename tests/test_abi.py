@@ -293,7 +293,9 @@ def test_swapped_pair_planning(tg):
     st, p = plan(tg, 3072, 4096, 4096, dtype=2, sms=152)
     assert p.tuned == 0 and p.group_m == 4   # operands within half of L2
     st, p = plan(tg, 4096, 4096, 4096, dtype=2, sms=152)
-    assert p.tuned == 1 and p.group_m == 2    # the table's measured raster group
+    assert p.tuned == 1 and p.group_m == 4    # the table's measured raster group
+    st, p = plan(tg, 4096, 4096, 4096, dtype=3, sms=152)
+    assert p.tuned == 1 and p.group_m == 2 and p.tile_m == 224
     for tm in (128, 192, 224, 256):
         st, p = plan(tg, 300, 520, 200, dtype=2, swap_ab=2, tile_m=tm)
         assert st == tg.OK and p.swap_ab == 1 and p.tile_m == tm and p.tile_n == 256

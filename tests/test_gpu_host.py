@@ -93,3 +93,10 @@ def test_k_zero_from_host():
 def test_reused_device_buffers_see_each_calls_inputs():
     bufs = run_host(700, 400, 300, wl.BF16, seed=94, panels=2)
     run_host(700, 400, 300, wl.BF16, seed=95, panels=4, dev_bufs=bufs)
+
+
+def test_graduated_panels_from_host():
+    """C of 8 MB (fp32 2048 x 1024): the automatic schedule takes graduated
+    panels of 128, 128, 256, 512, 512 and 512 rows; the product is checked
+    against the oracle like every other schedule."""
+    run_host(2048, 1024, 512, wl.BF16_F32OUT, seed=96)
