@@ -417,6 +417,9 @@ TGEMM_API int tgemm_transpose(int64_t rows, int64_t cols,
  * panels: row panels of A and C (0 = chosen by the library: one when C is
  *   below 6 MB, else graduated whole numbers of 128-row tiles, small first so
  *   that C's copy back starts early; n > 0 = n even panels; 1 = no overlap).
+ *   With fp32 output, several panels and K >= 256, the first panel's product
+ *   runs in two K halves, the first while B's second half is being copied
+ *   (the partial sum is rounded once to fp32 before the second half is added).
  * stream: everything the call does follows the work already enqueued on
  *   `stream`, and later work on `stream` follows all of it, including the
  *   copy of C to the host.  The call returns once the work is enqueued:

@@ -100,3 +100,13 @@ def test_graduated_panels_from_host():
     panels of 128, 128, 256, 512, 512 and 512 rows; the product is checked
     against the oracle like every other schedule."""
     run_host(2048, 1024, 512, wl.BF16_F32OUT, seed=96)
+
+
+@pytest.mark.parametrize("dtype,panels", [(wl.F16_F32OUT, 3), (wl.BF16_F32OUT, 0), (wl.BF16, 3)],
+                         ids=["f16_f32out_3", "bf16_f32out_auto", "bf16_3"])
+def test_first_panel_in_two_k_halves(dtype, panels):
+    """fp32 output with several panels and K >= 256: the first panel's product
+    runs in two K halves (the second added onto the first as B's second half
+    arrives); with padded host rows, a K that is not a multiple of the 64-deep
+    split point's step, and a 16-bit output for contrast (one pass)."""
+    run_host(1300, 1300, 700, dtype, seed=97, lda=712, ldb=1308, ldc=1303, panels=panels)  # fp32 C: 6.8 MB

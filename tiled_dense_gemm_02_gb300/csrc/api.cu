@@ -1268,12 +1268,21 @@ int tgemm_gemm_host(int64_t M, int64_t N, int64_t K, const void* A_host, int64_t
   cudaStream_t in = nullptr, out = nullptr;
   if ((st = tgemm::copy_streams(&in, &out)) != TGEMM_OK) return st;
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // Early first panel (fp32 output, several panels, K >= 256): the first
+  // panel's product runs in two K halves, the first while the second half of
+  // B is still being copied (B's rows are contiguous, so its first K1 rows
+  // arrive first), the second added onto it (beta = 1) once B is complete.
+  // The copy of C back, the longest leg, then starts sooner.  The partial sum
+  // is rounded once to fp32, well inside the product's error bound; 16-bit
+  // outputs keep the single pass.
+  const bool split_first = K >= 256 && npanels > 1 && eo == 4 && dtype != TGEMM_F32;
+  const int64_t k1 = split_first ? K / 2 / 64 * 64 : K;
   tgemm::CallEvents evs;
-  cudaEvent_t ev_start, ev_b, ev_done;
+  cudaEvent_t ev_start, ev_b, ev_b1, ev_done;
   std::vector<cudaEvent_t> ev_a(npanels), ev_c(npanels);
   cudaError_t e;
   if ((e = evs.make(&ev_start)) != cudaSuccess || (e = evs.make(&ev_b)) != cudaSuccess ||
-      (e = evs.make(&ev_done)) != cudaSuccess)
+      (e = evs.make(&ev_b1)) != cudaSuccess || (e = evs.make(&ev_done)) != cudaSuccess)
     return tgemm::cuda_fail(e, "cudaEventCreate");
   for (int64_t p = 0; p < npanels; ++p)
     if ((e = evs.make(&ev_a[p])) != cudaSuccess || (e = evs.make(&ev_c[p])) != cudaSuccess)
@@ -1288,10 +1297,26 @@ int tgemm_gemm_host(int64_t M, int64_t N, int64_t K, const void* A_host, int64_t
   char* da = static_cast<char*>(dA);
   char* dc = static_cast<char*>(dC);
   if (K > 0) {
-    if ((e = tgemm::copy_rows(dB, N * ei, B_host, ldb * ei, N * ei, K, cudaMemcpyHostToDevice, in)) != cudaSuccess ||
-        (e = cudaEventRecord(ev_b, in)) != cudaSuccess || (e = cudaStreamWaitEvent(s, ev_b, 0)) != cudaSuccess)
+    const char* bh = static_cast<const char*>(B_host);
+    char* db = static_cast<char*>(dB);
+    if (split_first) {
+      // the first panel of A, then B's first K1 rows, then the rest of B
+      if ((e = tgemm::copy_rows(da, K * ei, ah, lda * ei, K * ei, panel_rows[0], cudaMemcpyHostToDevice, in)) !=
+              cudaSuccess ||
+          (e = cudaEventRecord(ev_a[0], in)) != cudaSuccess ||
+          (e = tgemm::copy_rows(db, N * ei, bh, ldb * ei, N * ei, k1, cudaMemcpyHostToDevice, in)) != cudaSuccess ||
+          (e = cudaEventRecord(ev_b1, in)) != cudaSuccess)
+        return tgemm::cuda_fail(e, "copy of B");
+    }
+    if ((e = tgemm::copy_rows(db + k1 * N * ei * (split_first ? 1 : 0), N * ei,
+                              bh + k1 * ldb * ei * (split_first ? 1 : 0), ldb * ei, N * ei, split_first ? K - k1 : K,
+                              cudaMemcpyHostToDevice, in)) != cudaSuccess ||
+        (e = cudaEventRecord(ev_b, in)) != cudaSuccess)
       return tgemm::cuda_fail(e, "copy of B");
-    for (int64_t p = 0, r0 = 0; p < npanels; r0 += panel_rows[p], ++p) {
+    if (!split_first && (e = cudaStreamWaitEvent(s, ev_b, 0)) != cudaSuccess)
+      return tgemm::cuda_fail(e, "stream ordering");
+    for (int64_t p = split_first ? 1 : 0, r0 = split_first ? panel_rows[0] : 0; p < npanels;
+         r0 += panel_rows[p], ++p) {
       const int64_t rows = panel_rows[p];
       if ((e = tgemm::copy_rows(da + r0 * K * ei, K * ei, ah + r0 * lda * ei, lda * ei, K * ei, rows,
                                 cudaMemcpyHostToDevice, in)) != cudaSuccess ||
@@ -1302,8 +1327,23 @@ int tgemm_gemm_host(int64_t M, int64_t N, int64_t K, const void* A_host, int64_t
   for (int64_t p = 0, r0 = 0; p < npanels; r0 += panel_rows[p], ++p) {
     const int64_t rows = panel_rows[p];
     if (K > 0 && (e = cudaStreamWaitEvent(s, ev_a[p], 0)) != cudaSuccess) return tgemm::cuda_fail(e, "stream ordering");
-    st = tgemm_gemm(rows, N, K, K > 0 ? da + r0 * K * ei : nullptr, K > 0 ? K : 1, dB, N, dc + r0 * N * eo, N, dtype,
-                    stream);
+    if (split_first && p == 0) {
+      // K1 rows of B have arrived: the first half of the first panel's product
+      if ((e = cudaStreamWaitEvent(s, ev_b1, 0)) != cudaSuccess) return tgemm::cuda_fail(e, "stream ordering");
+      st = tgemm_gemm(rows, N, k1, da, K, dB, N, dc, N, dtype, stream);
+      if (st != TGEMM_OK) return st;
+      // all of B: the second half, added onto the first
+      if ((e = cudaStreamWaitEvent(s, ev_b, 0)) != cudaSuccess) return tgemm::cuda_fail(e, "stream ordering");
+      tgemm_epilogue acc_onto;
+      std::memset(&acc_onto, 0, sizeof acc_onto);
+      acc_onto.alpha = 1.0f;
+      acc_onto.beta = 1.0f;
+      st = tgemm_gemm_epilogue(rows, N, K - k1, da + k1 * ei, K, static_cast<char*>(dB) + k1 * N * ei, N, dc, N, dtype,
+                               &acc_onto, nullptr, nullptr, 0, stream);
+    } else {
+      st = tgemm_gemm(rows, N, K, K > 0 ? da + r0 * K * ei : nullptr, K > 0 ? K : 1, dB, N, dc + r0 * N * eo, N,
+                      dtype, stream);
+    }
     if (st != TGEMM_OK) return st;
     if ((e = cudaEventRecord(ev_c[p], s)) != cudaSuccess || (e = cudaStreamWaitEvent(out, ev_c[p], 0)) != cudaSuccess ||
         (e = tgemm::copy_rows(ch + r0 * ldc * eo, ldc * eo, dc + r0 * N * eo, N * eo, N * eo, rows,
