@@ -76,6 +76,9 @@ def parse_args():
     p.add_argument("--no-configs", action="store_true",
                    help="skip the other workloads, the FP32 probe and the host-dispatch measurement")
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU work of the oracle sample")
+    p.add_argument("--workspace", action="store_true",
+                   help="time the call through tgemm_gemm_ws with a workspace of tgemm_workspace_size bytes "
+                        "(the library may then repack unaligned operands)")
     p.add_argument("--epilogue", default="none", choices=sorted(EPILOGUES),
                    help="fused epilogue C = act(alpha A.B + beta C + bias) timed with the product")
     return p.parse_args()
@@ -517,7 +520,14 @@ def run_ours(args, w: wl.Workload):
     stream = torch.cuda.current_stream(dev)
     sptr = stream.cuda_stream
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    st, plan = tg.plan(w.M, w.N, w.K, a.data_ptr(), w.K, b.data_ptr(), w.N, c.data_ptr(), w.N, w.dtype, None, sms)
+    ws, ws_bytes = None, 0
+    if args.workspace:
+        st, ws_bytes = tg.workspace_size(w.M, w.N, w.K, a.data_ptr(), w.K, b.data_ptr(), w.N, c.data_ptr(), w.N,
+                                         w.dtype, None)
+        assert st == tg.OK, tg.status_string(st)
+        ws = torch.zeros(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
+    st, plan = tg.plan(w.M, w.N, w.K, a.data_ptr(), w.K, b.data_ptr(), w.N, c.data_ptr(), w.N, w.dtype, None, sms,
+                       workspace_bytes=ws_bytes)
     assert st == tg.OK, tg.status_string(st)
 
     epi = EPILOGUES[args.epilogue]
@@ -528,11 +538,11 @@ def run_ours(args, w: wl.Workload):
                                                      activation=epi[3])
 
     def call():
-        if epi_struct is None:
+        if epi_struct is None and ws is None:
             s = tg.gemm(w.M, w.N, w.K, a.data_ptr(), w.K, b.data_ptr(), w.N, c.data_ptr(), w.N, w.dtype, sptr)
         else:
             s = tg.gemm_epilogue(w.M, w.N, w.K, a.data_ptr(), w.K, b.data_ptr(), w.N, c.data_ptr(), w.N, w.dtype,
-                                 epi_struct, None, 0, 0, sptr)
+                                 epi_struct, None, ws.data_ptr() if ws is not None else 0, ws_bytes, sptr)
         if s != tg.OK:
             raise RuntimeError(tg.status_string(s))
 
@@ -692,7 +702,8 @@ def run_ours(args, w: wl.Workload):
         "vs_baseline": None, "dtype": fin, "data": "synthetic",
         "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "in": fin, "out": fout, "accumulate": "f32",
                    "l2": "flushed before every timed step (256 MiB write)", "parallelism": f"replicas{world}",
-                   "kernel": plan.as_dict(), "sms": sms, "epilogue": args.epilogue, "step_ms_min": min(step_ms),
+                   "kernel": plan.as_dict(), "sms": sms, "epilogue": args.epilogue, "workspace_bytes": ws_bytes,
+                   "step_ms_min": min(step_ms),
                    "step_ms_median": statistics.median(step_ms), "wall_s": wall,
                    "host_dispatch_us": dispatch[w.name]["us_per_call"] if dispatch and w.name in dispatch else None},
         "roofline": roofline,
