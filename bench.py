@@ -76,6 +76,8 @@ def parse_args():
     p.add_argument("--no-configs", action="store_true",
                    help="skip the other workloads, the FP32 probe and the host-dispatch measurement")
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU work of the oracle sample")
+    p.add_argument("--cublas", action="store_true",
+                   help="also time torch.matmul (cuBLAS) on the same inputs, as context (outside the timed region)")
     p.add_argument("--workspace", action="store_true",
                    help="time the call through tgemm_gemm_ws with a workspace of tgemm_workspace_size bytes "
                         "(the library may then repack unaligned operands)")
@@ -378,12 +380,14 @@ def host_dispatch(tg, w: wl.Workload, dev, calls: int = 200):
             "map_hits": after["map_hits"] - before["map_hits"], "calls": calls, "workload": w.name}
 
 
-def time_workload(tg, w: wl.Workload, dev, flush, steps: int, peaks: dict, fp32_peak=None, options=None):
+def time_workload(tg, w: wl.Workload, dev, flush, steps: int, peaks: dict, fp32_peak=None, options=None,
+                  cublas: bool = False):
     """One workload timed like the headline (L2 flushed before each step,
     CUDA events around the call on its stream), checked against the oracle,
     with its roofline: min(peak FLOP/s, compulsory AI x measured HBM GB/s).
     With `options` the call is tgemm_gemm_ws with those options and a
-    workspace of tgemm_workspace_size bytes (allocated before timing)."""
+    workspace of tgemm_workspace_size bytes (allocated before timing).  With
+    `cublas`, torch.matmul on the same inputs is timed after it as context."""
     import torch
     fin, fout = wl.IN_FORMAT[w.dtype], wl.OUT_FORMAT[w.dtype]
     A, B = wl.make_inputs(w)
@@ -449,7 +453,42 @@ def time_workload(tg, w: wl.Workload, dev, flush, steps: int, peaks: dict, fp32_
                                 "sk_iters", "workspace_bytes", "packed")},
             "call": "tgemm_gemm" if options is None else f"tgemm_gemm_ws {dict(options)}",
             "launches_per_step": kernel_launches_per_call(tg, plan, False)}
+    if cublas:
+        entry["context_cublas"] = cublas_context(a, b, w, dev, flush, steps)
     return entry, (A, B, got)
+
+
+def cublas_context(a_bits, b_bits, w: wl.Workload, dev, flush, steps: int) -> dict:
+    """torch.matmul (cuBLAS) on the same device inputs, timed like the
+    workload (L2 flush, then CUDA events around the call on the stream):
+    context beside the library's number, never part of it.  cuBLAS writes the
+    input type, so for bf16 -> fp32 workloads its output is bf16; fp32 runs
+    with TF32 off."""
+    import torch
+    tdt = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[wl.IN_FORMAT[w.dtype]]
+    at, bt = a_bits.view(tdt), b_bits.view(tdt)
+    prev = torch.backends.cuda.matmul.allow_tf32
+    torch.backends.cuda.matmul.allow_tf32 = False
+    try:
+        stream = torch.cuda.current_stream(dev)
+        for _ in range(3):
+            flush.fill_(1)
+            torch.matmul(at, bt)
+        torch.cuda.synchronize(dev)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        for i, (s_, e_) in enumerate(ev):
+            flush.fill_(i)
+            s_.record(stream)
+            torch.matmul(at, bt)
+            e_.record(stream)
+        torch.cuda.synchronize(dev)
+    finally:
+        torch.backends.cuda.matmul.allow_tf32 = prev
+    ms = [s_.elapsed_time(e_) for s_, e_ in ev]
+    mean = sum(ms) / len(ms)
+    return {"what": "torch.matmul (cuBLAS) on the same inputs, timed the same way; context, not used by the library",
+            "out": str(tdt).replace("torch.", ""), "ms_mean": mean, "ms_median": statistics.median(ms),
+            "tflops": w.flops / (mean / 1e3) / 1e12, "steps": steps}
 
 
 def check_output(w: wl.Workload, A, B, got) -> dict:
@@ -608,6 +647,12 @@ def run_ours(args, w: wl.Workload):
     if world > 1:
         e2e_ms = max_over_ranks(e2e_ms, dev)
     e2e_value = world * w.flops / (e2e_ms / 1e3) / 1e12
+    headline_cublas = None
+    if world == 1 and args.cublas and epi is None:
+        try:
+            headline_cublas = cublas_context(a, b, w, dev, flush, min(args.steps, 20))
+        except Exception as exc:  # context only: the line is printed whatever happens here
+            headline_cublas = {"error": repr(exc)}
 
     if rank != 0:
         if world > 1:
@@ -658,7 +703,7 @@ def run_ours(args, w: wl.Workload):
                 continue
             try:
                 configs[name], outputs[name] = time_workload(tg, wl.BY_NAME[name], dev, flush, steps, peaks,
-                                                             fp32_peak)
+                                                             fp32_peak, cublas=args.cublas)
             except Exception as exc:
                 errors[name] = repr(exc)
         # the ragged shape again through tgemm_gemm_ws: with a workspace the
@@ -708,6 +753,7 @@ def run_ours(args, w: wl.Workload):
                    "host_dispatch_us": dispatch[w.name]["us_per_call"] if dispatch and w.name in dispatch else None},
         "roofline": roofline,
         "check": check,
+        "context_cublas": headline_cublas,
         "configs": configs,
         "host_dispatch": dispatch,
         "cpu_baseline": cpu,
