@@ -35,11 +35,14 @@ namespace {
 
 // One 32 x 32 block of C (rows m0.., columns n0..) from the lanes' values:
 // lane l holds column n0 + l, v[i] is row m0 + i (the fused epilogue, when on,
-// is applied in place first).
+// is applied in place first).  `throttle`: wait until this warp's previous
+// bulk store has read its buffer before staging the block (one store in flight
+// per warp) rather than the one before it (two in flight).
 template <bool EPI>
 __device__ __forceinline__ void store_block_t(uint32_t (&v)[32], int m0, int n0, int zc, int64_t c_off,
                                               bool tma_store, const TcArgs& args, const CUtensorMap* mapC,
-                                              uint8_t* stage_base, int& sbuf, int lane, float bias_v) {
+                                              uint8_t* stage_base, int& sbuf, int lane, float bias_v,
+                                              bool throttle) {
   const int out_fmt = args.out_fmt;
   if constexpr (EPI) {
     // lane = column (its bias is bias_v).  Each step is one uniform branch
@@ -70,7 +73,12 @@ __device__ __forceinline__ void store_block_t(uint32_t (&v)[32], int m0, int n0,
   }
   if (tma_store) {
     uint8_t* buf = stage_base + sbuf * 4096;
-    if (lane == 0) ptx::bulk_wait_group_read<1>();
+    if (lane == 0) {
+      if (throttle)
+        ptx::bulk_wait_group_read<0>();
+      else
+        ptx::bulk_wait_group_read<1>();
+    }
     __syncwarp();
     if (out_fmt == OUT_F32) {
 #pragma unroll
@@ -360,6 +368,12 @@ __global__ void __launch_bounds__(32 * (2 + kEpiWarps), 1)
         if (args.epi.bias && n0 + lane < args.N) bias_v = args.epi.bias[n0 + lane];
       }
       const int nblk = min(TM / 32, (args.M - mb * TM + 31) / 32);  // blocks of rows inside C
+      // The stores of C pass through the SM's bulk-copy path, which the next
+      // tile's operand loads need at about the rate it can deliver.  While a
+      // later tile of this pair is being loaded, fp32 blocks go out one store
+      // per warp at a time (bf16 4096^3 -> fp32: 86.1 -> 84.5 us); the pair's
+      // last tile, with nothing left to load, keeps two in flight.
+      const bool throttle = args.out_fmt == OUT_F32 && t + npairs < args.num_tiles;
       if (staged_prior && n0 < args.N) {
         // the first block's prior C, loaded while the tile's MMAs run (after
         // the previous tile's stores have read the buffers)
@@ -405,7 +419,8 @@ __global__ void __launch_bounds__(32 * (2 + kEpiWarps), 1)
           } else {
             ptx::tmem_ld_32x32b_x32(tbase + c * 32, v);
             ptx::tmem_wait_ld();
-            store_block_t<EPI>(v, m0, n0, b, c_off, tma_store, args, &mapC, stage_base, sbuf, lane, bias_v);
+            store_block_t<EPI>(v, m0, n0, b, c_off, tma_store, args, &mapC, stage_base, sbuf, lane, bias_v,
+                               throttle);
           }
         }
         if (!ok) break;
