@@ -110,3 +110,51 @@ def test_first_panel_in_two_k_halves(dtype, panels):
     arrives); with padded host rows, a K that is not a multiple of the 64-deep
     split point's step, and a 16-bit output for contrast (one pass)."""
     run_host(1300, 1300, 700, dtype, seed=97, lda=712, ldb=1308, ldc=1303, panels=panels)  # fp32 C: 6.8 MB
+
+
+def test_host_calls_from_several_threads():
+    """Three host threads, each on its own stream with its own buffers, call
+    tgemm_gemm_host three times in a row (fp32 output in three panels, so the
+    first panel runs in two K halves).  The calls share the library's copy
+    streams and its pool of events; every product is checked against the
+    oracle and every padding element of C's host rows keeps its canary."""
+    import threading
+    lib = H.tg()
+    dev = torch.device("cuda:0")
+    M, N, K, dtype = 700, 900, 512, wl.BF16_F32OUT
+    fin, fout = wl.IN_FORMAT[dtype], wl.OUT_FORMAT[dtype]
+    ldc = N + 4
+    errors = []
+
+    def worker(w):
+        try:
+            torch.cuda.set_device(0)
+            stream = torch.cuda.Stream(device=dev)
+            dA = torch.empty(M * K * 2, dtype=torch.uint8, device=dev)
+            dB = torch.empty(K * N * 2, dtype=torch.uint8, device=dev)
+            dC = torch.empty(M * N * 4, dtype=torch.uint8, device=dev)
+            for call in range(3):
+                A, B = wl.make_inputs(wl.Workload("host_threads", M, N, K, dtype, "uniform", 200 + 10 * w + call))
+                a_h, a_ptr = host_buffer(A, True)
+                b_h, b_ptr = host_buffer(B, True)
+                c_h, c_ptr = host_buffer(np.full((M, ldc), H.CANARY[fout], dtype=H.NP_BITS[fout]), True)
+                st = lib.gemm_host(M, N, K, a_ptr, K, b_ptr, N, c_ptr, ldc, dtype, dA.data_ptr(), dB.data_ptr(),
+                                   dC.data_ptr(), 3, stream.cuda_stream)
+                assert st == lib.OK, lib.status_string(st)
+                stream.synchronize()
+                assert lib.device_status(stream.cuda_stream) == lib.OK
+                raw = c_h.numpy().view(H.NP_BITS[fout]).reshape(M, ldc)
+                assert np.all(raw[:, N:] == H.CANARY[fout]), "a padding element of C's host rows was written"
+                got = wl.decode(np.ascontiguousarray(raw[:, :N]), fout)
+                D, S = oracle.gemm(np.ascontiguousarray(A), np.ascontiguousarray(B), fin, M, N, K)
+                ok, ratio, where = tolerance.check(got, D, S, fin, fout)
+                assert ok, f"thread {w} call {call}: error/bound {ratio:.3g} at {where}"
+        except Exception as exc:  # reported by the main thread
+            errors.append(repr(exc))
+
+    threads = [threading.Thread(target=worker, args=(w,)) for w in range(3)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors

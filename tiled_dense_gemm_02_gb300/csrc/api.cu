@@ -132,14 +132,37 @@ cudaError_t copy_rows(void* dst, int64_t dpitch, const void* src, int64_t spitch
   return cudaMemcpy2DAsync(dst, dpitch, src, spitch, width, rows, kind, s);
 }
 
-// Events of one tgemm_gemm_host call, released when the call returns (a
-// recorded event that has not completed yet is released once it completes).
+// Events of tgemm_gemm_host calls come from a per-device pool (guarded by
+// g_mutex): a call takes the events it needs and hands them back when it
+// returns, whether or not the work they mark has completed.  Recording an
+// event again only changes what later waits and queries see; a wait already
+// enqueued stays bound to the record it was enqueued against.  So calls
+// create events only while the pool grows, and never destroy them.
+struct EventPool {
+  std::vector<cudaEvent_t> free;
+};
+EventPool g_event_pools[64];
+
 struct CallEvents {
+  int dev = 0;
   std::vector<cudaEvent_t> ev;
   ~CallEvents() {
-    for (cudaEvent_t e : ev) cudaEventDestroy(e);
+    if (ev.empty()) return;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    std::vector<cudaEvent_t>& f = g_event_pools[dev].free;
+    f.insert(f.end(), ev.begin(), ev.end());
   }
   cudaError_t make(cudaEvent_t* out) {
+    {
+      std::lock_guard<std::mutex> lock(g_mutex);
+      std::vector<cudaEvent_t>& f = g_event_pools[dev].free;
+      if (!f.empty()) {
+        *out = f.back();
+        f.pop_back();
+        ev.push_back(*out);
+        return cudaSuccess;
+      }
+    }
     const cudaError_t e = cudaEventCreateWithFlags(out, cudaEventDisableTiming);
     if (e == cudaSuccess) ev.push_back(*out);
     return e;
@@ -1278,9 +1301,11 @@ int tgemm_gemm_host(int64_t M, int64_t N, int64_t K, const void* A_host, int64_t
   const bool split_first = K >= 256 && npanels > 1 && eo == 4 && dtype != TGEMM_F32;
   const int64_t k1 = split_first ? K / 2 / 64 * 64 : K;
   tgemm::CallEvents evs;
+  cudaError_t e = cudaGetDevice(&evs.dev);
+  if (e != cudaSuccess) return tgemm::cuda_fail(e, "cudaGetDevice");
+  if (evs.dev < 0 || evs.dev >= 64) return tgemm::cuda_fail(cudaErrorInvalidDevice, "device ordinal");
   cudaEvent_t ev_start, ev_b, ev_b1, ev_done;
   std::vector<cudaEvent_t> ev_a(npanels), ev_c(npanels);
-  cudaError_t e;
   if ((e = evs.make(&ev_start)) != cudaSuccess || (e = evs.make(&ev_b)) != cudaSuccess ||
       (e = evs.make(&ev_b1)) != cudaSuccess || (e = evs.make(&ev_done)) != cudaSuccess)
     return tgemm::cuda_fail(e, "cudaEventCreate");
