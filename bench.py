@@ -76,6 +76,8 @@ def parse_args():
     p.add_argument("--no-configs", action="store_true",
                    help="skip the other workloads, the FP32 probe and the host-dispatch measurement")
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU work of the oracle sample")
+    p.add_argument("--options", type=json.loads, default=None,
+                   help="tgemm_options fields for the timed call, as a JSON object (e.g. '{\"group_m\": 32}')")
     p.add_argument("--cublas", action="store_true",
                    help="also time torch.matmul (cuBLAS) on the same inputs, as context (outside the timed region)")
     p.add_argument("--workspace", action="store_true",
@@ -560,12 +562,13 @@ def run_ours(args, w: wl.Workload):
     sptr = stream.cuda_stream
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     ws, ws_bytes = None, 0
+    opts = args.options
     if args.workspace:
         st, ws_bytes = tg.workspace_size(w.M, w.N, w.K, a.data_ptr(), w.K, b.data_ptr(), w.N, c.data_ptr(), w.N,
-                                         w.dtype, None)
+                                         w.dtype, opts)
         assert st == tg.OK, tg.status_string(st)
         ws = torch.zeros(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
-    st, plan = tg.plan(w.M, w.N, w.K, a.data_ptr(), w.K, b.data_ptr(), w.N, c.data_ptr(), w.N, w.dtype, None, sms,
+    st, plan = tg.plan(w.M, w.N, w.K, a.data_ptr(), w.K, b.data_ptr(), w.N, c.data_ptr(), w.N, w.dtype, opts, sms,
                        workspace_bytes=ws_bytes)
     assert st == tg.OK, tg.status_string(st)
 
@@ -577,11 +580,13 @@ def run_ours(args, w: wl.Workload):
                                                      activation=epi[3])
 
     def call():
-        if epi_struct is None and ws is None:
+        if epi_struct is None and ws is None and opts is None:
             s = tg.gemm(w.M, w.N, w.K, a.data_ptr(), w.K, b.data_ptr(), w.N, c.data_ptr(), w.N, w.dtype, sptr)
+        elif epi_struct is None and ws is None:
+            s = tg.gemm_ex(w.M, w.N, w.K, a.data_ptr(), w.K, b.data_ptr(), w.N, c.data_ptr(), w.N, w.dtype, opts, sptr)
         else:
             s = tg.gemm_epilogue(w.M, w.N, w.K, a.data_ptr(), w.K, b.data_ptr(), w.N, c.data_ptr(), w.N, w.dtype,
-                                 epi_struct, None, ws.data_ptr() if ws is not None else 0, ws_bytes, sptr)
+                                 epi_struct, opts, ws.data_ptr() if ws is not None else 0, ws_bytes, sptr)
         if s != tg.OK:
             raise RuntimeError(tg.status_string(s))
 
@@ -748,6 +753,7 @@ def run_ours(args, w: wl.Workload):
         "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "in": fin, "out": fout, "accumulate": "f32",
                    "l2": "flushed before every timed step (256 MiB write)", "parallelism": f"replicas{world}",
                    "kernel": plan.as_dict(), "sms": sms, "epilogue": args.epilogue, "workspace_bytes": ws_bytes,
+                   "options": opts,
                    "step_ms_min": min(step_ms),
                    "step_ms_median": statistics.median(step_ms), "wall_s": wall,
                    "host_dispatch_us": dispatch[w.name]["us_per_call"] if dispatch and w.name in dispatch else None},
