@@ -425,7 +425,8 @@ TGEMM_API int tgemm_transpose(int64_t rows, int64_t cols,
  *   copy of C to the host.  The call returns once the work is enqueued:
  *   synchronise `stream` before reading C_host.  The copies run on two
  *   streams per device that the library creates on first use and keeps;
- *   ordering with `stream` is by events, created and released per call.
+ *   ordering with `stream` is by events, taken from a per-device pool that
+ *   the library keeps (created as the pool grows, never destroyed).
  * Errors: as tgemm_gemm for the product (M, N, K, dtype, leading dimensions);
  *   TGEMM_ERR_INVALID_VALUE for a null buffer with a nonzero extent or
  *   panels < 0, TGEMM_ERR_MISALIGNED for a pointer not aligned to its element
