@@ -70,7 +70,8 @@ def parse_args():
     p.add_argument("--gpus", type=int, default=1)
     p.add_argument("--steps", type=int, default=50)
     p.add_argument("--warmup", type=int, default=5)
-    p.add_argument("--workload", default=wl.HEADLINE.name, choices=sorted(wl.BY_NAME) + sorted(wl.TRANSPOSE_BY_NAME))
+    p.add_argument("--workload", default=wl.HEADLINE.name,
+                   choices=sorted(wl.BY_NAME) + sorted(wl.TRANSPOSE_BY_NAME) + sorted(wl.BATCH_BY_NAME))
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-configs", action="store_true",
@@ -910,8 +911,156 @@ def run_transpose(args, w):
         torch.distributed.destroy_process_group()
 
 
+def run_batched(args, w):
+    """A strided batch in one tgemm_gemm_batched call: TFLOP/s of the whole
+    batch, timed like the product workloads (L2 flushed before each step, CUDA
+    events around the call), with three of its products checked in full
+    against the oracle after the timed region."""
+    import torch
+    world, rank, local = dist_env()
+    if world > 1:
+        init_replicas(local, "nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    _build_library()
+    import tiled_dense_gemm_02_gb300 as tg
+    fin, fout = wl.IN_FORMAT[w.dtype], wl.OUT_FORMAT[w.dtype]
+    A, B = wl.make_batch_inputs(w)
+    tdt = {"f32": torch.int32, "f16": torch.int16, "bf16": torch.int16}
+    npv = {"f32": np.int32, "f16": np.int16, "bf16": np.int16}
+    a_host = torch.from_numpy(A.view(npv[fin])).pin_memory()
+    b_host = torch.from_numpy(B.view(npv[fin])).pin_memory()
+    c_host = torch.empty((w.batch * w.M, w.N), dtype=tdt[fout]).pin_memory()
+    a, b = a_host.to(dev), b_host.to(dev)
+    c = torch.empty((w.batch * w.M, w.N), dtype=tdt[fout], device=dev)
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sptr = stream.cuda_stream
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    sa, sb, sc = w.M * w.K, w.K * w.N, w.M * w.N
+    st, plan, launches = tg.plan_batched(w.batch, w.M, w.N, w.K, a.data_ptr(), w.K, sa, b.data_ptr(), w.N, sb,
+                                         c.data_ptr(), w.N, sc, w.dtype, args.options, sms)
+    assert st == tg.OK, tg.status_string(st)
+
+    def call():
+        s_ = tg.gemm_batched(w.batch, w.M, w.N, w.K, a.data_ptr(), w.K, sa, b.data_ptr(), w.N, sb, c.data_ptr(), w.N,
+                             sc, w.dtype, None, args.options, sptr)
+        if s_ != tg.OK:
+            raise RuntimeError(tg.status_string(s_))
+
+    for _ in range(max(args.warmup, 3)):
+        flush.fill_(1)
+        call()
+    torch.cuda.synchronize(dev)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    sampler.start()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    for i in range(args.steps):
+        flush.fill_(i)
+        starts[i].record(stream)
+        call()
+        ends[i].record(stream)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop()
+    assert tg.device_status(sptr) == tg.OK
+    step_ms = [s_.elapsed_time(e_) for s_, e_ in zip(starts, ends)]
+    total_ms = sum(step_ms)
+    if world > 1:
+        total_ms = max_over_ranks(total_ms, dev)
+    ms = total_ms / args.steps
+    value = world * w.flops * args.steps / (total_ms / 1e3) / 1e12
+    got = c.cpu().numpy().view(np.uint32 if fout == "f32" else np.uint16).copy()
+    # end to end: inputs in from pinned host memory, the batch, C back
+    e2e = []
+    for i in range(5):
+        s_, e_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s_.record(stream)
+        a.copy_(a_host, non_blocking=True)
+        b.copy_(b_host, non_blocking=True)
+        call()
+        c_host.copy_(c, non_blocking=True)
+        e_.record(stream)
+        torch.cuda.synchronize(dev)
+        if i >= 2:
+            e2e.append(s_.elapsed_time(e_))
+    e2e_ms = sum(e2e) / len(e2e)
+    cublas = None
+    if args.cublas and world == 1:
+        tt = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}[fin]
+        at = a.view(tt).view(w.batch, w.M, w.K)
+        bt = b.view(tt).view(w.batch, w.K, w.N)
+        for _ in range(3):
+            flush.fill_(1)
+            torch.bmm(at, bt)
+        torch.cuda.synchronize(dev)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        for i, (s_, e_) in enumerate(ev):
+            flush.fill_(i)
+            s_.record(stream)
+            torch.bmm(at, bt)
+            e_.record(stream)
+        torch.cuda.synchronize(dev)
+        cms = sum(s_.elapsed_time(e_) for s_, e_ in ev) / len(ev)
+        cublas = {"what": "torch.bmm (cuBLAS) on the same inputs, timed the same way; context, not used by the library",
+                  "ms_mean": cms, "tflops": w.flops / (cms / 1e3) / 1e12}
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
+    # three products of the batch, every element, against the oracle
+    one = w.one()
+    worst, checked = 0.0, 0
+    for bi in (0, w.batch // 2, w.batch - 1):
+        ratio, n = full_check(one, A[bi * w.M:(bi + 1) * w.M], B[bi * w.K:(bi + 1) * w.K],
+                              got[bi * w.M:(bi + 1) * w.M])
+        worst, checked = max(worst, ratio), checked + n
+    peaks, peak_src = load_peaks()
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    achieved = w.flops / (ms / 1e3) / 1e12
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        cpu = cpu_oracle_sample(one, A[:w.M], B[:w.K], args.cpu_seconds)
+        cpu["sample"] = "one product of the batch: " + cpu["sample"]
+    line = {
+        "metric": "GEMM TFLOP/s", "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": fin, "data": "synthetic",
+        "config": {"workload": w.name, "batch": w.batch, "M": w.M, "N": w.N, "K": w.K, "in": fin, "out": fout,
+                   "l2": "flushed before every timed step (256 MiB write)", "parallelism": f"replicas{world}",
+                   "kernel": plan.as_dict(), "launches_per_call": launches, "options": args.options,
+                   "step_ms_min": min(step_ms), "step_ms_median": statistics.median(step_ms)},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                     "traffic": None, "peak_source": f"{peak_src} bf16_tflops (burst; kernel timed alone)",
+                     "algorithmic_flops_per_launch": w.flops},
+        "check": {"max_err_over_bound": worst, "elements_checked": checked,
+                  "what": "products 0, batch/2 and batch-1 of the last timed step, every element, against the oracle"},
+        "context_cublas": cublas,
+        "cpu_baseline": cpu,
+        "clocks": clocks,
+        "e2e": {"value": world * w.flops / (e2e_ms / 1e3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
+                "h2d_bytes_per_step": int(A.nbytes + B.nbytes), "d2h_bytes_per_step": int(c.numel() * c.element_size())},
+        "gpu_launches": args.steps * launches,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
 def main():
     args = parse_args()
+    if args.workload in wl.BATCH_BY_NAME:
+        if args.impl == "reference":
+            bw = wl.BATCH_BY_NAME[args.workload]
+            run_reference(args, bw.one())
+        else:
+            run_batched(args, wl.BATCH_BY_NAME[args.workload])
+        return
     if args.workload in wl.TRANSPOSE_BY_NAME:
         if args.impl == "reference":
             run_transpose_reference(args, wl.TRANSPOSE_BY_NAME[args.workload])

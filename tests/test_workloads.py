@@ -75,3 +75,18 @@ def test_workload_table():
     assert (h.M, h.N, h.K, h.dtype) == (4096, 4096, 4096, wl.BF16_F32OUT)
     assert h.flops == 2 * 4096 ** 3
     assert h.compulsory_bytes == (2 * 4096 * 4096) * 2 + 4096 * 4096 * 4
+
+
+def test_batch_workload_inputs():
+    """The batch benchmark's inputs: matrix 0 of the batch is the one-product
+    workload's input (one seeded stream per operand), every matrix is distinct
+    and every value is a bf16 value in [-1, 1] (rounding can reach 1)."""
+    bw = wl.BATCH_BY_NAME["batch64_bf16_512x512x512"]
+    A, B = wl.make_batch_inputs(bw)
+    assert A.shape == (bw.batch * bw.M, bw.K) and B.shape == (bw.batch * bw.K, bw.N)
+    A1, B1 = wl.make_inputs(bw.one())
+    assert np.array_equal(A[:bw.M], A1) and np.array_equal(B[:bw.K], B1)
+    assert not np.array_equal(A[:bw.M], A[bw.M:2 * bw.M])
+    vals = wl.decode(A[: 4 * bw.M], "bf16")
+    assert np.all(vals >= -1.0) and np.all(vals <= 1.0)
+    assert bw.flops == 2 * 64 * 512 ** 3

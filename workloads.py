@@ -122,6 +122,43 @@ TRANSPOSE_BY_NAME = {w.name: w for w in TRANSPOSE_WORKLOADS}
 HEADLINE = BY_NAME["bf16_4096x4096x4096_f32out"]
 
 
+@dataclass(frozen=True)
+class BatchWorkload:
+    """A strided batch of `batch` products of one shape ("矩阵乘法中的平铺",
+    closing advice on batched interfaces): matrix b of A is rows
+    [b M, (b + 1) M) of one (batch M) x K array, of B rows [b K, (b + 1) K) of
+    one (batch K) x N array, of C rows [b M, (b + 1) M) of (batch M) x N."""
+    name: str
+    batch: int
+    M: int
+    N: int
+    K: int
+    dtype: int
+    dist: str
+    seed_index: int
+
+    @property
+    def flops(self) -> int:
+        return 2 * self.batch * self.M * self.N * self.K
+
+    def one(self) -> Workload:
+        """One product of the batch, as a workload (for checks and samples)."""
+        return Workload(self.name + "_one", self.M, self.N, self.K, self.dtype, self.dist, self.seed_index)
+
+
+# 64 products of 512^3: each alone fills 4 of 76 CTA pairs; the batch fills them all
+BATCH_WORKLOADS = [BatchWorkload("batch64_bf16_512x512x512", 64, 512, 512, 512, BF16, "uniform", 9)]
+BATCH_BY_NAME = {w.name: w for w in BATCH_WORKLOADS}
+
+
+def make_batch_inputs(w: BatchWorkload):
+    """(A_bits, B_bits): (batch M) x K and (batch K) x N, each from one seeded stream."""
+    fmt = IN_FORMAT[w.dtype]
+    A = make_matrix(w.batch * w.M, w.K, fmt, w.dist, seed_for(w.seed_index, "A"), w.K, None)
+    B = make_matrix(w.batch * w.K, w.N, fmt, w.dist, seed_for(w.seed_index, "B"), w.K, None)
+    return A, B
+
+
 def seed_for(seed_index: int, which: str) -> int:
     return SEED_BASE + 16 * seed_index + (0 if which == "A" else 1)
 
