@@ -142,3 +142,31 @@ def test_many_small_products():
     M, N, K = 128, 256, 512
     plan, launches = run_batch(64, M, N, K, wl.BF16, M * K, K * N, M * N, seed=570)
     assert launches == 1 and plan.ctas == 2 * min(plan.dp_tiles, 76)
+
+
+def test_benchmark_batch_every_product():
+    """The benchmark's batch (64 products of bf16 512 x 512 x 512, inputs of
+    workloads.make_batch_inputs, one launch in the default plan): every element
+    of every product against the oracle."""
+    lib = H.tg()
+    dev = torch.device("cuda:0")
+    bw = wl.BATCH_BY_NAME["batch64_bf16_512x512x512"]
+    A, B = wl.make_batch_inputs(bw)
+    M, N, K, batch = bw.M, bw.N, bw.K, bw.batch
+    a = torch.from_numpy(A.view(np.int16)).to(dev)
+    b = torch.from_numpy(B.view(np.int16)).to(dev)
+    c = torch.zeros((batch * M, N), dtype=torch.int16, device=dev)
+    stream = torch.cuda.current_stream(dev).cuda_stream
+    st = lib.gemm_batched(batch, M, N, K, a.data_ptr(), K, M * K, b.data_ptr(), N, K * N, c.data_ptr(), N, M * N,
+                          bw.dtype, None, None, stream)
+    assert st == lib.OK, lib.status_string(st)
+    assert lib.device_status(stream) == lib.OK
+    pst, plan, launches = lib.plan_batched(batch, M, N, K, a.data_ptr(), K, M * K, b.data_ptr(), N, K * N,
+                                           c.data_ptr(), N, M * N, bw.dtype, None, 152)
+    assert pst == lib.OK and launches == 1
+    got_all = wl.decode(c.cpu().numpy().view(np.uint16), "bf16")
+    for bi in range(batch):
+        Ab, Bb = A[bi * M:(bi + 1) * M], B[bi * K:(bi + 1) * K]
+        D, S = oracle.gemm(np.ascontiguousarray(Ab), np.ascontiguousarray(Bb), "bf16", M, N, K)
+        ok, ratio, where = tolerance.check(got_all[bi * M:(bi + 1) * M], D, S, "bf16", "bf16")
+        assert ok, f"product {bi}: error/bound {ratio:.3g} at {where}"
